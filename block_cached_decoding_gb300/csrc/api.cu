@@ -1,0 +1,331 @@
+// Host side of the C ABI declared in include/fdllm.h: argument validation,
+// workspace layout, dispatch to the kernels, status codes and error messages.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fdllm {
+
+// Per-device error word for bounded device waits (see fdllm_last_device_error).
+__device__ int32_t g_device_error_word = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+fdllm_status fail(fdllm_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+fdllm_status cuda_status(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return FDLLM_OK;
+  return fail(FDLLM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+
+int32_t *error_word_ptr() {
+  static int32_t *ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = (int32_t *)p;
+  }
+  return ptrs[dev];
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------------------
+// attention
+// ----------------------------------------------------------------------------
+fdllm_status resolve_attn(const fdllm_attn_desc *d, AttnProblem &p) {
+  if (!d) return fail(FDLLM_EINVAL, "attn: null descriptor");
+  if (d->batch < 1) return fail(FDLLM_EINVAL, "attn: batch must be >= 1 (got %d)", d->batch);
+  if (d->prompt_len < 0) return fail(FDLLM_EINVAL, "attn: prompt_len < 0");
+  if (d->block_size < 1) return fail(FDLLM_EINVAL, "attn: block_size must be >= 1");
+  if (d->gen_length < d->block_size || d->gen_length % d->block_size != 0)
+    return fail(FDLLM_EINVAL, "attn: gen_length (%d) must be a positive multiple of block_size (%d)",
+                d->gen_length, d->block_size);
+  const int nblocks = d->gen_length / d->block_size;
+  if (d->block_idx < 0 || d->block_idx >= nblocks)
+    return fail(FDLLM_EINVAL, "attn: block_idx %d outside [0, %d)", d->block_idx, nblocks);
+  if (d->n_kv_heads < 1 || d->n_q_heads < 1 || d->n_q_heads % d->n_kv_heads != 0)
+    return fail(FDLLM_EINVAL, "attn: n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)",
+                d->n_q_heads, d->n_kv_heads);
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(FDLLM_EINVAL, "attn: head_dim must be 64 or 128 (got %d)", d->head_dim);
+  if (d->use_cache != 0 && d->use_cache != 1) return fail(FDLLM_EINVAL, "attn: use_cache must be 0 or 1");
+  if (d->dual_cache != 0 && d->dual_cache != 1) return fail(FDLLM_EINVAL, "attn: dual_cache must be 0 or 1");
+  if (d->dtype != FDLLM_BF16 && d->dtype != FDLLM_F32) return fail(FDLLM_EINVAL, "attn: bad dtype %d", d->dtype);
+  if (d->out_f32 != 0 && d->out_f32 != 1) return fail(FDLLM_EINVAL, "attn: out_f32 must be 0 or 1");
+  if (!(d->sm_scale >= 0.f) || isinf(d->sm_scale)) return fail(FDLLM_EINVAL, "attn: sm_scale must be finite and >= 0");
+  const int64_t n = (int64_t)d->prompt_len + d->gen_length;
+  if (n > (1 << 24)) return fail(FDLLM_EINVAL, "attn: sequence too long");
+  const int s = d->prompt_len + d->block_idx * d->block_size;
+  p.batch = d->batch;
+  p.seq_len = (int)n;
+  p.hq = d->n_q_heads;
+  p.hkv = d->n_kv_heads;
+  p.d = d->head_dim;
+  if (!d->use_cache) {
+    p.fresh0 = 0;
+    p.nq = (int)n;
+  } else if (d->dual_cache) {
+    p.fresh0 = s;
+    p.nq = d->block_size;
+  } else {
+    p.fresh0 = s;
+    p.nq = (int)n - s;
+  }
+  p.scale = d->sm_scale > 0.f ? d->sm_scale : (float)(1.0 / sqrt((double)d->head_dim));
+  p.in_bf16 = d->dtype == FDLLM_BF16;
+  p.out_f32 = d->out_f32;
+  return FDLLM_OK;
+}
+
+}  // namespace
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int sm_count() {
+  static int counts[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  if (!counts[dev]) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = c > 0 ? c : 1;
+  }
+  return counts[dev];
+}
+
+namespace {
+
+// ----------------------------------------------------------------------------
+// select
+// ----------------------------------------------------------------------------
+fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
+  if (!d) return fail(FDLLM_EINVAL, "select: null descriptor");
+  if (d->batch < 1) return fail(FDLLM_EINVAL, "select: batch must be >= 1");
+  if (d->block_size < 1 || d->block_size > 256)
+    return fail(FDLLM_EINVAL, "select: block_size must be in [1, 256] (got %d)", d->block_size);
+  if (d->block_start < 0 || d->seq_len < 1 || (int64_t)d->block_start + d->block_size > d->seq_len)
+    return fail(FDLLM_EINVAL, "select: block [%d, %d) outside the sequence of length %d", d->block_start,
+                d->block_start + d->block_size, d->seq_len);
+  if (d->hidden < 64 || d->hidden % 64 != 0)
+    return fail(FDLLM_EINVAL, "select: hidden must be a positive multiple of 64 (got %d)", d->hidden);
+  if (d->vocab < 2) return fail(FDLLM_EINVAL, "select: vocab must be >= 2");
+  if ((int64_t)d->batch * d->block_size > 2048)
+    return fail(FDLLM_EINVAL, "select: batch * block_size must be <= 2048");
+  if (d->mask_id >= 0 && d->mask_id < d->vocab)
+    return fail(FDLLM_EINVAL, "select: mask_id %d is a vocabulary id; it must lie outside [0, vocab)", d->mask_id);
+  if (d->dtype != FDLLM_BF16 && d->dtype != FDLLM_F32) return fail(FDLLM_EINVAL, "select: bad dtype %d", d->dtype);
+  switch (d->strategy) {
+    case FDLLM_SELECT_THRESHOLD:
+      if (isnan(d->threshold)) return fail(FDLLM_EINVAL, "select: threshold is NaN");
+      break;
+    case FDLLM_SELECT_FACTOR:
+      if (!(d->factor > 0.f)) return fail(FDLLM_EINVAL, "select: factor must be > 0");
+      break;
+    case FDLLM_SELECT_TOPK:
+      if (d->topk < 1) return fail(FDLLM_EINVAL, "select: topk must be >= 1");
+      break;
+    default:
+      return fail(FDLLM_EINVAL, "select: unknown strategy %d", d->strategy);
+  }
+  p.batch = d->batch;
+  p.seq_len = d->seq_len;
+  p.s = d->block_start;
+  p.B = d->block_size;
+  p.H = d->hidden;
+  p.V = d->vocab;
+  p.mask_id = d->mask_id;
+  p.strategy = d->strategy;
+  p.topk = d->topk;
+  p.factor = d->factor;
+  const double tau = d->threshold;
+  // c > tau  <=>  log((1 - c) / c) < log((1 - tau) / tau)
+  p.kappa_tau = tau >= 1.0 ? -INFINITY : (tau <= 0.0 ? INFINITY : (float)log((1.0 - tau) / tau));
+  p.in_bf16 = d->dtype == FDLLM_BF16;
+  return FDLLM_OK;
+}
+
+// workspace: partials VocabStat [b * B, splits] (16 bytes each); the tensor-core
+// kernel serves bf16 blocks of up to 512 rows, the CUDA-core kernel the rest
+struct SelectLayout {
+  size_t total;
+  int splits;
+  bool tc;
+};
+
+SelectLayout select_layout(const SelectProblem &p) {
+  SelectLayout L;
+  L.tc = lmhead_tc_supported(p);
+  L.splits = L.tc ? lmhead_tc_grid(p) : lmhead_simt_splits(p);
+  L.total = align_up((size_t)p.batch * p.B * L.splits * sizeof(VocabStat), 256);
+  return L;
+}
+
+}  // namespace
+}  // namespace fdllm
+
+using namespace fdllm;
+
+extern "C" {
+
+int32_t fdllm_version(void) { return 100; }
+
+uint64_t fdllm_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *fdllm_status_string(int32_t s) {
+  switch (s) {
+    case FDLLM_OK: return "FDLLM_OK: success";
+    case FDLLM_EINVAL: return "FDLLM_EINVAL: invalid argument";
+    case FDLLM_ECUDA: return "FDLLM_ECUDA: CUDA runtime error";
+    case FDLLM_ETIMEOUT: return "FDLLM_ETIMEOUT: a bounded device wait expired";
+    case FDLLM_EUNSUPPORTED: return "FDLLM_EUNSUPPORTED: not supported by this build";
+    default: return "unknown fdllm status";
+  }
+}
+
+const char *fdllm_last_error(void) { return t_last_error.c_str(); }
+
+fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail) {
+  fdllm_status st = cuda_status(cudaStreamSynchronize((cudaStream_t)stream), "stream synchronize");
+  if (st != FDLLM_OK) return st;
+  int32_t *w = error_word_ptr();
+  if (!w) return fail(FDLLM_ECUDA, "device error word unavailable");
+  int32_t v = 0;
+  st = cuda_status(cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost), "read device error word");
+  if (st != FDLLM_OK) return st;
+  if (v != 0) {
+    const int32_t zero = 0;
+    st = cuda_status(cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice), "clear device error word");
+    if (st != FDLLM_OK) return st;
+  }
+  if (detail) *detail = v;
+  return v ? fail(FDLLM_ETIMEOUT, "device wait gave up at site %d", v) : FDLLM_OK;
+}
+
+int64_t fdllm_attn_query_count(const fdllm_attn_desc *desc) {
+  AttnProblem p;
+  if (resolve_attn(desc, p) != FDLLM_OK) return -1;
+  return p.nq;
+}
+
+static size_t attn_workspace(const AttnProblem &p) {
+  return attn_tc_supported(p) ? attn_tc_workspace(p) : attn_simt_workspace(p);
+}
+
+size_t fdllm_attn_workspace_size(const fdllm_attn_desc *desc) {
+  AttnProblem p;
+  if (resolve_attn(desc, p) != FDLLM_OK) return 0;
+  return attn_workspace(p);
+}
+
+fdllm_status fdllm_block_attn(const fdllm_attn_desc *desc, const void *q, const void *k_cache,
+                              const void *v_cache, const void *k_fresh, const void *v_fresh,
+                              void *out, float *lse, void *workspace, size_t ws_bytes,
+                              fdllm_stream_t stream) {
+  AttnProblem p;
+  fdllm_status st = resolve_attn(desc, p);
+  if (st != FDLLM_OK) return st;
+  const void *req[] = {q, k_cache, v_cache, k_fresh, v_fresh, out};
+  const char *names[] = {"q", "k_cache", "v_cache", "k_fresh", "v_fresh", "out"};
+  for (int i = 0; i < 6; ++i) {
+    if (!req[i]) return fail(FDLLM_EINVAL, "attn: %s is null", names[i]);
+    if (!aligned16(req[i])) return fail(FDLLM_EINVAL, "attn: %s is not 16-byte aligned", names[i]);
+  }
+  const size_t need = attn_workspace(p);
+  if (ws_bytes < need || (need && !workspace))
+    return fail(FDLLM_EINVAL, "attn: workspace of %zu bytes is smaller than the %zu required", ws_bytes, need);
+  p.q = q; p.kc = k_cache; p.vc = v_cache; p.kf = k_fresh; p.vf = v_fresh;
+  if (workspace && !aligned16(workspace)) return fail(FDLLM_EINVAL, "attn: workspace must be 16-byte aligned");
+  p.out = out; p.lse = lse; p.ws = workspace; p.ws_bytes = ws_bytes;
+  p.err = error_word_ptr();
+  cudaStream_t cs = (cudaStream_t)stream;
+  return cuda_status(attn_tc_supported(p) ? launch_attn_tc(p, cs) : launch_attn_simt(p, cs), "attn launch");
+}
+
+size_t fdllm_select_workspace_size(const fdllm_select_desc *desc) {
+  SelectProblem p;
+  if (resolve_select(desc, p) != FDLLM_OK) return 0;
+  return select_layout(p).total;
+}
+
+fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *hidden,
+                                     const void *lm_head_w, int32_t *tokens, uint8_t *unmasked,
+                                     float *conf, float *kappa, int32_t *argmax,
+                                     int32_t *n_masked_left, void *workspace, size_t ws_bytes,
+                                     fdllm_stream_t stream) {
+  SelectProblem p;
+  fdllm_status st = resolve_select(desc, p);
+  if (st != FDLLM_OK) return st;
+  const void *req[] = {hidden, lm_head_w, tokens, unmasked, conf, argmax, n_masked_left, workspace};
+  const char *names[] = {"hidden", "lm_head_w", "tokens", "unmasked", "conf", "argmax", "n_masked_left", "workspace"};
+  for (int i = 0; i < 8; ++i)
+    if (!req[i]) return fail(FDLLM_EINVAL, "select: %s is null", names[i]);
+  if (!aligned16(hidden) || !aligned16(lm_head_w))
+    return fail(FDLLM_EINVAL, "select: hidden and lm_head_w must be 16-byte aligned");
+  if (!aligned16(workspace)) return fail(FDLLM_EINVAL, "select: workspace must be 16-byte aligned");
+  const SelectLayout L = select_layout(p);
+  if (ws_bytes < L.total)
+    return fail(FDLLM_EINVAL, "select: workspace of %zu bytes is smaller than the %zu required", ws_bytes, L.total);
+  p.hidden = hidden; p.w = lm_head_w; p.tokens = tokens; p.unmasked = unmasked; p.conf = conf;
+  p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
+  p.err = error_word_ptr();
+  VocabStat *part = (VocabStat *)workspace;
+  cudaStream_t cs = (cudaStream_t)stream;
+  st = cuda_status(L.tc ? launch_lmhead_tc(p, part, L.splits, cs) : launch_lmhead_simt(p, part, L.splits, cs),
+                   "lm-head launch");
+  if (st != FDLLM_OK) return st;
+  return cuda_status(launch_select(p, part, L.splits, cs), "select launch");
+}
+
+fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
+                             int32_t head_dim, int32_t start, int32_t len, int32_t dtype,
+                             void *k_cache, void *v_cache, const void *k_src, const void *v_src,
+                             fdllm_stream_t stream) {
+  if (mode != FDLLM_SPLICE_WINDOW && mode != FDLLM_SPLICE_REFRESH)
+    return fail(FDLLM_EINVAL, "splice: unknown mode %d", mode);
+  if (batch < 1 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1)
+    return fail(FDLLM_EINVAL, "splice: batch, seq_len, n_kv_heads and head_dim must be >= 1");
+  if (dtype != FDLLM_BF16 && dtype != FDLLM_F32) return fail(FDLLM_EINVAL, "splice: bad dtype %d", dtype);
+  if (start < 0 || len < 0 || (int64_t)start + len > seq_len)
+    return fail(FDLLM_EINVAL, "splice: window [%d, %d) outside [0, %d)", start, start + len, seq_len);
+  if (mode == FDLLM_SPLICE_REFRESH && (start != 0 || len != seq_len))
+    return fail(FDLLM_EINVAL, "splice: REFRESH rewrites the whole cache (start 0, len seq_len)");
+  const int64_t row_bytes = (int64_t)n_kv_heads * head_dim * (dtype == FDLLM_BF16 ? 2 : 4);
+  if (row_bytes % 16 != 0) return fail(FDLLM_EINVAL, "splice: Hkv * d * element size must be a multiple of 16 bytes");
+  const void *ptrs[] = {k_cache, v_cache, k_src, v_src};
+  for (int i = 0; i < 4; ++i) {
+    if (!ptrs[i]) return fail(FDLLM_EINVAL, "splice: null pointer");
+    if (!aligned16(ptrs[i])) return fail(FDLLM_EINVAL, "splice: pointers must be 16-byte aligned");
+  }
+  return cuda_status(launch_splice(batch, seq_len, row_bytes, start, len, k_cache, v_cache, k_src,
+                                   v_src, (cudaStream_t)stream),
+                     "splice launch");
+}
+
+}  // extern "C"

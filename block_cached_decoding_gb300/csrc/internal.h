@@ -1,0 +1,74 @@
+// Launchers shared between the host ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fdllm.h"
+
+namespace fdllm {
+
+struct VocabStat;  // common.cuh
+
+// Resolved attention problem (validated by api.cu).
+struct AttnProblem {
+  int batch, seq_len, nq, hq, hkv, d;
+  int fresh0;       // first position with fresh K/V (== first query position)
+  float scale;      // softmax scale
+  int in_bf16;      // q / k / v storage
+  int out_f32;
+  const void *q, *kc, *vc, *kf, *vf;
+  void *out;
+  float *lse;
+  void *ws;
+  size_t ws_bytes;
+  int32_t *err;
+};
+
+// Resolved select problem.
+struct SelectProblem {
+  int batch, seq_len, s, B, H, V, mask_id, strategy, topk;
+  float kappa_tau;  // c > tau  <=>  kappa < kappa_tau
+  float factor;
+  int in_bf16;
+  const void *hidden, *w;
+  int32_t *tokens;
+  uint8_t *unmasked;
+  float *conf, *kappa;
+  int32_t *argmax, *n_left;
+  void *ws;
+  size_t ws_bytes;
+  int32_t *err;
+};
+
+int sm_count();  // SMs of the current device (cached per device)
+void count_launches(int n);  // adds to fdllm_launch_counter()
+
+// attn_simt.cu
+size_t attn_simt_workspace(const AttnProblem &p);
+cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t st);
+
+// attn_tc.cu: tcgen05 block attention (bf16, head_dim 64 / 128)
+bool attn_tc_supported(const AttnProblem &p);
+size_t attn_tc_workspace(const AttnProblem &p);
+cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st);
+
+// lmhead_simt.cu: per-split vocabulary partials for the masked rows
+int lmhead_simt_splits(const SelectProblem &p);
+cudaError_t launch_lmhead_simt(const SelectProblem &p, VocabStat *part, int splits, cudaStream_t st);
+
+// lmhead_tc.cu: the same partials from the tcgen05 kernel (bf16, batch * B <= 512)
+bool lmhead_tc_supported(const SelectProblem &p);
+int lmhead_tc_grid(const SelectProblem &p);
+cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, int grid, cudaStream_t st);
+
+// select.cu: merge partials [b * B, splits] over splits and unmask
+cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st);
+
+// splice.cu
+cudaError_t launch_splice(int batch, int64_t cache_rows, int64_t row_bytes, int64_t start,
+                          int64_t len, void *kc, void *vc, const void *ks, const void *vs,
+                          cudaStream_t st);
+
+}  // namespace fdllm

@@ -1,0 +1,312 @@
+// LM head + online vocabulary reduction on the 5th-generation tensor cores.
+//
+// logits = h W^T for the block rows (b * B <= 512), never stored: each CTA owns
+// a contiguous range of the vocabulary in units of 64 rows of W and streams
+// them through shared memory once.  Per CTA (one per SM, 256 threads):
+//   warp 0  TMA producer: W tiles (64-row boxes, 128-byte swizzle, L2
+//           evict-first) and the hidden-row tiles (128-row boxes) per 64-wide
+//           K chunk, into an S-stage ring guarded by full/empty mbarriers
+//   warp 1  TMEM owner and MMA issuer: tcgen05.mma M=128 (block rows) x
+//           N=64..256 (vocabulary) x K=16, fp32 accumulator in TMEM, double
+//           buffered so the epilogue of tile t overlaps the MMAs of tile t+1
+//   warps 4-7 epilogue: tcgen05.ld of the accumulator (one thread per block
+//           row), folded into the row's VocabStat in increasing vocabulary order
+// At the end every masked row writes its VocabStat for this CTA's range to the
+// partials [b * B, grid]; the select kernel merges them.
+//
+// Template MT = 128-row tiles of block rows (1, 2 or 4): the vocabulary tile is
+// NV = 256 / MT rows so that 2 x MT x NV = 512 TMEM columns.  Rows of a tile
+// with no masked position are neither loaded nor multiplied.
+//
+// Every mbarrier wait is bounded; a wait that gives up records a site code in
+// the device error word, the CTA stops issuing work, waits (bounded) for the
+// copies and MMAs it already issued, frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace fdllm {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnit = 64;        // vocabulary rows per W box
+constexpr int kKChunk = 64;      // K elements per stage (one 128-byte swizzle atom)
+constexpr int kABox = 128;       // block rows per hidden-tile box
+
+template <int MT>
+struct Cfg {
+  static constexpr int NV = 256 / MT;                       // vocabulary rows per tile
+  static constexpr int UNITS = NV / kUnit;                  // W boxes per tile
+  static constexpr int A_BYTES = MT * kABox * kKChunk * 2;  // hidden tiles per stage
+  static constexpr int W_BYTES = NV * kKChunk * 2;          // W tile per stage
+  static constexpr int STAGE = A_BYTES + W_BYTES;
+  static constexpr int STAGES = MT == 4 ? 3 : 4;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, flags*/;
+};
+
+struct Shared {
+  uint64_t full[4];
+  uint64_t empty[4];
+  uint64_t accf[2];
+  uint64_t acce[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t issued;     // stages issued by the producer
+  int32_t consumed;   // stages consumed by the MMA issuer
+  uint32_t active;    // bit m: 128-row tile m has a masked row
+  uint8_t masked[512];
+};
+
+__device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site) {
+  record_device_error(err, site);
+  atomicExch(&sh.abort, 1);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                     const int32_t *__restrict__ tokens, int batch, int seq_len, int s, int B, int mask_id, int H,
+                     int V, VocabStat *__restrict__ part, int32_t *err) {
+  using C = Cfg<MT>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *tiles = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Shared &sh = *(Shared *)(tiles + C::STAGES * C::STAGE);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = batch * B;
+  const int G = gridDim.x, g = blockIdx.x;
+
+  // vocabulary units [u0, u1) of this CTA
+  const int units = (V + kUnit - 1) / kUnit;
+  const int u0 = (int)((int64_t)units * g / G), u1 = (int)((int64_t)units * (g + 1) / G);
+  const int ntiles = (u1 - u0 + C::UNITS - 1) / C::UNITS;
+  const int kchunks = H / kKChunk;
+
+  // masked block rows (same on every CTA)
+  if (threadIdx.x == 0) { sh.abort = 0; sh.issued = 0; sh.consumed = 0; sh.active = 0; }
+  __syncthreads();
+  for (int r = threadIdx.x; r < MT * kABox; r += kThreads) {
+    bool m = false;
+    if (r < rows) {
+      const int bb = r / B, i = r - bb * B;
+      m = tokens[(int64_t)bb * seq_len + s + i] == mask_id;
+    }
+    sh.masked[r] = m;
+    if (m) atomicOr(&sh.active, 1u << (r / kABox));
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      tc::mbar_init(&sh.full[i], 1);
+      tc::mbar_init(&sh.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sh.accf[i], 1);
+      tc::mbar_init(&sh.acce[i], 4);
+    }
+    tc::mbar_init(&sh.drain, 1);
+    tc::fence_barrier_init();
+    tc::prefetch_tensormap(&map_h);
+    tc::prefetch_tensormap(&map_w);
+  }
+  if (warp == 1) tc::tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t active = sh.active;
+  const uint32_t tmem = sh.tmem_base;
+  int nact = 0;
+#pragma unroll
+  for (int m = 0; m < MT; ++m) nact += (active >> m) & 1;
+
+  if (active != 0 && ntiles > 0) {
+    if (warp == 0) {
+      // ---------------- TMA producer ----------------
+      if (lane == 0) {
+        const uint64_t pol_w = tc::policy_evict_first();
+        const uint64_t pol_h = tc::policy_evict_last();
+        int it = 0;
+        for (int t = 0; t < ntiles && !sh.abort; ++t) {
+          const int tu0 = u0 + t * C::UNITS;
+          const int nu = min(C::UNITS, u1 - tu0);
+          const uint32_t bytes = (uint32_t)(nact * kABox * kKChunk * 2 + nu * kUnit * kKChunk * 2);
+          for (int kc = 0; kc < kchunks; ++kc, ++it) {
+            const int st = it % C::STAGES;
+            const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+            if (!tc::mbar_wait(&sh.empty[st], ph ^ 1u)) { set_abort(sh, err, 101); break; }
+            unsigned char *a = tiles + st * C::STAGE;
+            unsigned char *w = a + C::A_BYTES;
+            tc::mbar_arrive_expect_tx(&sh.full[st], bytes);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+              if ((active >> m) & 1)
+                tc::tma_load_2d(a + m * kABox * kKChunk * 2, &map_h, &sh.full[st], kc * kKChunk, m * kABox, pol_h);
+            for (int u = 0; u < nu; ++u)
+              tc::tma_load_2d(w + u * kUnit * kKChunk * 2, &map_w, &sh.full[st], kc * kKChunk, (tu0 + u) * kUnit,
+                              pol_w);
+            atomicExch(&sh.issued, it + 1);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------- MMA issuer ----------------
+      if (lane == 0) {
+        int it = 0;
+        for (int t = 0; t < ntiles && !sh.abort; ++t) {
+          const int tu0 = u0 + t * C::UNITS;
+          const int nu = min(C::UNITS, u1 - tu0);
+          const uint32_t idesc = tc::idesc_bf16_f32(128, (uint32_t)(nu * kUnit));
+          const int j = t & 1;
+          if (!tc::mbar_wait(&sh.acce[j], ((uint32_t)(t >> 1) & 1u) ^ 1u)) { set_abort(sh, err, 102); break; }
+          tc::fence_after_sync();
+          bool ok = true;
+          for (int kc = 0; kc < kchunks; ++kc, ++it) {
+            const int st = it % C::STAGES;
+            const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+            if (!tc::mbar_wait(&sh.full[st], ph)) { set_abort(sh, err, 103); ok = false; break; }
+            tc::fence_after_sync();
+            const uint32_t a = tc::smem_u32(tiles + st * C::STAGE);
+            const uint32_t w = a + C::A_BYTES;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              if (!((active >> m) & 1)) continue;
+              const uint32_t d = tmem + (uint32_t)(j * MT * C::NV + m * C::NV);
+#pragma unroll
+              for (int kk = 0; kk < kKChunk / 16; ++kk)
+                tc::mma_bf16(d, tc::sw128_desc(a + m * kABox * kKChunk * 2 + kk * 32), tc::sw128_desc(w + kk * 32),
+                             idesc, (kc | kk) != 0);
+            }
+            tc::mma_commit(&sh.empty[st]);
+            atomicExch(&sh.consumed, it + 1);
+          }
+          if (!ok) break;
+          tc::mma_commit(&sh.accf[j]);
+        }
+        // every MMA this thread issued has completed once `drain` fires
+        tc::mma_commit(&sh.drain);
+        if (!tc::mbar_wait(&sh.drain, 0)) record_device_error(err, 104);
+      }
+    } else if (warp >= 4) {
+      // ---------------- epilogue ----------------
+      const int q = warp - 4;  // TMEM lane quadrant of this warp
+      VocabStat st[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) st[m] = vs_identity();
+      bool ok = true;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const int tu0 = u0 + t * C::UNITS;
+        const int ncol = min(C::UNITS, u1 - tu0) * kUnit;
+        const int v0 = tu0 * kUnit;
+        const int j = t & 1;
+        if (!tc::mbar_wait(&sh.accf[j], (uint32_t)(t >> 1) & 1u)) { set_abort(sh, err, 105); ok = false; break; }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (!((active >> m) & 1)) continue;
+          const int row = m * kABox + q * 32 + lane;
+          const bool valid = sh.masked[row] != 0;
+          if (__ballot_sync(0xffffffffu, valid) == 0u) continue;
+          const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * MT * C::NV + m * C::NV);
+          for (int c0 = 0; c0 < ncol; c0 += 32) {
+            uint32_t r[32];
+            tc::tmem_ld_32x32b_x32(base + (uint32_t)c0, r);
+            tc::tmem_ld_wait();
+            if (valid) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int v = v0 + c0 + e;
+                if (v < V) vs_push(st[m], __uint_as_float(r[e]), v);
+              }
+            }
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.acce[j]);
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) {
+        const int row = m * kABox + q * 32 + lane;
+        if (((active >> m) & 1) && row < rows && sh.masked[row]) part[(int64_t)row * G + g] = st[m];
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (sh.abort && threadIdx.x == 0) {
+    // copies issued but never consumed still land in this CTA's shared memory: wait for them
+    for (int it = sh.consumed; it < sh.issued; ++it)
+      tc::mbar_wait(&sh.full[it % C::STAGES], (uint32_t)(it / C::STAGES) & 1u);
+  }
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] as a 2-D map with box [box_cols, box_rows], 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kKChunk, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MT>
+cudaError_t launch_mt(const SelectProblem &p, VocabStat *part, int grid, cudaStream_t st) {
+  CUtensorMap mh, mw;
+  if (!make_map(&mh, p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H, kABox) ||
+      !make_map(&mw, p.w, (uint64_t)p.V, (uint64_t)p.H, kUnit))
+    return cudaErrorInvalidValue;
+  auto k = lmhead_tc_kernel<MT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, Cfg<MT>::SMEM, st>>>(mh, mw, p.tokens, p.batch, p.seq_len, p.s, p.B, p.mask_id, p.H, p.V,
+                                          part, p.err);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool lmhead_tc_supported(const SelectProblem &p) {
+  return p.in_bf16 && (int64_t)p.batch * p.B <= 512 && p.H % kKChunk == 0;
+}
+
+int lmhead_tc_grid(const SelectProblem &p) {
+  const int units = (p.V + kUnit - 1) / kUnit;
+  const int sms = sm_count();
+  return units < sms ? units : sms;
+}
+
+cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, int grid, cudaStream_t st) {
+  const int rows = p.batch * p.B;
+  if (rows <= 128) return launch_mt<1>(p, part, grid, st);
+  if (rows <= 256) return launch_mt<2>(p, part, grid, st);
+  return launch_mt<4>(p, part, grid, st);
+}
+
+}  // namespace fdllm

@@ -1,0 +1,44 @@
+// KV cache splice / refresh: cache[:, start : start + len] <- src for K and V.
+// Pure data movement, bound by HBM bandwidth: 16-byte vector copies over a
+// grid sized to the SM count, both tensors in one launch.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fdllm {
+
+__global__ void __launch_bounds__(256) splice_kernel(int batch, int64_t cache_vecs_per_b,
+                                                      int64_t start_vec, int64_t len_vecs,
+                                                      uint4 *__restrict__ kc, uint4 *__restrict__ vc,
+                                                      const uint4 *__restrict__ ks,
+                                                      const uint4 *__restrict__ vs) {
+  const int64_t per_tensor = (int64_t)batch * len_vecs;
+  const int64_t total = 2 * per_tensor;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const bool is_v = i >= per_tensor;
+    const int64_t j = is_v ? i - per_tensor : i;
+    const int64_t b = j / len_vecs;
+    const int64_t r = j - b * len_vecs;
+    const uint4 x = __ldcs((is_v ? vs : ks) + j);  // streamed once
+    uint4 *dst = (is_v ? vc : kc) + b * cache_vecs_per_b + start_vec + r;
+    *dst = x;
+  }
+}
+
+cudaError_t launch_splice(int batch, int64_t cache_rows, int64_t row_bytes, int64_t start,
+                          int64_t len, void *kc, void *vc, const void *ks, const void *vs,
+                          cudaStream_t st) {
+  const int64_t rv = row_bytes / 16;
+  const int64_t total = 2 * (int64_t)batch * len * rv;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  splice_kernel<<<(unsigned)blocks, 256, 0, st>>>(batch, cache_rows * rv, start * rv, len * rv,
+                                                  (uint4 *)kc, (uint4 *)vc, (const uint4 *)ks,
+                                                  (const uint4 *)vs);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace fdllm

@@ -1,0 +1,219 @@
+"""ctypes binding of libfdllm.so (include/fdllm.h, include/fdllm_synth.h).
+
+Argument marshalling only: each function takes torch tensors (or raw device
+addresses as ints) and forwards their addresses, sizes and the CUDA stream to
+the C ABI of the same name; every step of the computation runs in the CUDA
+library.  Loading fails loudly if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfdllm.so")
+
+OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED = range(5)
+BF16, F32 = 0, 1
+SELECT_THRESHOLD, SELECT_FACTOR, SELECT_TOPK = 0, 1, 2
+SPLICE_WINDOW, SPLICE_REFRESH = 0, 1
+SYNTH_W, SYNTH_KCACHE, SYNTH_VCACHE, SYNTH_Q, SYNTH_KFRESH, SYNTH_VFRESH, SYNTH_HID, SYNTH_PLANT, SYNTH_PROMPT = range(1, 10)
+
+EXPORTS = (
+    "fdllm_attn_query_count", "fdllm_attn_workspace_size", "fdllm_block_attn",
+    "fdllm_select_workspace_size", "fdllm_confidence_select", "fdllm_kv_splice",
+    "fdllm_status_string", "fdllm_last_error", "fdllm_last_device_error", "fdllm_version",
+    "fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
+    "fdllm_synth_prompt", "fdllm_launch_counter",
+)
+
+
+class FdllmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class AttnDesc(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("prompt_len", C.c_int32), ("gen_length", C.c_int32),
+                ("block_size", C.c_int32), ("block_idx", C.c_int32), ("n_q_heads", C.c_int32),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("use_cache", C.c_int32),
+                ("dual_cache", C.c_int32), ("sm_scale", C.c_float), ("dtype", C.c_int32),
+                ("out_f32", C.c_int32)]
+
+
+class SelectDesc(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("seq_len", C.c_int32), ("block_start", C.c_int32),
+                ("block_size", C.c_int32), ("hidden", C.c_int32), ("vocab", C.c_int32),
+                ("mask_id", C.c_int32), ("strategy", C.c_int32), ("threshold", C.c_float),
+                ("factor", C.c_float), ("topk", C.c_int32), ("dtype", C.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library; raises if it is missing (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+        L.fdllm_attn_query_count.argtypes = [C.POINTER(AttnDesc)]
+        L.fdllm_attn_query_count.restype = i64
+        L.fdllm_attn_workspace_size.argtypes = [C.POINTER(AttnDesc)]
+        L.fdllm_attn_workspace_size.restype = sz
+        L.fdllm_block_attn.argtypes = [C.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.fdllm_block_attn.restype = i32
+        L.fdllm_select_workspace_size.argtypes = [C.POINTER(SelectDesc)]
+        L.fdllm_select_workspace_size.restype = sz
+        L.fdllm_confidence_select.argtypes = [C.POINTER(SelectDesc)] + [vp] * 9 + [sz, vp]
+        L.fdllm_confidence_select.restype = i32
+        L.fdllm_kv_splice.argtypes = [i32] * 8 + [vp] * 5
+        L.fdllm_kv_splice.restype = i32
+        L.fdllm_status_string.argtypes = [i32]
+        L.fdllm_status_string.restype = C.c_char_p
+        L.fdllm_last_error.argtypes = []
+        L.fdllm_last_error.restype = C.c_char_p
+        L.fdllm_last_device_error.argtypes = [vp, C.POINTER(i32)]
+        L.fdllm_last_device_error.restype = i32
+        L.fdllm_version.argtypes = []
+        L.fdllm_version.restype = i32
+        L.fdllm_launch_counter.argtypes = []
+        L.fdllm_launch_counter.restype = C.c_uint64
+        u64 = C.c_uint64
+        L.fdllm_synth_normals.argtypes = [u64, i32, C.POINTER(i64), i32, i64, i64, C.c_float, i32, vp, vp]
+        L.fdllm_synth_kv_cache.argtypes = [u64, i32, i32, i32, i32, i32, i64, C.c_float, i32, vp, vp]
+        L.fdllm_synth_rows.argtypes = [u64, i32, i32, i64, i32, i32, i32, C.c_float, i32, vp, vp]
+        L.fdllm_synth_hidden.argtypes = [u64, i32, i64, i32, i32, i32, i32, C.c_double, vp, i32, vp, vp]
+        L.fdllm_synth_prompt.argtypes = [u64, i32, i32, i32, vp, vp]
+        for f in ("fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
+                  "fdllm_synth_prompt"):
+            getattr(L, f).restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int):
+    if st != OK:
+        msg = lib().fdllm_last_error().decode(errors="replace")
+        raise FdllmError(st, msg or lib().fdllm_status_string(st).decode())
+
+
+def dtype_code(t) -> int:
+    import torch
+    return {torch.bfloat16: BF16, torch.float32: F32}[t.dtype]
+
+
+# ---------------------------------------------------------------------------
+# hot path
+# ---------------------------------------------------------------------------
+
+def attn_desc(*, batch, prompt_len, gen_length, block_size, block_idx, n_q_heads, n_kv_heads, head_dim,
+              use_cache=1, dual_cache=1, sm_scale=0.0, dtype=BF16, out_f32=1) -> AttnDesc:
+    return AttnDesc(batch, prompt_len, gen_length, block_size, block_idx, n_q_heads, n_kv_heads, head_dim,
+                    use_cache, dual_cache, sm_scale, dtype, out_f32)
+
+
+def select_desc(*, batch, seq_len, block_start, block_size, hidden, vocab, mask_id, threshold=0.9,
+                strategy=SELECT_THRESHOLD, factor=1.0, topk=1, dtype=BF16) -> SelectDesc:
+    return SelectDesc(batch, seq_len, block_start, block_size, hidden, vocab, mask_id, strategy, threshold,
+                      factor, topk, dtype)
+
+
+def fdllm_attn_query_count(desc: AttnDesc) -> int:
+    return lib().fdllm_attn_query_count(C.byref(desc))
+
+
+def fdllm_attn_workspace_size(desc: AttnDesc) -> int:
+    return lib().fdllm_attn_workspace_size(C.byref(desc))
+
+
+def fdllm_block_attn(desc, q, k_cache, v_cache, k_fresh, v_fresh, out, lse=None, workspace=None,
+                     ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_block_attn(C.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_fresh),
+                                  _ptr(v_fresh), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
+                                  _stream(stream)))
+
+
+def fdllm_select_workspace_size(desc: SelectDesc) -> int:
+    return lib().fdllm_select_workspace_size(C.byref(desc))
+
+
+def fdllm_confidence_select(desc, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax, n_masked_left,
+                            workspace, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_confidence_select(C.byref(desc), _ptr(hidden), _ptr(lm_head_w), _ptr(tokens),
+                                         _ptr(unmasked), _ptr(conf), _ptr(kappa), _ptr(argmax),
+                                         _ptr(n_masked_left), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fdllm_kv_splice(mode, batch, seq_len, n_kv_heads, head_dim, start, length, dtype, k_cache, v_cache,
+                    k_src, v_src, stream=None):
+    _check(lib().fdllm_kv_splice(mode, batch, seq_len, n_kv_heads, head_dim, start, length, dtype,
+                                 _ptr(k_cache), _ptr(v_cache), _ptr(k_src), _ptr(v_src), _stream(stream)))
+
+
+def fdllm_last_device_error(stream=None) -> tuple[int, int]:
+    detail = C.c_int32(0)
+    st = lib().fdllm_last_device_error(_stream(stream), C.byref(detail))
+    return st, detail.value
+
+
+def fdllm_version() -> int:
+    return lib().fdllm_version()
+
+
+def fdllm_launch_counter() -> int:
+    return lib().fdllm_launch_counter()
+
+
+# ---------------------------------------------------------------------------
+# device twin of the seeded input generator (harness, not the method)
+# ---------------------------------------------------------------------------
+
+def fdllm_synth_normals(seed, kind, coords, n, offset, sigma, dtype, out, stream=None):
+    arr = (C.c_int64 * max(1, len(coords)))(*coords)
+    _check(lib().fdllm_synth_normals(seed, kind, arr, len(coords), n, offset, sigma, dtype, _ptr(out),
+                                     _stream(stream)))
+
+
+def fdllm_synth_kv_cache(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch, sigma, dtype, out, stream=None):
+    _check(lib().fdllm_synth_kv_cache(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch, sigma, dtype,
+                                      _ptr(out), _stream(stream)))
+
+
+def fdllm_synth_rows(seed, kind, batch, step, pos0, npos, width, sigma, dtype, out, stream=None):
+    _check(lib().fdllm_synth_rows(seed, kind, batch, step, pos0, npos, width, sigma, dtype, _ptr(out),
+                                  _stream(stream)))
+
+
+def fdllm_synth_hidden(seed, batch, step, pos0, npos, hidden, vocab, p_plant, w, dtype, out, stream=None):
+    _check(lib().fdllm_synth_hidden(seed, batch, step, pos0, npos, hidden, vocab, p_plant, _ptr(w), dtype,
+                                    _ptr(out), _stream(stream)))
+
+
+def fdllm_synth_prompt(seed, batch, prompt_len, vocab, out, stream=None):
+    _check(lib().fdllm_synth_prompt(seed, batch, prompt_len, vocab, _ptr(out), _stream(stream)))

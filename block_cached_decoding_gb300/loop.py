@@ -1,0 +1,162 @@
+"""Block-wise generation loop on the GPU (Algorithm 1 of the Fast-dLLM pages,
+section 3.4.4), driving the three ABI calls in lock step over a batch.
+
+The model forward pass is out of scope, so each step's queries, fresh keys and
+values and hidden states are drawn by the device twin of the seeded generator
+(a stand-in keyed by (sequence, step, position)); caches are re-drawn for each
+refresh epoch (block index) and written with fdllm_kv_splice(REFRESH) at each
+block boundary, standing in for the fused recomputation of every position's
+K/V after a block completes.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import fdllm as F
+from .configs import Workload
+
+
+def _packed(buf: torch.Tensor, shape) -> torch.Tensor:
+    """Dense view of the leading elements of `buf` with `shape` (buffers are sized for the largest step)."""
+    n = 1
+    for x in shape:
+        n *= x
+    return buf.view(-1)[:n].view(shape)
+
+
+@dataclass
+class StepResult:
+    step: int
+    block: int
+    block_start: int
+    unmasked: torch.Tensor      # uint8 [b, B]
+    conf: torch.Tensor          # fp32 [b, B]
+    kappa: torch.Tensor         # fp32 [b, B]
+    argmax: torch.Tensor        # int32 [b, B]
+    n_left: torch.Tensor        # int32 [b]
+    attn_out: torch.Tensor      # [b, nq, Hq, d]
+
+
+class BlockDecoder:
+    def __init__(self, wl: Workload, *, tau: float = 0.9, strategy: int = F.SELECT_THRESHOLD,
+                 factor: float = 1.0, topk: int = 1, sigma_w: float | None = None, device: str = "cuda"):
+        self.wl = wl
+        self.tau, self.strategy, self.factor, self.topk = tau, strategy, factor, topk
+        self.sigma_w = wl.sigma_w if sigma_w is None else sigma_w
+        self.dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+        self.code = F.F32 if wl.dtype == "f32" else F.BF16
+        b, n, hq, hkv, d, B = wl.batch, wl.seq_len, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.block_size
+        dev = torch.device(device)
+        self.w = torch.empty(wl.vocab, wl.hidden, dtype=self.dt, device=dev)
+        F.fdllm_synth_normals(wl.seed, F.SYNTH_W, [], wl.vocab * wl.hidden, 0, self.sigma_w, self.code, self.w)
+        self.kc = torch.empty(b, n, hkv, d, dtype=self.dt, device=dev)
+        self.vc = torch.empty_like(self.kc)
+        self.k_stage = torch.empty_like(self.kc)
+        self.v_stage = torch.empty_like(self.kc)
+        self.tokens = torch.full((b, n), wl.mask_id, dtype=torch.int32, device=dev)
+        prompt = torch.empty(b, wl.prompt_len, dtype=torch.int32, device=dev)
+        F.fdllm_synth_prompt(wl.seed, b, wl.prompt_len, wl.vocab, prompt)
+        self.tokens.fill_(wl.mask_id)
+        self.tokens[:, :wl.prompt_len] = prompt
+        nq_max = {"dual": B, "prefix": n - wl.prompt_len, "none": n}[wl.mode]
+        self.q = torch.empty(b, nq_max, hq, d, dtype=self.dt, device=dev)
+        self.kf = torch.empty(b, nq_max, hkv, d, dtype=self.dt, device=dev)
+        self.vf = torch.empty_like(self.kf)
+        self.attn_out = torch.empty(b, nq_max, hq, d, dtype=torch.float32, device=dev)
+        self.hidden = torch.empty(b, B, wl.hidden, dtype=self.dt, device=dev)
+        self.unmasked = torch.empty(b, B, dtype=torch.uint8, device=dev)
+        self.conf = torch.empty(b, B, dtype=torch.float32, device=dev)
+        self.kappa = torch.empty_like(self.conf)
+        self.argmax = torch.empty(b, B, dtype=torch.int32, device=dev)
+        self.n_left = torch.empty(b, dtype=torch.int32, device=dev)
+        sd = self.select_desc(wl.prompt_len)
+        self.sel_ws = torch.empty(F.fdllm_select_workspace_size(sd), dtype=torch.uint8, device=dev)
+        self.attn_ws_bytes = max(F.fdllm_attn_workspace_size(self.attn_desc(k))
+                                 for k in range(wl.gen_length // B))
+        self.attn_ws = torch.empty(max(self.attn_ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    # -- descriptors -------------------------------------------------------
+    def attn_desc(self, k: int) -> F.AttnDesc:
+        wl = self.wl
+        return F.attn_desc(batch=wl.batch, prompt_len=wl.prompt_len, gen_length=wl.gen_length,
+                           block_size=wl.block_size, block_idx=k, n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads,
+                           head_dim=wl.head_dim, use_cache=0 if wl.mode == "none" else 1,
+                           dual_cache=1 if wl.mode == "dual" else 0, dtype=self.code, out_f32=1)
+
+    def select_desc(self, s: int) -> F.SelectDesc:
+        wl = self.wl
+        return F.select_desc(batch=wl.batch, seq_len=wl.seq_len, block_start=s, block_size=wl.block_size,
+                             hidden=wl.hidden, vocab=wl.vocab, mask_id=wl.mask_id, threshold=self.tau,
+                             strategy=self.strategy, factor=self.factor, topk=self.topk, dtype=self.code)
+
+    # -- pieces ------------------------------------------------------------
+    def query_range(self, k: int) -> tuple[int, int]:
+        wl = self.wl
+        s = wl.prompt_len + k * wl.block_size
+        if wl.mode == "dual":
+            return s, s + wl.block_size
+        if wl.mode == "prefix":
+            return s, wl.seq_len
+        return 0, wl.seq_len
+
+    def refresh(self, k: int):
+        """Block boundary: caches recomputed for refresh epoch k (drawn), written by REFRESH."""
+        wl = self.wl
+        F.fdllm_synth_kv_cache(wl.seed, F.SYNTH_KCACHE, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, k, 1.0,
+                               self.code, self.k_stage)
+        F.fdllm_synth_kv_cache(wl.seed, F.SYNTH_VCACHE, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, k, 1.0,
+                               self.code, self.v_stage)
+        F.fdllm_kv_splice(F.SPLICE_REFRESH, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, 0, wl.seq_len,
+                          self.code, self.kc, self.vc, self.k_stage, self.v_stage)
+
+    def draw_step_inputs(self, g: int, k: int):
+        wl = self.wl
+        p0, p1 = self.query_range(k)
+        nq = p1 - p0
+        b = wl.batch
+        F.fdllm_synth_rows(wl.seed, F.SYNTH_Q, b, g, p0, nq, wl.n_q_heads * wl.head_dim, 1.0, self.code, self.q)
+        F.fdllm_synth_rows(wl.seed, F.SYNTH_KFRESH, b, g, p0, nq, wl.n_kv_heads * wl.head_dim, 1.0, self.code, self.kf)
+        F.fdllm_synth_rows(wl.seed, F.SYNTH_VFRESH, b, g, p0, nq, wl.n_kv_heads * wl.head_dim, 1.0, self.code, self.vf)
+        s = wl.prompt_len + k * wl.block_size
+        F.fdllm_synth_hidden(wl.seed, b, g, s, wl.block_size, wl.hidden, wl.vocab, wl.p_plant, self.w, self.code,
+                             self.hidden)
+
+    def step(self, g: int, k: int) -> StepResult:
+        """One denoising step of block k: attention over the cache, then confidence select."""
+        wl = self.wl
+        p0, p1 = self.query_range(k)
+        nq = p1 - p0
+        self.draw_step_inputs(g, k)
+        b, hq, hkv, d = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+        q, out = _packed(self.q, (b, nq, hq, d)), _packed(self.attn_out, (b, nq, hq, d))
+        kf, vf = _packed(self.kf, (b, nq, hkv, d)), _packed(self.vf, (b, nq, hkv, d))
+        F.fdllm_block_attn(self.attn_desc(k), q, self.kc, self.vc, kf, vf, out, None, self.attn_ws,
+                           ws_bytes=self.attn_ws_bytes)
+        s = wl.prompt_len + k * wl.block_size
+        F.fdllm_confidence_select(self.select_desc(s), self.hidden, self.w, self.tokens, self.unmasked, self.conf,
+                                  self.kappa, self.argmax, self.n_left, self.sel_ws)
+        return StepResult(g, k, s, self.unmasked, self.conf, self.kappa, self.argmax, self.n_left, out)
+
+    def run(self, hook=None, max_steps_per_block: int | None = None):
+        """Decode every block left to right; returns (tokens, steps per block)."""
+        wl = self.wl
+        steps = []
+        g = 0
+        cap = max_steps_per_block or wl.block_size
+        for k in range(wl.gen_length // wl.block_size):
+            self.refresh(k)
+            n = 0
+            while True:
+                r = self.step(g, k)
+                if hook is not None:
+                    hook(self, r)
+                g += 1
+                n += 1
+                if int(r.n_left.max().item()) == 0:
+                    break
+                if n >= cap:
+                    raise RuntimeError(f"block {k} did not finish within {cap} steps")
+            steps.append(n)
+        return self.tokens, steps

@@ -1,0 +1,225 @@
+/*
+ * fdllm.h -- C ABI of the GB300 (sm_103a) Fast-dLLM block-cached decoding hot path.
+ *
+ * Three operations make up one denoising step of block-wise decoding for a
+ * masked-diffusion LM ("Fast-dLLM: Training-free Acceleration of Diffusion LLM
+ * by Enabling KV Cache and Parallel Decoding", paper-graph-ui summary):
+ *
+ *   fdllm_block_attn          attention of the recomputed queries over the
+ *                             approximate KV cache (section 3.4.2, "PrefixCache"
+ *                             and "DualCache"; section 3.4.4 "Cache reuse").
+ *   fdllm_confidence_select   LM head over the block's masked positions with an
+ *                             online softmax giving confidence and argmax, then
+ *                             confidence-aware unmasking (section 3.4.3:
+ *                             confidence c_i = max_v p(x_i = v); threshold
+ *                             strategy with the progress guarantee; factor
+ *                             strategy; the fixed top-k baseline of section 5).
+ *   fdllm_kv_splice           writes fresh K/V into the cache window, or the
+ *                             whole recomputed cache at a block boundary
+ *                             (section 3.4.2 "Cache Overhead and Fused Updates",
+ *                             section 3.4.4 step 3 "Cache update").
+ *
+ * Knob names follow the Fast-dLLM README's command line: gen_length,
+ * block_size, use_cache, if_cache_position (here: dual_cache), threshold.
+ *
+ * Conventions shared by every call
+ *  - Pointers marked "device" are CUDA device (or managed) memory owned by the
+ *    caller; the library never allocates, frees or retains them.  Every tensor
+ *    is dense, row-major in the order its layout names, and 16-byte aligned.
+ *  - Calls are asynchronous and ordered on `stream` (NULL: the legacy default
+ *    stream).  A returned FDLLM_OK means the work was enqueued.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns FDLLM_EINVAL and launches nothing.  fdllm_last_error()
+ *    returns a message for the last failure on the calling thread.
+ *  - Kernels never wait without bound.  A device wait that gives up records
+ *    FDLLM_ETIMEOUT in a per-device error word, which fdllm_last_device_error()
+ *    reads and clears.
+ *  - Floating-point inputs are bf16 or fp32 (fdllm_dtype); all accumulation is
+ *    fp32.
+ */
+#ifndef FDLLM_H_
+#define FDLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (same type as cudaStream_t / CUstream). */
+typedef struct CUstream_st *fdllm_stream_t;
+
+typedef enum {
+  FDLLM_OK = 0,
+  FDLLM_EINVAL = 1,       /* bad argument: shape, range, alignment, null pointer, small workspace */
+  FDLLM_ECUDA = 2,        /* a CUDA runtime call failed (launch error, no device) */
+  FDLLM_ETIMEOUT = 3,     /* a bounded device wait expired (see fdllm_last_device_error) */
+  FDLLM_EUNSUPPORTED = 4  /* valid request this build does not implement */
+} fdllm_status;
+
+typedef enum { FDLLM_BF16 = 0, FDLLM_F32 = 1 } fdllm_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* Block attention                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Sequence layout: N = prompt_len + gen_length positions; block k (0-based)
+ * spans [s, e) with s = prompt_len + k * block_size, e = s + block_size
+ * (section 3.4.4 "Determine block boundaries", written there 1-based).
+ *
+ * Which positions have fresh (this step's) queries, keys and values:
+ *   use_cache = 1, dual_cache = 1  DualCache:   [s, e)   (nq = block_size)
+ *   use_cache = 1, dual_cache = 0  PrefixCache: [s, N)   (nq = N - s; block and suffix)
+ *   use_cache = 0                  no cache:    [0, N)   (nq = N)
+ * Every other position's key and value is read from the cache: the prefix
+ * [0, s) and, with DualCache, the suffix [e, N).  Attention is bidirectional
+ * (no causal mask): every query attends to all N positions. */
+typedef struct {
+  int32_t batch;       /* b >= 1 */
+  int32_t prompt_len;  /* |p0| >= 0 */
+  int32_t gen_length;  /* L >= block_size, a multiple of block_size */
+  int32_t block_size;  /* B >= 1 */
+  int32_t block_idx;   /* 0 <= k < gen_length / block_size */
+  int32_t n_q_heads;   /* Hq, a multiple of n_kv_heads */
+  int32_t n_kv_heads;  /* Hkv; query head h reads KV head h / (Hq / Hkv) */
+  int32_t head_dim;    /* d: 64 or 128 */
+  int32_t use_cache;   /* 0 or 1 */
+  int32_t dual_cache;  /* 0 or 1 (ignored when use_cache = 0) */
+  float sm_scale;      /* score scale; 0 selects 1 / sqrt(head_dim) */
+  int32_t dtype;       /* fdllm_dtype of q, caches and fresh K/V */
+  int32_t out_f32;     /* 1: out is fp32; 0: out has `dtype` */
+} fdllm_attn_desc;
+
+/* Number of fresh query positions nq for `desc` (see the table above), or -1
+ * if the descriptor is invalid. */
+int64_t fdllm_attn_query_count(const fdllm_attn_desc *desc);
+
+/* Scratch bytes fdllm_block_attn needs for `desc` (split-KV partial results);
+ * 0 on an invalid descriptor. */
+size_t fdllm_attn_workspace_size(const fdllm_attn_desc *desc);
+
+/* O_i = sum_j softmax_j(q_i . k_j * sm_scale) v_j over all N positions j.
+ *   q        device [b, nq, Hq, d]   fresh queries, positions as in the table
+ *   k_cache  device [b, N, Hkv, d]   cached keys (rows at fresh positions unread)
+ *   v_cache  device [b, N, Hkv, d]   cached values
+ *   k_fresh  device [b, nq, Hkv, d]  this step's keys at the fresh positions
+ *   v_fresh  device [b, nq, Hkv, d]  this step's values
+ *   out      device [b, nq, Hq, d]   fp32 if out_f32 else dtype
+ *   lse      device [b, nq, Hq] fp32 natural-log softmax denominators, or NULL
+ *   workspace device, >= fdllm_attn_workspace_size(desc) bytes (NULL if that is 0);
+ *            contents on entry are ignored.
+ * Errors: FDLLM_EINVAL for an invalid descriptor, a null required pointer, a
+ * pointer not 16-byte aligned or a short workspace. */
+fdllm_status fdllm_block_attn(const fdllm_attn_desc *desc, const void *q, const void *k_cache,
+                              const void *v_cache, const void *k_fresh, const void *v_fresh,
+                              void *out, float *lse, void *workspace, size_t ws_bytes,
+                              fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* LM head + confidence + parallel unmask                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef enum {
+  FDLLM_SELECT_THRESHOLD = 0, /* unmask every masked i with c_i > threshold; if none, the single
+                                 most confident one (progress guarantee) */
+  FDLLM_SELECT_FACTOR = 1,    /* sort by confidence; unmask the largest n with
+                                 (n + 1) (1 - c_(n)) < factor, at least one */
+  FDLLM_SELECT_TOPK = 2       /* unmask the topk most confident masked positions */
+} fdllm_select_strategy;
+
+typedef struct {
+  int32_t batch;        /* b >= 1 */
+  int32_t seq_len;      /* N, row length of `tokens` */
+  int32_t block_start;  /* s: the block is tokens[:, s : s + block_size] */
+  int32_t block_size;   /* B, 1..256 */
+  int32_t hidden;       /* H, a multiple of 64 */
+  int32_t vocab;        /* V >= 2 */
+  int32_t mask_id;      /* the [MASK] token id; positions holding it are masked */
+  int32_t strategy;     /* fdllm_select_strategy */
+  float threshold;      /* tau (strategy THRESHOLD); tau >= 1 unmasks one per step */
+  float factor;         /* f > 0 (strategy FACTOR) */
+  int32_t topk;         /* k >= 1 (strategy TOPK) */
+  int32_t dtype;        /* fdllm_dtype of hidden and lm_head_w */
+} fdllm_select_desc;
+
+/* Scratch bytes fdllm_confidence_select needs (per-split softmax partials for
+ * up to batch * block_size rows); 0 on an invalid descriptor. */
+size_t fdllm_select_workspace_size(const fdllm_select_desc *desc);
+
+/* One confidence-aware unmask step.
+ * For every masked position i of the block (tokens[b, s + i] == mask_id) the
+ * logits l = hidden[b, i] . W^T are reduced over the whole vocabulary without
+ * being stored, giving
+ *   argmax[b, i] = lowest v with l_v = max l
+ *   conf[b, i]   = c = max_v softmax(l)_v
+ *   kappa[b, i]  = log((1 - c) / c), computed without cancellation so it still
+ *                  orders positions whose confidence rounds to 1
+ * Selection (per `strategy`) ranks by kappa (lowest position first on ties)
+ * and writes tokens[b, s + i] = argmax[b, i] for the chosen positions.
+ *   hidden        device [b, B, H]   hidden states of all block positions (rows of
+ *                                    positions that are not masked are not read)
+ *   lm_head_w     device [V, H]      LM-head weight, row v = token v
+ *   tokens        device int32 [b, N], updated in place
+ *   unmasked      device uint8 [b, B] out: 1 where this step unmasked
+ *   conf          device fp32 [b, B] out: c, NaN where not masked
+ *   kappa         device fp32 [b, B] out or NULL: log-odds, NaN where not masked
+ *   argmax        device int32 [b, B] out: token, -1 where not masked
+ *   n_masked_left device int32 [b] out: masked positions left in the block
+ *   workspace     device, >= fdllm_select_workspace_size(desc) bytes
+ * Errors: FDLLM_EINVAL for an invalid descriptor, null or misaligned pointers, or
+ * a short workspace. */
+fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *hidden,
+                                     const void *lm_head_w, int32_t *tokens, uint8_t *unmasked,
+                                     float *conf, float *kappa, int32_t *argmax,
+                                     int32_t *n_masked_left, void *workspace, size_t ws_bytes,
+                                     fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* KV cache splice / refresh                                                 */
+/* ------------------------------------------------------------------------ */
+
+typedef enum {
+  FDLLM_SPLICE_WINDOW = 0,  /* cache[:, start : start + len] <- src[:, 0 : len] */
+  FDLLM_SPLICE_REFRESH = 1  /* block boundary: cache[:, 0 : N] <- src (start must be 0, len = N) */
+} fdllm_splice_mode;
+
+/* Copies keys and values into the cache, both as [b, rows, Hkv, d].
+ *   k_cache, v_cache  device [b, seq_len, Hkv, d]
+ *   k_src, v_src      device [b, len, Hkv, d]
+ * Hkv * d * element size must be a multiple of 16 bytes.
+ * Errors: FDLLM_EINVAL for a window outside [0, seq_len), REFRESH with
+ * start != 0 or len != seq_len, null or misaligned pointers. */
+fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
+                             int32_t head_dim, int32_t start, int32_t len, int32_t dtype,
+                             void *k_cache, void *v_cache, const void *k_src, const void *v_src,
+                             fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Static description of a status code. */
+const char *fdllm_status_string(int32_t status);
+
+/* Message describing the last non-OK status returned on the calling thread
+ * (thread-local; valid until the next failing call on that thread). */
+const char *fdllm_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word: FDLLM_OK if no device wait gave up since the last read, else
+ * FDLLM_ETIMEOUT (`detail`, if not NULL, receives the site code). */
+fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
+
+/* ABI version: 100 * major + minor. */
+int32_t fdllm_version(void);
+
+/* Number of kernels this library has launched in the process so far (all
+ * devices, all threads): a diagnostic for counting launches per step. */
+uint64_t fdllm_launch_counter(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FDLLM_H_ */

@@ -1,0 +1,119 @@
+"""The C ABI library loads, exports every declared symbol and rejects bad
+arguments on the host (no GPU needed: validation runs before any launch)."""
+import ctypes as C
+import glob
+import os
+import re
+
+import pytest
+
+from block_cached_decoding_gb300 import fdllm as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(fdllm_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(F.LIB_PATH):
+        from block_cached_decoding_gb300 import build
+        build.build()
+    return F.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert {"fdllm_block_attn", "fdllm_confidence_select", "fdllm_kv_splice"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(F.EXPORTS) <= declared
+
+
+def test_status_strings_and_version(lib):
+    assert F.fdllm_version() == 100
+    for s in range(5):
+        assert lib.fdllm_status_string(s).decode().startswith("FDLLM_")
+
+
+def _attn(**kw):
+    base = dict(batch=1, prompt_len=64, gen_length=64, block_size=16, block_idx=0, n_q_heads=4, n_kv_heads=4,
+                head_dim=64, use_cache=1, dual_cache=1, dtype=F.F32)
+    base.update(kw)
+    return F.attn_desc(**base)
+
+
+def test_query_counts_follow_the_cache_mode(lib):
+    # DualCache: the block; PrefixCache: block + suffix; no cache: every position
+    assert F.fdllm_attn_query_count(_attn()) == 16
+    assert F.fdllm_attn_query_count(_attn(dual_cache=0, block_idx=1)) == 128 - 80
+    assert F.fdllm_attn_query_count(_attn(use_cache=0)) == 128
+
+
+@pytest.mark.parametrize("bad", [dict(batch=0), dict(block_idx=4), dict(block_idx=-1), dict(gen_length=60),
+                                 dict(n_q_heads=6), dict(head_dim=96), dict(use_cache=2), dict(dtype=7),
+                                 dict(sm_scale=float("nan"))])
+def test_attn_rejects_bad_descriptors(lib, bad):
+    d = _attn(**bad)
+    assert F.fdllm_attn_query_count(d) == -1
+    with pytest.raises(F.FdllmError) as e:
+        F.fdllm_block_attn(d, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == F.EINVAL
+
+
+def test_attn_rejects_null_and_misaligned_pointers(lib):
+    with pytest.raises(F.FdllmError) as e:
+        F.fdllm_block_attn(_attn(), 16, 16, 0, 16, 16, 16, stream=0)
+    assert e.value.status == F.EINVAL and "v_cache is null" in str(e.value)
+    with pytest.raises(F.FdllmError) as e:
+        F.fdllm_block_attn(_attn(), 16, 18, 16, 16, 16, 16, stream=0)
+    assert e.value.status == F.EINVAL and "aligned" in str(e.value)
+
+
+def _sel(**kw):
+    base = dict(batch=1, seq_len=128, block_start=64, block_size=16, hidden=256, vocab=1024, mask_id=1024,
+                threshold=0.9, dtype=F.F32)
+    base.update(kw)
+    return F.select_desc(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(block_size=0), dict(block_size=300), dict(block_start=120),
+                                 dict(hidden=100), dict(vocab=1), dict(mask_id=5), dict(strategy=9),
+                                 dict(strategy=F.SELECT_FACTOR, factor=0.0), dict(strategy=F.SELECT_TOPK, topk=0),
+                                 dict(threshold=float("nan")), dict(batch=16, block_size=256)])
+def test_select_rejects_bad_descriptors(lib, bad):
+    d = _sel(**bad)
+    assert F.fdllm_select_workspace_size(d) == 0
+    with pytest.raises(F.FdllmError) as e:
+        F.fdllm_confidence_select(d, 16, 16, 16, 16, 16, 16, 16, 16, 16, ws_bytes=1 << 30, stream=0)
+    assert e.value.status == F.EINVAL
+
+
+def test_select_rejects_short_workspace(lib):
+    d = _sel()
+    need = F.fdllm_select_workspace_size(d)
+    assert need > 0
+    with pytest.raises(F.FdllmError) as e:
+        F.fdllm_confidence_select(d, 16, 16, 16, 16, 16, 16, 16, 16, 16, ws_bytes=need - 1, stream=0)
+    assert e.value.status == F.EINVAL and "workspace" in str(e.value)
+
+
+@pytest.mark.parametrize("args", [
+    (F.SPLICE_WINDOW, 1, 128, 4, 64, 120, 16),     # window past the end
+    (F.SPLICE_REFRESH, 1, 128, 4, 64, 0, 64),      # refresh must cover the whole cache
+    (F.SPLICE_WINDOW, 1, 128, 1, 4, 0, 16),        # row of 16 bytes fp32 ok, but 4 bf16 = 8 bytes
+    (5, 1, 128, 4, 64, 0, 16),
+])
+def test_splice_rejects_bad_windows(lib, args):
+    mode, b, n, hkv, d, start, ln = args
+    dtype = F.BF16 if (hkv, d) == (1, 4) else F.F32
+    with pytest.raises(F.FdllmError) as e:
+        F.fdllm_kv_splice(mode, b, n, hkv, d, start, ln, dtype, 16, 16, 16, 16, stream=0)
+    assert e.value.status == F.EINVAL

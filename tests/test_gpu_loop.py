@@ -1,0 +1,91 @@
+"""The GPU block loop in lock step with the oracle (tiny fp32 setting, and a
+small bf16 batch).  At every step the oracle evaluates the GPU's current state
+(tokens, caches, step inputs); disagreements inside the tolerance bands are
+counted and the run continues with the GPU's decision."""
+import numpy as np
+import pytest
+import torch
+
+from block_cached_decoding_gb300 import configs, synth
+from block_cached_decoding_gb300 import fdllm as F
+from block_cached_decoding_gb300.loop import BlockDecoder
+from gpu_helpers import assert_attention_close, compare_select, ensure_built, f64
+from oracle import fdllm_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def lockstep(wl, tau, strategy="threshold"):
+    dec = BlockDecoder(wl, tau=tau, strategy={"threshold": F.SELECT_THRESHOLD, "factor": F.SELECT_FACTOR}[strategy])
+    w64 = f64(synth.lm_head_weight(wl.seed, wl.vocab, wl.hidden, wl.sigma_w, wl.dtype), wl.dtype)
+    state = {"exempt": 0, "steps": 0, "unmasked": 0}
+    caches = {}
+
+    def hook(d, r):
+        g, k, s = r.step, r.block, r.block_start
+        if k not in caches:
+            caches.clear()
+            caches[k] = [f64(synth.kv_cache(wl.seed, kind, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, k,
+                                             wl.dtype), wl.dtype) for kind in (synth.KIND_KCACHE, synth.KIND_VCACHE)]
+        kc, vc = caches[k]
+        p0, p1 = d.query_range(k)
+        pos = range(p0, p1)
+        b = wl.batch
+        q = synth.per_position(wl.seed, synth.KIND_Q, b, g, pos, wl.n_q_heads * wl.head_dim, wl.dtype)
+        kf = synth.per_position(wl.seed, synth.KIND_KFRESH, b, g, pos, wl.n_kv_heads * wl.head_dim, wl.dtype)
+        vf = synth.per_position(wl.seed, synth.KIND_VFRESH, b, g, pos, wl.n_kv_heads * wl.head_dim, wl.dtype)
+        shp = (b, len(pos), -1, wl.head_dim)
+        o_ref, _ = O.block_attention(f64(q, wl.dtype).reshape(shp), kc, vc, f64(kf, wl.dtype).reshape(shp),
+                                     f64(vf, wl.dtype).reshape(shp), mode=wl.mode, s=s, e=s + wl.block_size,
+                                     n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads)
+        assert_attention_close(r.attn_out.cpu().numpy().astype(np.float64), o_ref)
+        # select: the oracle evaluates the tokens as they were before this step
+        t_after = d.tokens.cpu().numpy().astype(np.int64)
+        um = r.unmasked.cpu().numpy().astype(bool)
+        t_before = t_after.copy()
+        t_before[:, s:s + wl.block_size][um] = wl.mask_id
+        hid, _, _ = synth.hidden_states(wl.seed, b, g, range(s, s + wl.block_size), wl.hidden, wl.vocab, wl.sigma_w,
+                                        wl.dtype, wl.p_plant)
+        _, info = O.decode_step(t_before, f64(hid, wl.dtype), w64, s=s, block_size=wl.block_size, mask_id=wl.mask_id,
+                                tau=tau, strategy=strategy)
+        got = {"unmask": um, "conf": r.conf.cpu().numpy(), "kappa": r.kappa.cpu().numpy(),
+               "token": r.argmax.cpu().numpy()}
+        state["exempt"] += compare_select(info, got, tau, strategy)
+        state["steps"] += 1
+        state["unmasked"] += int(um.sum())
+        if tau >= 1.0:
+            assert np.all(um.sum(axis=1) == info["masked_before"].any(axis=1))
+
+    tokens, steps = dec.run(hook=hook)
+    t = tokens.cpu().numpy()
+    assert not (t == wl.mask_id).any() and t.max() < wl.vocab
+    assert max(steps) <= wl.block_size
+    assert state["unmasked"] == wl.batch * wl.gen_length
+    return state, steps
+
+
+@pytest.mark.parametrize("tau", [0.9, 1.0])
+def test_tiny_fp32_loop(tau):
+    wl = configs.TINY
+    state, steps = lockstep(wl, tau)
+    if tau >= 1.0:
+        assert steps == [wl.block_size] * (wl.gen_length // wl.block_size)
+    assert state["exempt"] <= 2
+
+
+def test_small_bf16_batched_dual_loop():
+    wl = configs.LLADA_BATCH.with_(batch=3, prompt_len=40, gen_length=64, block_size=16, n_q_heads=4,
+                                   n_kv_heads=2, head_dim=128, hidden=512, vocab=3000)
+    state, _ = lockstep(wl, 0.9)
+    assert state["exempt"] <= 3
+
+
+def test_small_bf16_prefix_loop():
+    wl = configs.LLADA_STEP.with_(prompt_len=30, gen_length=64, block_size=32, n_q_heads=4, n_kv_heads=4,
+                                  head_dim=64, hidden=256, vocab=2000)
+    lockstep(wl, 0.9)

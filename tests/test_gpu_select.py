@@ -1,0 +1,120 @@
+"""fdllm_confidence_select against the oracle's decode step."""
+import numpy as np
+import pytest
+import torch
+
+from block_cached_decoding_gb300 import configs
+from block_cached_decoding_gb300 import fdllm as F
+from block_cached_decoding_gb300 import synth
+from gpu_helpers import SelectOutputs, code, compare_select, dev, ensure_built, f64
+from oracle import fdllm_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+_W = {}
+
+
+def weight(seed, V, H, sigma, dtype):
+    key = (seed, V, H, sigma, dtype)
+    if key not in _W:
+        w = synth.lm_head_weight(seed, V, H, sigma, dtype)
+        _W[key] = (w, dev(w, dtype), f64(w, dtype))
+    return _W[key]
+
+
+def one_step(*, batch, prompt_len, gen_length, block_size, block_idx, H, V, dtype, tau=0.9, p_plant=0.4,
+             sigma=None, seed=0, step=0, premask=None, strategy="threshold", factor=1.0, topk=1):
+    sigma = sigma if sigma is not None else float(np.sqrt(0.02))
+    n = prompt_len + gen_length
+    s, e = O.block_window(prompt_len, block_size, block_idx)
+    w, w_dev, w64 = weight(seed, V, H, sigma, dtype)
+    hid, _, _ = synth.hidden_states(seed, batch, step, range(s, e), H, V, sigma, dtype, p_plant)
+    tokens = np.full((batch, n), V, dtype=np.int64)
+    tokens[:, :prompt_len] = synth.prompt_tokens(seed, batch, prompt_len, V)
+    tokens[:, :s] = np.where(tokens[:, :s] == V, 7, tokens[:, :s])
+    if premask is not None:                        # some block positions already decoded
+        tokens[:, s:e] = np.where(premask, V, 5)
+    ref_tokens, info = O.decode_step(tokens, f64(hid, dtype), w64, s=s, block_size=block_size, mask_id=V, tau=tau,
+                                     strategy=strategy, factor=factor, topk=topk)
+    strat = {"threshold": F.SELECT_THRESHOLD, "factor": F.SELECT_FACTOR, "topk": F.SELECT_TOPK}[strategy]
+    desc = F.select_desc(batch=batch, seq_len=n, block_start=s, block_size=block_size, hidden=H, vocab=V, mask_id=V,
+                         threshold=tau, strategy=strat, factor=factor, topk=topk, dtype=code(dtype))
+    t_dev = torch.from_numpy(tokens.astype(np.int32)).cuda()
+    outs = SelectOutputs(desc, batch, block_size)
+    outs.run(desc, dev(hid, dtype), w_dev, t_dev)
+    got = outs.host()
+    compare_select(info, got, tau, strategy)
+    t_got = t_dev.cpu().numpy()
+    # tokens: only this step's unmasked positions changed, to the GPU's argmax
+    changed = t_got != tokens
+    assert not changed[:, :s].any() and not changed[:, e:].any()
+    for b in range(batch):
+        for i in np.nonzero(got["unmask"][b])[0]:
+            assert t_got[b, s + i] == got["token"][b, i]
+    assert np.array_equal(got["n_left"], (t_got[:, s:e] == V).sum(axis=1))
+    return info, got
+
+
+def test_tiny_fp32_first_step():
+    wl = configs.TINY
+    info, got = one_step(batch=1, prompt_len=64, gen_length=64, block_size=16, block_idx=0, H=wl.hidden,
+                         V=wl.vocab, dtype="f32", p_plant=wl.p_plant, sigma=wl.sigma_w, seed=wl.seed)
+    assert got["unmask"].sum() >= 1
+
+
+@pytest.mark.parametrize("tau", [0.5, 0.9, 1.0, 0.0])
+def test_bf16_thresholds(tau):
+    one_step(batch=2, prompt_len=64, gen_length=64, block_size=32, block_idx=1, H=512, V=5000, dtype="bf16", tau=tau,
+             seed=1)
+
+
+def test_bf16_std_reading_all_fallback():
+    info, got = one_step(batch=3, prompt_len=16, gen_length=32, block_size=32, block_idx=0, H=256, V=3001,
+                         dtype="bf16", sigma=0.02, seed=2)
+    assert np.all(got["unmask"].sum(axis=1) == 1)
+
+
+def test_partially_decoded_block_and_empty_sequence():
+    rng = np.random.default_rng(0)
+    pm = rng.random((3, 24)) < 0.4
+    pm[1] = False                                  # sequence 1 has nothing left to unmask
+    info, got = one_step(batch=3, prompt_len=10, gen_length=48, block_size=24, block_idx=1, H=256, V=2048,
+                         dtype="bf16", seed=3, premask=pm)
+    assert got["unmask"][1].sum() == 0 and got["n_left"][1] == 0
+
+
+@pytest.mark.parametrize("strategy,kw", [("factor", dict(factor=1.0)), ("factor", dict(factor=0.3)),
+                                         ("topk", dict(topk=2)), ("topk", dict(topk=40))])
+def test_strategies(strategy, kw):
+    one_step(batch=2, prompt_len=32, gen_length=64, block_size=32, block_idx=0, H=256, V=4096, dtype="bf16", seed=4,
+             strategy=strategy, **kw)
+
+
+@pytest.mark.parametrize("H,V,B", [(64, 2, 1), (192, 1000, 7), (1024, 33333, 48), (256, 70000, 256)])
+def test_ragged_shapes(H, V, B):
+    one_step(batch=1, prompt_len=3, gen_length=B, block_size=B, block_idx=0, H=H, V=V, dtype="bf16", seed=5)
+
+
+@pytest.mark.parametrize("batch,B,H,V", [(4, 32, 256, 5000),     # 128 block rows: one row tile
+                                         (6, 32, 320, 9001),     # 192 rows: two row tiles
+                                         (16, 32, 256, 4097),    # 512 rows: four row tiles
+                                         (20, 32, 128, 3000)])   # 640 rows: CUDA-core path
+def test_batched_row_tiles(batch, B, H, V):
+    rng = np.random.default_rng(batch)
+    pm = rng.random((batch, B)) < 0.5
+    if batch >= 16:
+        pm[4:8] = False          # rows 128..255: a row tile with nothing masked is skipped
+    one_step(batch=batch, prompt_len=8, gen_length=B, block_size=B, block_idx=0, H=H, V=V, dtype="bf16",
+             seed=6, premask=pm)
+
+
+def test_nothing_masked_anywhere():
+    info, got = one_step(batch=2, prompt_len=8, gen_length=32, block_size=32, block_idx=0, H=256, V=1000,
+                         dtype="bf16", seed=7, premask=np.zeros((2, 32), bool))
+    assert got["unmask"].sum() == 0 and np.all(got["n_left"] == 0)
