@@ -329,3 +329,72 @@ fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------
+// Allocation-free confidence select: the partials live in a file-scope device
+// array instead of a caller workspace (see fdllm_confidence_select_noalloc in
+// include/fdllm.h for the callers this serves and the limits).
+// ----------------------------------------------------------------------------
+namespace fdllm {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FDLLM_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name is only a stand-in for the symbol, so the address is looked up
+// once per device (with that device current) and cached.
+fdllm_status noalloc_scratch(void **out) {
+  static void *ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  fdllm_status st = cuda_status(cudaGetDevice(&dev), "noalloc select: cudaGetDevice");
+  if (st != FDLLM_OK) return st;
+  if (dev < 0 || dev >= kMaxDevices) return fail(FDLLM_ECUDA, "noalloc select: device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    st = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_scratch), "noalloc select: cudaGetSymbolAddress");
+    if (st != FDLLM_OK) return st;
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return FDLLM_OK;
+}
+
+}  // namespace
+}  // namespace fdllm
+
+extern "C" fdllm_status fdllm_confidence_select_noalloc(const fdllm_select_desc *desc, const void *hidden,
+                                                        const void *lm_head_w, int32_t *tokens,
+                                                        uint8_t *unmasked, float *conf, float *kappa,
+                                                        int32_t *argmax, int32_t *n_masked_left,
+                                                        fdllm_stream_t stream) {
+  SelectProblem p;
+  fdllm_status st = resolve_select(desc, p);
+  if (st != FDLLM_OK) return st;
+  const void *req[] = {hidden, lm_head_w, tokens, unmasked, conf, argmax, n_masked_left};
+  const char *names[] = {"hidden", "lm_head_w", "tokens", "unmasked", "conf", "argmax", "n_masked_left"};
+  for (int i = 0; i < 7; ++i)
+    if (!req[i]) return fail(FDLLM_EINVAL, "noalloc select: %s is null", names[i]);
+  if (!aligned16(hidden) || !aligned16(lm_head_w))
+    return fail(FDLLM_EINVAL, "noalloc select: hidden and lm_head_w must be 16-byte aligned");
+  const SelectLayout L = select_layout(p);
+  if (L.total > FDLLM_NOALLOC_SCRATCH_BYTES)
+    return fail(FDLLM_EINVAL,
+                "noalloc select: the vocabulary partials need %zu bytes, more than the %u-byte static scratch "
+                "(batch * block_size = %d rows x %d splits); use fdllm_confidence_select with a workspace",
+                L.total, (unsigned)FDLLM_NOALLOC_SCRATCH_BYTES, p.batch * p.B, L.splits);
+  void *scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != FDLLM_OK) return st;
+  p.hidden = hidden; p.w = lm_head_w; p.tokens = tokens; p.unmasked = unmasked; p.conf = conf;
+  p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left;
+  p.ws = scratch; p.ws_bytes = FDLLM_NOALLOC_SCRATCH_BYTES;
+  p.err = error_word_ptr();
+  VocabStat *part = (VocabStat *)scratch;
+  cudaStream_t cs = (cudaStream_t)stream;
+  st = cuda_status(L.tc ? launch_lmhead_tc(p, part, L.splits, cs) : launch_lmhead_simt(p, part, L.splits, cs),
+                   "noalloc select: lm-head launch");
+  if (st != FDLLM_OK) return st;
+  return cuda_status(launch_select(p, part, L.splits, cs), "noalloc select: select launch");
+}

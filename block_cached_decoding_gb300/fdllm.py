@@ -24,8 +24,10 @@ EXPORTS = (
     "fdllm_select_workspace_size", "fdllm_confidence_select", "fdllm_kv_splice",
     "fdllm_status_string", "fdllm_last_error", "fdllm_last_device_error", "fdllm_version",
     "fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
-    "fdllm_synth_prompt", "fdllm_launch_counter",
+    "fdllm_synth_prompt", "fdllm_launch_counter", "fdllm_confidence_select_noalloc",
 )
+
+NOALLOC_SCRATCH_BYTES = 2 << 20
 
 
 class FdllmError(RuntimeError):
@@ -71,6 +73,8 @@ def lib() -> C.CDLL:
         L.fdllm_select_workspace_size.restype = sz
         L.fdllm_confidence_select.argtypes = [C.POINTER(SelectDesc)] + [vp] * 9 + [sz, vp]
         L.fdllm_confidence_select.restype = i32
+        L.fdllm_confidence_select_noalloc.argtypes = [C.POINTER(SelectDesc)] + [vp] * 9
+        L.fdllm_confidence_select_noalloc.restype = i32
         L.fdllm_kv_splice.argtypes = [i32] * 8 + [vp] * 5
         L.fdllm_kv_splice.restype = i32
         L.fdllm_status_string.argtypes = [i32]
@@ -168,6 +172,14 @@ def fdllm_confidence_select(desc, hidden, lm_head_w, tokens, unmasked, conf, kap
     _check(lib().fdllm_confidence_select(C.byref(desc), _ptr(hidden), _ptr(lm_head_w), _ptr(tokens),
                                          _ptr(unmasked), _ptr(conf), _ptr(kappa), _ptr(argmax),
                                          _ptr(n_masked_left), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fdllm_confidence_select_noalloc(desc, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax, n_masked_left,
+                                    stream=None):
+    """fdllm_confidence_select with its scratch in the library's static device array (no workspace)."""
+    _check(lib().fdllm_confidence_select_noalloc(C.byref(desc), _ptr(hidden), _ptr(lm_head_w), _ptr(tokens),
+                                                 _ptr(unmasked), _ptr(conf), _ptr(kappa), _ptr(argmax),
+                                                 _ptr(n_masked_left), _stream(stream)))
 
 
 def fdllm_kv_splice(mode, batch, seq_len, n_kv_heads, head_dim, start, length, dtype, k_cache, v_cache,

@@ -176,6 +176,43 @@ fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *
                                      fdllm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Allocation-free confidence select                                         */
+/* ------------------------------------------------------------------------ */
+
+/* The paper has no counterpart to this call; it exists for callers of this
+ * library that cannot allocate device memory, e.g. a plug-in inside a host
+ * framework that owns every device allocation and hands the plug-in only its
+ * inputs and outputs, or a runtime that forbids allocation once serving has
+ * started.  It computes exactly what fdllm_confidence_select computes, with the
+ * same arguments except the workspace.
+ *
+ * Scratch: the per-split vocabulary partials live in a fixed array of
+ * FDLLM_NOALLOC_SCRATCH_BYTES (2 MiB) compiled into this library as a
+ * file-scope __device__ array; every GPU that loads the library holds it until
+ * the process exits.  The call accepts exactly the descriptors for which
+ * fdllm_select_workspace_size(desc) <= 2 MiB (for bf16 and batch * block_size
+ * <= 512 that is batch * block_size * SM count * 16 bytes); any larger request
+ * returns FDLLM_EINVAL with a message and launches nothing.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current, so make that first call
+ * before any stream capture.
+ * Sharing: every call uses the same array and it keeps the last call's
+ * contents.  Nothing in it has to start at zero (a call writes every entry it
+ * later reads), but calls that overlap on the GPU -- unordered streams, or
+ * several host threads -- race on the array and give wrong results; order them
+ * on one stream or with events.
+ * The call never calls cudaMalloc, cudaFree or any other allocating routine.
+ * Errors: as fdllm_confidence_select, plus FDLLM_EINVAL when the partials would
+ * exceed the array and FDLLM_ECUDA when the set-up lookup fails. */
+#define FDLLM_NOALLOC_SCRATCH_BYTES (2u << 20)
+
+fdllm_status fdllm_confidence_select_noalloc(const fdllm_select_desc *desc, const void *hidden,
+                                             const void *lm_head_w, int32_t *tokens,
+                                             uint8_t *unmasked, float *conf, float *kappa,
+                                             int32_t *argmax, int32_t *n_masked_left,
+                                             fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* KV cache splice / refresh                                                 */
 /* ------------------------------------------------------------------------ */
 
