@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace fdllm {
 
@@ -19,6 +20,15 @@ __device__ int32_t g_device_error_word = 0;
 namespace {
 
 thread_local std::string t_last_error;
+
+// One thread waits on an mbarrier that expects an arrival nobody makes.
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t *err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  tc::mbar_init(&bar, 1);
+  tc::fence_barrier_init();
+  if (!tc::mbar_wait(&bar, 0, limit_ns)) record_device_error(err, 900);
+}
 
 fdllm_status fail(fdllm_status st, const char *fmt, ...) {
   char buf[512];
@@ -195,6 +205,15 @@ using namespace fdllm;
 extern "C" {
 
 int32_t fdllm_version(void) { return 100; }
+
+fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");
+  int32_t *err = error_word_ptr();
+  if (!err) return fail(FDLLM_ECUDA, "selftest: device error word unavailable");
+  selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ms * 1000000ull, err);
+  count_launches(1);
+  return cuda_status(cudaGetLastError(), "selftest launch");
+}
 
 uint64_t fdllm_launch_counter(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -19,6 +19,14 @@
 //              split-KV partials with (max, l) for the combine kernel.
 // With every score tile of the CTA resident in TMEM the softmax needs a single
 // max, so O never has to be rescaled.
+//
+// Merging the splits: when a unit has at most 8 splits they run as one thread
+// block cluster and merge through distributed shared memory: every CTA
+// publishes its rows' (max, l), weights its O rows by l_s 2^(m_s - M) / L and
+// stores them in its own shared memory; CTA c then sums rows [c R/C, (c+1) R/C)
+// across the cluster and writes the output.  Longer key ranges fall back to
+// fp32 partials in the workspace and a combine kernel.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,6 +40,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTile = 128;  // keys per tile and rows per query tile
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 
 struct Plan {
   int f0, f1;           // cached prefix [0, f0), cached suffix [f1, N)
@@ -44,6 +53,7 @@ struct Plan {
   int qtiles_per_head;  // tiles per head when nq > 128
   int nqt;              // query tiles per KV head
   int units;            // batch * Hkv * nqt
+  int cluster;          // 1: splits of a unit form a cluster and merge in DSMEM
 };
 
 template <int D>
@@ -57,7 +67,7 @@ struct Cfg {
 
 template <int D, int T>
 struct Smem {
-  static constexpr int BYTES = Cfg<D>::TILE_BYTES * (1 + T) + Cfg<D>::KP_BYTES * T + 1024 + 512;
+  static constexpr int BYTES = Cfg<D>::TILE_BYTES * (1 + T) + Cfg<D>::KP_BYTES * T + 1024 + 2048;
   static constexpr int TMEM_COLS = T == 1 ? 256 : 512;  // S tiles + O
 };
 
@@ -65,6 +75,7 @@ struct Bars {
   uint64_t qfull, kfull[2], vfull[2], sfull[2], pfull[2], ofull, drain;
   uint32_t tmem_base;
   int32_t abort;
+  float2 ml[kTile];  // this CTA's (max in log2 units, l) per row, read by the cluster
 };
 
 struct KeyTile {
@@ -98,7 +109,7 @@ struct Args {
   int32_t *err;
 };
 
-template <int D, int T>
+template <int D, int T, bool CL>
 __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
@@ -149,6 +160,8 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
   tc::pdl_launch_dependents();
   const uint32_t tmem = br.tmem_base;
   const uint32_t tmem_o = tmem + (uint32_t)(T * kTile);
+  bool ok_cl = false;   // cluster merge: this thread's row finished its split
+  float ms_cl = 0.f;    // cluster merge: this thread's row max in log2 units
 
   if (warp == 0) {
     if (lane == 0) {
@@ -215,19 +228,28 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
     const int r = q * 32 + lane;                    // query row of the tile (TMEM lane)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     bool ok = true;
-    // pass 1: the row max over all valid scores of the CTA
+    // pass 1: the row max over all valid scores of the CTA (TMEM read 64 columns per wait)
     float mx = kNegInf;
     for (int t = 0; t < nt && ok; ++t) {
       if (!tc::mbar_wait(&br.sfull[t], 0)) { record_device_error(a.err, 205); atomicExch(&br.abort, 1); ok = false; break; }
       tc::fence_after_sync();
       const int nv = key_tile(pl, a.nq, a.n, k0 + t).nvalid;
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        uint32_t x[32];
-        tc::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(t * kTile + c0), x);
-        tc::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c0 + e < nv) mx = fmaxf(mx, __uint_as_float(x[e]));
+      for (int c0 = 0; c0 < kTile; c0 += 64) {
+        uint32_t x[32], y[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(t * kTile + c0), x);
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(t * kTile + c0 + 32), y);
+        tc::tmem_ld_wait();
+        if (nv >= kTile) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, fmaxf(__uint_as_float(x[e]), __uint_as_float(y[e])));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (c0 + e < nv) mx = fmaxf(mx, __uint_as_float(x[e]));
+            if (c0 + 32 + e < nv) mx = fmaxf(mx, __uint_as_float(y[e]));
+          }
+        }
       }
     }
     // pass 2: P = exp2((s - max) * scale * log2 e) as bf16 into the K buffer; l = sum P
@@ -236,27 +258,31 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
     for (int t = 0; t < nt && ok; ++t) {
       const int nv = key_tile(pl, a.nq, a.n, k0 + t).nvalid;
       unsigned char *p_s = k_s + t * CF::KP_BYTES;
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
-        uint32_t x[32];
-        tc::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(t * kTile + c0), x);
+#pragma unroll
+      for (int c0 = 0; c0 < kTile; c0 += 64) {
+        uint32_t x[64];
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(t * kTile + c0), *(uint32_t(*)[32])&x[0]);
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + (uint32_t)(t * kTile + c0 + 32), *(uint32_t(*)[32])&x[32]);
         tc::tmem_ld_wait();
-        uint32_t pk[16];
+        // these 64 keys are one 128-byte row of the swizzle atom column c0 / 64: 8 chunks of 8 keys
+        unsigned char *rowp = p_s + (c0 / 64) * (kTile * 128) + r * 128;
+        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = (c0 + e < nv) ? exp2f(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
-          const float p1 = (c0 + e + 1 < nv) ? exp2f(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
-          l += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pk[e / 2] = *(uint32_t *)&h2;
-        }
-        // 32 keys = 4 16-byte chunks of this row, in the 128-byte swizzle layout
-        const int half = c0 / 64;
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t pk[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int chunk = (c0 % 64) / 8 + cc;
-          unsigned char *dst = p_s + half * (kTile * 128) + r * 128 + ((chunk ^ (r & 7)) * 16);
-          *(uint4 *)dst = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int e = ch * 8 + e2 * 2;
+            const float p0 = (c0 + e < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
+            const float p1 = (c0 + e + 1 < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
+            l0 += p0;
+            l1 += p1;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            pk[e2] = *(uint32_t *)&h2;
+          }
+          *(uint4 *)(rowp + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        l += l0 + l1;
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -264,7 +290,12 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
       if (lane == 0) tc::mbar_arrive(&br.pfull[t]);
     }
     if (ok && !tc::mbar_wait(&br.ofull, 0)) { record_device_error(a.err, 206); atomicExch(&br.abort, 1); ok = false; }
-    if (ok) {
+    if constexpr (CL) {
+      // publish this split's (max, l) of row r; O is weighted after the cluster barrier
+      br.ml[r] = ok ? make_float2(ms, l) : make_float2(kNegInf, 0.f);
+      ok_cl = ok;
+      ms_cl = ms;
+    } else if (ok) {
       tc::fence_after_sync();
       // row r of the tile -> (head, query); O streams from TMEM 32 columns at a time
       const int hs = pl.qtiles_per_head == 0 ? r / pl.qr : 0;
@@ -308,6 +339,74 @@ __global__ void __launch_bounds__(kThreads, T == 1 ? 2 : 1)
           a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = mx * a.scale + __logf(l);
       }
     }
+  }
+  if constexpr (CL) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = pl.nsplit;
+    const int crank = (int)cluster.block_rank();
+    constexpr int CH = D / 4;                          // float4 chunks per row
+    float *ored = (float *)k_s;                        // [128][D] fp32, chunks swizzled by row
+    tc::fence_before_sync();
+    cluster.sync();                                    // every split's (max, l) is published
+    float M = kNegInf, L = 0.f;
+    const int r = (warp - 4) * 32 + lane;
+    if (warp >= 4) {
+      tc::fence_after_sync();
+      for (int c = 0; c < C; ++c) M = fmaxf(M, cluster.map_shared_rank(&br.ml[r], c)->x);
+      for (int c = 0; c < C; ++c) {
+        const float2 v = *cluster.map_shared_rank(&br.ml[r], c);
+        if (v.y > 0.f) L += v.y * exp2f(v.x - M);
+      }
+      const float w = (ok_cl && L > 0.f) ? exp2f(ms_cl - M) / L : 0.f;
+      const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t x[32];
+        tc::tmem_ld_32x32b_x32(tmem_o + lane_base + (uint32_t)c0, x);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int ch = c0 / 4 + i;
+          float4 v = ok_cl ? make_float4(__uint_as_float(x[4 * i]) * w, __uint_as_float(x[4 * i + 1]) * w,
+                                         __uint_as_float(x[4 * i + 2]) * w, __uint_as_float(x[4 * i + 3]) * w)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          *(float4 *)(ored + r * D + ((ch ^ (r & (CH - 1))) * 4)) = v;
+        }
+      }
+    }
+    tc::fence_before_sync();
+    cluster.sync();                                    // every split's weighted O is in its shared memory
+    // this CTA sums rows [r0, r1) over the cluster and writes them
+    const int rpc = (kTile + C - 1) / C;
+    const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);
+    for (int u = threadIdx.x; u < (r1 - r0) * CH; u += kThreads) {
+      const int row = r0 + u / CH, ch = u % CH;
+      const int hs = pl.qtiles_per_head == 0 ? row / pl.qr : 0;
+      const int qi = pl.qtiles_per_head == 0 ? row % pl.qr : q0 + row;
+      if (hs >= nh || qi >= a.nq) continue;
+      const float *src = ored + row * D + ((ch ^ (row & (CH - 1))) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < C; ++c) {
+        const float4 v = *(const float4 *)cluster.map_shared_rank(src, c);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      const int h = kvh * a.group + h0 + hs;
+      const int64_t o = (((int64_t)b * a.nq + qi) * a.hq + h) * D + ch * 4;
+      if (a.out_f32) {
+        *(float4 *)((float *)a.out + o) = acc;
+      } else {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        *(uint2 *)((__nv_bfloat16 *)a.out + o) = make_uint2(*(uint32_t *)&lo, *(uint32_t *)&hi);
+      }
+    }
+    if (warp >= 4 && a.lse && r >= r0 && r < r1 && L > 0.f) {
+      const int hs = pl.qtiles_per_head == 0 ? r / pl.qr : 0;
+      const int qi = pl.qtiles_per_head == 0 ? r % pl.qr : q0 + r;
+      if (hs < nh && qi < a.nq)
+        a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = (M + log2f(L)) * 0.6931471805599453f;
+    }
+    cluster.sync();                                    // no CTA leaves while a peer reads its shared memory
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -438,19 +537,40 @@ Plan make_plan(const AttnProblem &p) {
   }
   pl.T = best_t;
   pl.nsplit = (pl.kt + pl.T - 1) / pl.T;
+  if (pl.nsplit > kMaxCluster) {           // long key ranges: two tiles per CTA before anything else
+    pl.T = 2;
+    pl.nsplit = (pl.kt + 1) / 2;
+  }
+  pl.cluster = pl.nsplit > 1 && pl.nsplit <= kMaxCluster;
   return pl;
+}
+
+template <int D, int T, bool CL>
+cudaError_t launch_dtc(const Plan &pl, const CUtensorMap *maps, const Args &a, cudaStream_t st) {
+  auto k = attn_tc_kernel<D, T, CL>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D, T>::BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pl.units * pl.nsplit));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<D, T>::BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL ? (unsigned)pl.nsplit : 1u;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a);
+  count_launches(1);
+  return e;
 }
 
 template <int D, int T>
 cudaError_t launch_dt(const AttnProblem &p, const Plan &pl, const CUtensorMap *maps, const Args &a, cudaStream_t st) {
-  auto k = attn_tc_kernel<D, T>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D, T>::BYTES);
-  if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(pl.units * pl.nsplit);
-  k<<<grid, kThreads, Smem<D, T>::BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a);
-  count_launches(1);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || pl.nsplit == 1) return e;
+  cudaError_t e = pl.cluster ? launch_dtc<D, T, true>(pl, maps, a, st) : launch_dtc<D, T, false>(pl, maps, a, st);
+  if (e != cudaSuccess || pl.nsplit == 1 || pl.cluster) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(((int64_t)pl.units * kTile + 7) / 8));
   cfg.blockDim = dim3(256);
@@ -472,7 +592,7 @@ bool attn_tc_supported(const AttnProblem &p) { return p.in_bf16 && (p.d == 64 ||
 
 size_t attn_tc_workspace(const AttnProblem &p) {
   const Plan pl = make_plan(p);
-  if (pl.nsplit == 1) return 0;
+  if (pl.nsplit == 1 || pl.cluster) return 0;
   const size_t slots = (size_t)pl.units * pl.nsplit * kTile;
   return slots * p.d * 4 + slots * 8 + 256;
 }

@@ -7,6 +7,7 @@
 // row (partials [b * B, splits], indexed by block row).
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace fdllm {
 namespace {
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   VocabStat *st = (VocabStat *)(smem_raw + ((p.batch * p.B * 4 + 15) & ~15));  // [kWarps][R]
   const int R = compact_masked_rows(p.tokens, p.batch, p.seq_len, p.s, p.B, p.mask_id, rows);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tc::pdl_launch_dependents();
   for (int r = threadIdx.x; r < kWarps * R; r += blockDim.x) st[r] = vs_identity();
   __syncthreads();
 

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  tc::pdl_launch_dependents();
   const uint32_t active = sh.active;
   const uint32_t tmem = sh.tmem_base;
   int nact = 0;

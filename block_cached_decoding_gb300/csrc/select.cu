@@ -7,12 +7,14 @@
 //   top-k:     ranks < k
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace fdllm {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kMaxBlock = 256;
+constexpr int kMaxSplitsPerLane = 10;  // splits <= 320 handled with independent preloads
 
 __global__ void __launch_bounds__(kThreads)
     select_kernel(SelectProblem p, const VocabStat *__restrict__ part, int splits) {
@@ -21,6 +23,8 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float cf[kMaxBlock];
   __shared__ int tok[kMaxBlock];
   __shared__ int s_m, s_any, s_nbest, s_nsel;
+  // launched as a programmatic dependent of the LM-head kernel: wait for its partials
+  tc::pdl_wait_primary();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
   const int32_t *trow = p.tokens + (int64_t)b * p.seq_len + p.s;
@@ -47,7 +51,19 @@ __global__ void __launch_bounds__(kThreads)
   for (int j = warp; j < M; j += kThreads / 32) {
     const VocabStat *pr = part + ((int64_t)b * B + mpos[j]) * splits;
     VocabStat acc = vs_identity();
-    for (int g = lane; g < splits; g += 32) acc = vs_merge(acc, pr[g]);
+    if (splits <= 32 * kMaxSplitsPerLane) {
+      // issue every load of this lane before merging, so their latencies overlap
+      VocabStat v[kMaxSplitsPerLane];
+#pragma unroll
+      for (int k = 0; k < kMaxSplitsPerLane; ++k) {
+        const int g = lane + 32 * k;
+        v[k] = g < splits ? pr[g] : vs_identity();
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxSplitsPerLane; ++k) acc = vs_merge(acc, v[k]);
+    } else {
+      for (int g = lane; g < splits; g += 32) acc = vs_merge(acc, pr[g]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc = vs_merge(acc, vs_shfl_xor(acc, o));
     if (lane == 0) {
@@ -108,9 +124,21 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st) {
-  select_kernel<<<p.batch, kThreads, 0, st>>>(p, part, splits);
+  // programmatic dependent launch: the CTAs become resident while the LM-head
+  // kernel drains and wait for its memory inside the kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, select_kernel, p, part, splits);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace fdllm

@@ -54,13 +54,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed; false after
-// kWaitLimitNs (the caller records the failure and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// `limit_ns` (the caller records the failure and unwinds).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((i & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 
@@ -208,6 +208,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// 2^x on the special-function unit (flush-to-zero), the hardware instruction itself.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 }  // namespace tc
 }  // namespace fdllm

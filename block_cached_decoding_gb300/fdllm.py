@@ -25,6 +25,7 @@ EXPORTS = (
     "fdllm_status_string", "fdllm_last_error", "fdllm_last_device_error", "fdllm_version",
     "fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
     "fdllm_synth_prompt", "fdllm_launch_counter", "fdllm_confidence_select_noalloc",
+    "fdllm_selftest_bounded_wait",
 )
 
 NOALLOC_SCRATCH_BYTES = 2 << 20
@@ -85,6 +86,8 @@ def lib() -> C.CDLL:
         L.fdllm_last_device_error.restype = i32
         L.fdllm_version.argtypes = []
         L.fdllm_version.restype = i32
+        L.fdllm_selftest_bounded_wait.argtypes = [i32, vp]
+        L.fdllm_selftest_bounded_wait.restype = i32
         L.fdllm_launch_counter.argtypes = []
         L.fdllm_launch_counter.restype = C.c_uint64
         u64 = C.c_uint64
@@ -196,6 +199,10 @@ def fdllm_last_device_error(stream=None) -> tuple[int, int]:
 
 def fdllm_version() -> int:
     return lib().fdllm_version()
+
+
+def fdllm_selftest_bounded_wait(limit_ms: int, stream=None):
+    _check(lib().fdllm_selftest_bounded_wait(limit_ms, _stream(stream)))
 
 
 def fdllm_launch_counter() -> int:

@@ -32,6 +32,7 @@ def main():
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--mode", default="prefix", choices=["dual", "prefix", "none"])
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--time", action="store_true", help="report the mean call time over the reps (CUDA events)")
     a = ap.parse_args()
     wl = configs.LLADA_STEP
     dev = torch.device("cuda", 0)
@@ -50,7 +51,7 @@ def main():
         ws = torch.empty(F.fdllm_select_workspace_size(d), dtype=torch.uint8, device=dev)
         outs = [torch.empty(b, B, dtype=t, device=dev) for t in (torch.uint8, torch.float32, torch.float32, torch.int32)]
         nleft = torch.empty(b, dtype=torch.int32, device=dev)
-        for _ in range(a.reps):
+        def call():
             tokens.copy_(tokens0)
             F.fdllm_confidence_select(d, hid, W, tokens, *outs, nleft, ws)
     elif a.op == "attn":
@@ -72,15 +73,29 @@ def main():
         out = torch.empty(b, nq, a.hq, a.d, dtype=torch.bfloat16, device=dev)
         wsb = F.fdllm_attn_workspace_size(d)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
-        for _ in range(a.reps):
+        def call():
             F.fdllm_block_attn(d, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)
     else:
         kc = torch.zeros(b, n, a.hkv, a.d, dtype=torch.bfloat16, device=dev)
         vc = torch.zeros_like(kc)
         ks = torch.ones(b, n, a.hkv, a.d, dtype=torch.bfloat16, device=dev)
         vs = torch.ones_like(ks)
-        for _ in range(a.reps):
+        def call():
             F.fdllm_kv_splice(F.SPLICE_REFRESH, b, n, a.hkv, a.d, 0, n, code, kc, vc, ks, vs)
+    if a.time:
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(a.reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        print(f"{a.op} {vars(a)}: {e0.elapsed_time(e1) / a.reps * 1e3:.2f} us per call (mean of {a.reps}, L2 warm)")
+    else:
+        for _ in range(a.reps):
+            call()
     torch.cuda.synchronize()
     st, detail = F.fdllm_last_device_error()
     if st != F.OK:

@@ -248,6 +248,14 @@ const char *fdllm_last_error(void);
  * FDLLM_ETIMEOUT (`detail`, if not NULL, receives the site code). */
 fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
 
+/* Failure-detection self-test: launches one CTA that waits, through the same
+ * bounded mbarrier wait the kernels use, on a barrier nothing ever arrives at,
+ * with a limit of `limit_ms` milliseconds (1..1000).  The wait gives up,
+ * records site code 900 in the device error word and the kernel returns, so
+ * fdllm_last_device_error then reports FDLLM_ETIMEOUT and the CUDA context stays
+ * usable.  Returns FDLLM_EINVAL for a limit outside 1..1000. */
+fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream);
+
 /* ABI version: 100 * major + minor. */
 int32_t fdllm_version(void);
 

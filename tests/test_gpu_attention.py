@@ -71,7 +71,8 @@ def test_bf16_gqa(hq, hkv):
     dict(batch=1, prompt_len=0, gen_length=16, block_size=16, block_idx=0),    # no prompt, one block
     dict(batch=3, prompt_len=37, gen_length=60, block_size=20, block_idx=2),   # ragged block, last block
     dict(batch=1, prompt_len=5, gen_length=3, block_size=1, block_idx=1),      # block of one
-    dict(batch=1, prompt_len=300, gen_length=257 * 4, block_size=257, block_idx=3)])
+    dict(batch=1, prompt_len=300, gen_length=257 * 4, block_size=257, block_idx=3),
+    dict(batch=2, prompt_len=3000, gen_length=128, block_size=32, block_idx=1)])   # > 16 key tiles: fp32 partials
 def test_bf16_ragged(case):
     run_case(hq=4, hkv=2, d=128, mode="dual", dtype="bf16", seed=5, **case)
 

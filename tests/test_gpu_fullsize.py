@@ -1,0 +1,138 @@
+"""Parity at the full workload sizes (LLaDA-8B and Dream-7B shapes), in the
+launch configuration the benchmark times.
+
+The oracle cannot afford whole steps at these sizes for every step, so each
+test checks (a) every step's properties (at least one unmask per sequence
+that still has a masked position, tau >= 1 unmasks exactly one, a block ends
+within block_size steps, every position ends decoded), and (b) at sampled
+steps, the confidence select of every masked row (full-vocabulary float64
+oracle on the GPU's state) and the attention of sampled (sequence, query,
+head) rows."""
+import numpy as np
+import pytest
+import torch
+
+from block_cached_decoding_gb300 import configs, synth
+from block_cached_decoding_gb300 import fdllm as F
+from block_cached_decoding_gb300.loop import BlockDecoder
+from fullsize_helpers import weight_f64
+from gpu_helpers import assert_attention_close, compare_select, ensure_built, f64
+from oracle import fdllm_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _check_attention(wl, dec, r, rng, n_seq=2, n_rows=12):
+    g, k, s = r.step, r.block, r.block_start
+    p0, p1 = dec.query_range(k)
+    pos = list(range(p0, p1))
+    out = r.attn_out.float().cpu().numpy().astype(np.float64)
+    seqs = sorted(set(rng.choice(wl.batch, size=min(n_seq, wl.batch), replace=False).tolist()))
+    for b in seqs:
+        per = wl.seq_len * wl.n_kv_heads * wl.head_dim
+        cshape = (1, wl.seq_len, wl.n_kv_heads, wl.head_dim)
+        kc = f64(synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_KCACHE, b, k), per, 1.0, wl.dtype),
+                 wl.dtype).reshape(cshape)
+        vc = f64(synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_VCACHE, b, k), per, 1.0, wl.dtype),
+                 wl.dtype).reshape(cshape)
+        # this sequence's fresh K/V for every fresh position, queries for sampled positions
+        kf = np.stack([synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_KFRESH, b, g, p),
+                                            wl.n_kv_heads * wl.head_dim, 1.0, wl.dtype) for p in pos])
+        vf = np.stack([synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_VFRESH, b, g, p),
+                                            wl.n_kv_heads * wl.head_dim, 1.0, wl.dtype) for p in pos])
+        shp = (1, len(pos), wl.n_kv_heads, wl.head_dim)
+        keys = O.assemble_keys(wl.mode, s, s + wl.block_size, kc, f64(kf, wl.dtype).reshape(shp))
+        vals = O.assemble_keys(wl.mode, s, s + wl.block_size, vc, f64(vf, wl.dtype).reshape(shp))
+        qidx = sorted(rng.choice(len(pos), size=min(n_rows, len(pos)), replace=False).tolist())
+        q = np.stack([synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_Q, b, g, pos[i]),
+                                           wl.n_q_heads * wl.head_dim, 1.0, wl.dtype) for i in qidx])
+        q = f64(q, wl.dtype).reshape(1, len(qidx), wl.n_q_heads, wl.head_dim)
+        o_ref, _ = O.attention_full(q, keys, vals, wl.n_q_heads, wl.n_kv_heads)
+        assert_attention_close(out[b:b + 1, qidx], o_ref)
+
+
+def _check_select(wl, dec, r, w64, tau):
+    g, s = r.step, r.block_start
+    t_after = dec.tokens.cpu().numpy().astype(np.int64)
+    um = r.unmasked.cpu().numpy().astype(bool)
+    t_before = t_after.copy()
+    t_before[:, s:s + wl.block_size][um] = wl.mask_id
+    hid, _, _ = synth.hidden_states(wl.seed, wl.batch, g, range(s, s + wl.block_size), wl.hidden, wl.vocab,
+                                    wl.sigma_w, wl.dtype, wl.p_plant)
+    _, info = O.decode_step(t_before, f64(hid, wl.dtype), w64, s=s, block_size=wl.block_size, mask_id=wl.mask_id,
+                            tau=tau)
+    got = {"unmask": um, "conf": r.conf.cpu().numpy(), "kappa": r.kappa.cpu().numpy(),
+           "token": r.argmax.cpu().numpy()}
+    return compare_select(info, got, tau)
+
+
+def run_loop(wl, tau, sample_steps, w64, check_attn=True):
+    dec = BlockDecoder(wl, tau=tau)
+    rng = np.random.default_rng(int(tau * 100) + wl.seed)
+    stats = {"steps": 0, "exempt": 0, "checked": 0}
+
+    def hook(d, r):
+        um = r.unmasked.cpu().numpy().astype(bool)
+        left = r.n_left.cpu().numpy()
+        had = um.any(axis=1) | (left > 0)          # sequences that had a masked position this step
+        assert np.all(um.sum(axis=1)[had] >= 1)
+        if tau >= 1.0:
+            assert np.all(um.sum(axis=1) <= 1)
+        if stats["steps"] in sample_steps:
+            stats["exempt"] += _check_select(wl, d, r, w64, tau)
+            if check_attn:
+                _check_attention(wl, d, r, rng)
+            stats["checked"] += 1
+        stats["steps"] += 1
+
+    tokens, steps = dec.run(hook=hook)
+    t = tokens.cpu().numpy()
+    assert not (t == wl.mask_id).any() and t.max() < wl.vocab
+    assert max(steps) <= wl.block_size
+    return stats, steps
+
+
+def test_llada_single_step_as_benchmarked():
+    """The benchmark's step: PrefixCache block 0, 256 queries over 768 positions, 32 masked rows."""
+    wl = configs.LLADA_STEP
+    w64 = weight_f64(wl.seed, wl.vocab, wl.hidden, wl.sigma_w)
+    dec = BlockDecoder(wl, tau=0.9)
+    dec.refresh(0)
+    r = dec.step(0, 0)
+    torch.cuda.synchronize()
+    _check_select(wl, dec, r, w64, 0.9)
+    _check_attention(wl, dec, r, np.random.default_rng(0), n_seq=1, n_rows=48)
+    assert int(r.unmasked.sum()) >= 1
+
+
+@pytest.mark.parametrize("tau", [0.9, 1.0])
+def test_llada_dual_loop_1024(tau):
+    wl = configs.LLADA_LOOP
+    w64 = weight_f64(wl.seed, wl.vocab, wl.hidden, wl.sigma_w)
+    sample = {0, 1, 40, 200} if tau >= 1.0 else {0, 1, 30}
+    stats, steps = run_loop(wl, tau, sample, w64)
+    assert stats["checked"] == len(sample)
+    if tau >= 1.0:
+        assert steps == [wl.block_size] * (wl.gen_length // wl.block_size)    # exactly 1024 steps
+    else:
+        assert sum(steps) < wl.gen_length
+
+
+@pytest.mark.parametrize("tau", [0.7, 0.8, 0.9, 0.95])
+def test_llada_batch16_tau_sweep(tau):
+    wl = configs.LLADA_BATCH
+    w64 = weight_f64(wl.seed, wl.vocab, wl.hidden, wl.sigma_w)
+    stats, steps = run_loop(wl, tau, {0, 3}, w64, check_attn=(tau == 0.9))
+    assert stats["checked"] == 2
+
+
+def test_dream_gqa_dual_batch8():
+    wl = configs.DREAM
+    w64 = weight_f64(wl.seed, wl.vocab, wl.hidden, wl.sigma_w)
+    stats, steps = run_loop(wl, 0.9, {0, 2, 100}, w64)
+    assert stats["checked"] == 3
