@@ -181,10 +181,12 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   return FDLLM_OK;
 }
 
-// workspace: partials VocabStat [b * B, splits] (16 bytes each); the tensor-core
-// kernel serves bf16 blocks of up to 512 rows, the CUDA-core kernel the rest
+// workspace: [two 8-byte arrival tickets, merged RowStat per block row] [partials
+// VocabStat [b * B, splits], 16 bytes each]; the tensor-core kernel serves bf16
+// blocks of up to 512 rows (and runs the select itself), the CUDA-core kernel the
+// rest (followed by select_kernel)
 struct SelectLayout {
-  size_t total;
+  size_t part_off, total;
   int splits;
   bool tc;
 };
@@ -193,8 +195,19 @@ SelectLayout select_layout(const SelectProblem &p) {
   SelectLayout L;
   L.tc = lmhead_tc_supported(p);
   L.splits = L.tc ? lmhead_tc_grid(p) : lmhead_simt_splits(p);
-  L.total = align_up((size_t)p.batch * p.B * L.splits * sizeof(VocabStat), 256);
+  // [2 tickets + merged RowStat per block row] then the partials
+  L.part_off = align_up(16 + (size_t)p.batch * p.B * 8, 256);
+  L.total = L.part_off + align_up((size_t)p.batch * p.B * L.splits * sizeof(VocabStat), 256);
   return L;
+}
+
+// LM head + select on the partials at `ws` (laid out by select_layout)
+cudaError_t run_select(const SelectProblem &p, const SelectLayout &L, void *ws, cudaStream_t st) {
+  VocabStat *part = (VocabStat *)((char *)ws + L.part_off);
+  if (L.tc) return launch_lmhead_tc(p, part, (unsigned long long *)ws, L.splits, st);
+  cudaError_t e = launch_lmhead_simt(p, part, L.splits, st);
+  if (e != cudaSuccess) return e;
+  return launch_select(p, part, L.splits, st);
 }
 
 }  // namespace
@@ -314,12 +327,7 @@ fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *
   p.hidden = hidden; p.w = lm_head_w; p.tokens = tokens; p.unmasked = unmasked; p.conf = conf;
   p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
   p.err = error_word_ptr();
-  VocabStat *part = (VocabStat *)workspace;
-  cudaStream_t cs = (cudaStream_t)stream;
-  st = cuda_status(L.tc ? launch_lmhead_tc(p, part, L.splits, cs) : launch_lmhead_simt(p, part, L.splits, cs),
-                   "lm-head launch");
-  if (st != FDLLM_OK) return st;
-  return cuda_status(launch_select(p, part, L.splits, cs), "select launch");
+  return cuda_status(run_select(p, L, workspace, (cudaStream_t)stream), "lm-head / select launch");
 }
 
 fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
@@ -410,10 +418,5 @@ extern "C" fdllm_status fdllm_confidence_select_noalloc(const fdllm_select_desc 
   p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left;
   p.ws = scratch; p.ws_bytes = FDLLM_NOALLOC_SCRATCH_BYTES;
   p.err = error_word_ptr();
-  VocabStat *part = (VocabStat *)scratch;
-  cudaStream_t cs = (cudaStream_t)stream;
-  st = cuda_status(L.tc ? launch_lmhead_tc(p, part, L.splits, cs) : launch_lmhead_simt(p, part, L.splits, cs),
-                   "noalloc select: lm-head launch");
-  if (st != FDLLM_OK) return st;
-  return cuda_status(launch_select(p, part, L.splits, cs), "noalloc select: select launch");
+  return cuda_status(run_select(p, L, scratch, (cudaStream_t)stream), "noalloc select: lm-head / select launch");
 }

@@ -4,24 +4,29 @@
 // that no row outside a range is ever read: the cached prefix [0, f0), the fresh
 // keys of this step (nq rows, the query positions) and the cached suffix
 // [f1, N).  Softmax is invariant to the order of the keys, so the key tiles of
-// 128 rows are enumerated range by range.
+// 64 rows are enumerated range by range.
 //
 // One CTA = (sequence, KV head, 128-row query tile, split of the key tiles);
 // all query heads sharing the KV head are packed into the 128 rows when
 // nq <= 128.  Within the CTA the key tiles are pipelined:
 //   warp 0     TMA: the query tile once, then K and V tiles into a ring
-//   warp 1     TMEM owner, MMA issuer: S_i = Q K_i^T (M=128, N=128 keys,
+//   warp 1     TMEM owner, MMA issuer: S_i = Q K_i^T (M=128, N=64 keys,
 //              K=d) into one of two TMEM score buffers, then PV_i = P_i V_i
-//              (N=d, K=128 keys, V read MN-major) into one of two TMEM
-//              buffers; S_{i+1} is issued before PV_i
-//   warps 4-7  one thread per query row, online softmax in base 2: the tile
-//              max, P_i = 2^(S_i - m) written as bf16 (128-byte swizzle) into
-//              one of two P buffers, then O = O * alpha_i + PV_i in registers.
+//              (N=d, K=64 keys, V read MN-major) into one of two TMEM
+//              buffers; S_{i+1} is issued before PV_i; the K/V ring holds
+//              5 tiles (d = 128) so loads run ahead of the MMAs
+//   warps 4-7  one thread per query row, online softmax in base 2 with a lazy
+//              reference max: P_i = 2^(S_i - m_ref) is written as bf16 (128-byte
+//              swizzle) into one of two P buffers and the tensor core
+//              accumulates O += P_i V_i in TMEM.  m_ref moves only when a row's
+//              max exceeds it by more than 2^8; then that row of O (and l) is
+//              rescaled in TMEM once the previous PV product has landed.
 //              Tile i+1's softmax runs while the tensor core computes PV_i.
 // Splits of one unit form a thread block cluster (<= 8) and merge through
-// distributed shared memory: every CTA publishes its rows' (max, l), weights
-// its O rows by l_s 2^(m_s - M) / L into its own shared memory, and CTA c sums
-// rows [c R/C, (c+1) R/C) over the cluster and writes them.
+// distributed shared memory with stores only: every CTA writes its rows'
+// (max, l) into every peer, then its O rows weighted by l_s 2^(m_s - M) / L
+// into the peer that owns them (CTA c owns rows [c R/C, (c+1) R/C)), and each
+// owner sums its rows locally and writes them.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -34,7 +39,8 @@ namespace fdllm {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTile = 128;       // keys per tile and rows per query tile
+constexpr int kTile = 128;       // rows per query tile
+constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -53,23 +59,29 @@ struct Plan {
 template <int D>
 struct Cfg {
   static constexpr int DH = D / 64;                   // 64-column halves of a row
-  static constexpr int TILE_BYTES = kTile * D * 2;    // 128 rows x d bf16
-  static constexpr int HALF_BYTES = kTile * 128;      // 128 rows x 64 bf16
-  static constexpr int P_BYTES = kTile * kTile * 2;   // 128 rows x 128 keys bf16
-  static constexpr int NS = D == 128 ? 2 : 3;         // K/V ring stages
-  static constexpr int STAGE = 2 * TILE_BYTES;        // K + V
-  static constexpr int SMEM = TILE_BYTES + NS * STAGE + 2 * P_BYTES + 1024 + 2048;
-  static constexpr uint32_t S_COL = 0;                // TMEM: S0, S1, PV0, PV1
-  static constexpr uint32_t PV_COL = 2 * kTile;
+  static constexpr int Q_BYTES = kTile * D * 2;       // 128 query rows x d bf16
+  static constexpr int QHALF = kTile * 128;           // 128 rows x 64 bf16
+  static constexpr int KV_BYTES = kKeys * D * 2;      // 64 key rows x d bf16
+  static constexpr int KVHALF = kKeys * 128;          // 64 rows x 64 bf16
+  static constexpr int P_BYTES = kTile * kKeys * 2;   // 128 rows x 64 keys bf16 (one swizzle atom column)
+  static constexpr int STAGE = 2 * KV_BYTES;          // K + V
+  static constexpr int NS = D == 128 ? 5 : 8;         // K/V ring stages
+  // cluster merge: weighted O rows received by an owner, C * ceil(128 / C) <= 136 rows, then (max, l) of 8 peers
+  static constexpr int MERGE_ROWS = 136;
+  static constexpr int MERGE_BYTES = MERGE_ROWS * D * 4 + 8 * kTile * 8;
+  static constexpr int RING = NS * STAGE > MERGE_BYTES ? NS * STAGE : MERGE_BYTES;
+  static constexpr int SMEM = Q_BYTES + RING + 2 * P_BYTES + 1024 + 1024;
+  static constexpr uint32_t S_COL = 0;                // TMEM: S0, S1 (64 columns each), then O (D columns)
+  static constexpr uint32_t O_COL = 2 * kKeys;
+  static constexpr uint32_t TMEM_COLS = 256;
 };
 
 struct Bars {
-  uint64_t qfull, kvfull[3], kvempty[3], sfull[2], sempty[2], pfull[2], pvfull[2], pvempty[2], drain;
+  uint64_t qfull, kvfull[8], kvempty[8], sfull[2], sempty[2], pfull[2], pvdone, drain;
   uint32_t tmem_base;
   int32_t abort;
   int32_t issued;     // K/V tiles issued by the producer
   int32_t consumed;   // K/V tiles whose arrival the MMA issuer waited for
-  float2 ml[kTile];   // this CTA's (max in log2 units, l) per row, read by the cluster
 };
 
 struct KeyTile {
@@ -81,11 +93,11 @@ struct KeyTile {
 __device__ __forceinline__ KeyTile key_tile(const Plan &pl, int nq, int n, int k) {
   KeyTile t;
   if (k < pl.ka) {
-    t.range = 0; t.row0 = k * kTile; t.nvalid = min(kTile, pl.f0 - t.row0);
+    t.range = 0; t.row0 = k * kKeys; t.nvalid = min(kKeys, pl.f0 - t.row0);
   } else if (k < pl.ka + pl.kf) {
-    t.range = 1; t.row0 = (k - pl.ka) * kTile; t.nvalid = min(kTile, nq - t.row0);
+    t.range = 1; t.row0 = (k - pl.ka) * kKeys; t.nvalid = min(kKeys, nq - t.row0);
   } else {
-    t.range = 2; t.row0 = (k - pl.ka - pl.kf) * kTile; t.nvalid = min(kTile, n - pl.f1 - t.row0);
+    t.range = 2; t.row0 = (k - pl.ka - pl.kf) * kKeys; t.nvalid = min(kKeys, n - pl.f1 - t.row0);
   }
   return t;
 }
@@ -123,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NS = CF::NS;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *q_s = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char *kv_s = q_s + CF::TILE_BYTES;           // NS stages of (K tile, V tile)
-  unsigned char *p_s = kv_s + NS * CF::STAGE;           // 2 P buffers
+  unsigned char *kv_s = q_s + CF::Q_BYTES;              // NS stages of (K tile, V tile)
+  unsigned char *p_s = kv_s + CF::RING;                 // 2 P buffers
   Bars &br = *(Bars *)(p_s + 2 * CF::P_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Plan &pl = a.pl;
@@ -146,29 +158,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     br.abort = 0; br.issued = 0; br.consumed = 0;
     tc::mbar_init(&br.qfull, 1);
-    for (int i = 0; i < 3; ++i) { tc::mbar_init(&br.kvfull[i], 1); tc::mbar_init(&br.kvempty[i], 1); }
+    for (int i = 0; i < NS; ++i) { tc::mbar_init(&br.kvfull[i], 1); tc::mbar_init(&br.kvempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&br.sfull[i], 1);
       tc::mbar_init(&br.sempty[i], 4);
       tc::mbar_init(&br.pfull[i], 4);
-      tc::mbar_init(&br.pvfull[i], 1);
-      tc::mbar_init(&br.pvempty[i], 4);
     }
+    tc::mbar_init(&br.pvdone, 1);
     tc::mbar_init(&br.drain, 1);
     tc::fence_barrier_init();
   }
-  if (warp == 1) tc::tmem_alloc(&br.tmem_base, 512);
+  if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = br.tmem_base;
 
-  // thread of the softmax warps: its query row and running state
+  // thread of the softmax warps: its query row and running state (reference max, l)
   const int r = (warp - 4) * 32 + lane;
   float m_run = kNegInf, l_run = 0.f;
-  float o[D];
-#pragma unroll
-  for (int c = 0; c < D; ++c) o[c] = 0.f;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -177,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive_expect_tx(&br.qfull, (uint32_t)(pl.qr * 128 * CF::DH * nh));
       for (int hs = 0; hs < nh; ++hs)
         for (int dh = 0; dh < CF::DH; ++dh)
-          tc::tma_load_4d(q_s + dh * CF::HALF_BYTES + hs * pl.qr * 128, &mq, &br.qfull, dh * 64,
+          tc::tma_load_4d(q_s + dh * CF::QHALF + hs * pl.qr * 128, &mq, &br.qfull, dh * 64,
                           kvh * a.group + h0 + hs, q0, b, pol_q);
       for (int i = 0; i < nt && !br.abort; ++i) {
         const int st = i % NS;
@@ -188,16 +196,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char *ks = kv_s + st * CF::STAGE;
         tc::mbar_arrive_expect_tx(&br.kvfull[st], (uint32_t)CF::STAGE);
         for (int dh = 0; dh < CF::DH; ++dh) {
-          tc::tma_load_4d(ks + dh * CF::HALF_BYTES, mk, &br.kvfull[st], dh * 64, kvh, kt.row0, b, pol_kv);
-          tc::tma_load_4d(ks + CF::TILE_BYTES + dh * CF::HALF_BYTES, mv, &br.kvfull[st], dh * 64, kvh, kt.row0, b,
-                          pol_kv);
+          tc::tma_load_4d(ks + dh * CF::KVHALF, mk, &br.kvfull[st], dh * 64, kvh, kt.row0, b, pol_kv);
+          tc::tma_load_4d(ks + CF::KV_BYTES + dh * CF::KVHALF, mv, &br.kvfull[st], dh * 64, kvh, kt.row0, b, pol_kv);
         }
         atomicExch(&br.issued, i + 1);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = tc::idesc_bf16_f32(128, kTile, 0);
+      const uint32_t id_s = tc::idesc_bf16_f32(128, kKeys, 0);
       const uint32_t id_o = tc::idesc_bf16_f32(128, D, 1);
       const uint32_t qa = tc::smem_u32(q_s);
       bool ok = tc::mbar_wait(&br.qfull, 0);
@@ -211,9 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks / 4) * CF::HALF_BYTES + (ks % 4) * 32);
-          tc::mma_bf16(tmem + CF::S_COL + (uint32_t)(j * kTile), tc::sw128_desc(qa + off), tc::sw128_desc(ka + off),
-                       id_s, ks != 0);
+          const uint32_t kin = (uint32_t)((ks % 4) * 32);
+          tc::mma_bf16(tmem + CF::S_COL + (uint32_t)(j * kKeys), tc::sw128_desc(qa + (ks / 4) * CF::QHALF + kin),
+                       tc::sw128_desc(ka + (ks / 4) * CF::KVHALF + kin), id_s, ks != 0);
         }
         tc::mma_commit(&br.sfull[j]);
         return true;
@@ -221,17 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int i) -> bool {
         const int st = i % NS, j = i & 1;
         if (!tc::mbar_wait(&br.pfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 215); return false; }
-        if (!tc::mbar_wait(&br.pvempty[j], ((uint32_t)(i >> 1) & 1u) ^ 1u)) { fail(br, a.err, 216); return false; }
         tc::fence_after_sync();
         const uint32_t pa = tc::smem_u32(p_s + j * CF::P_BYTES);
-        const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::TILE_BYTES);
+        const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
 #pragma unroll
-        for (int ks = 0; ks < kTile / 16; ++ks) {
-          const uint32_t poff = (uint32_t)((ks / 4) * (kTile * 128) + (ks % 4) * 32);
-          tc::mma_bf16(tmem + CF::PV_COL + (uint32_t)(j * kTile), tc::sw128_desc(pa + poff),
-                       tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::HALF_BYTES), id_o, ks != 0);
-        }
-        tc::mma_commit(&br.pvfull[j]);
+        for (int ks = 0; ks < kKeys / 16; ++ks)
+          tc::mma_bf16(tmem + CF::O_COL, tc::sw128_desc(pa + (uint32_t)(ks * 32)),
+                       tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::KVHALF), id_o, (i | ks) != 0);
+        tc::mma_commit(&br.pvdone);
         tc::mma_commit(&br.kvempty[st]);
         return true;
       };
@@ -245,45 +249,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const uint32_t oa = tmem + lane_base + CF::O_COL;
     bool ok = true;
-    float alpha0 = 0.f, alpha1 = 0.f;   // rescale of tile i (slot i & 1), applied when PV_i arrives
-    // softmax of tile i: new running max, P_i into shared memory, running l
+    // wait until PV_i has been accumulated into O (phases complete in order, one per tile)
+    auto wait_pv = [&](int i) -> bool {
+      if (!tc::mbar_wait(&br.pvdone, (uint32_t)i & 1u)) { fail(br, a.err, 219); return false; }
+      tc::fence_after_sync();
+      return true;
+    };
+    // softmax of tile i: P_i = 2^((S_i - m_ref) * scale * log2 e) into shared memory, running l
     auto softmax = [&](int i) -> bool {
       const int j = i & 1;
       if (!tc::mbar_wait(&br.sfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 218); return false; }
       tc::fence_after_sync();
       const int nv = key_tile(pl, a.nq, a.n, k0 + i).nvalid;
-      const uint32_t sa = tmem + lane_base + CF::S_COL + (uint32_t)(j * kTile);
+      const uint32_t sa = tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys);
       float tm = kNegInf;
-#pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 64) {
+      {
         uint32_t x[32], y[32];
-        tc::tmem_ld_32x32b_x32(sa + (uint32_t)c0, x);
-        tc::tmem_ld_32x32b_x32(sa + (uint32_t)(c0 + 32), y);
+        tc::tmem_ld_32x32b_x32(sa, x);
+        tc::tmem_ld_32x32b_x32(sa + 32u, y);
         tc::tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          if (c0 + e < nv) tm = fmaxf(tm, __uint_as_float(x[e]));
-          if (c0 + 32 + e < nv) tm = fmaxf(tm, __uint_as_float(y[e]));
+          if (e < nv) tm = fmaxf(tm, __uint_as_float(x[e]));
+          if (32 + e < nv) tm = fmaxf(tm, __uint_as_float(y[e]));
         }
       }
-      const float m_new = fmaxf(m_run, tm);
-      const float al = tc::ex2_approx((m_run - m_new) * a.scale_log2);   // 0 on the first tile
-      if (j == 0) alpha0 = al; else alpha1 = al;
-      m_run = m_new;
-      const float ms = m_new * a.scale_log2;
+      // move the reference max only when the row max outgrows it by more than 2^8
+      const bool need = m_run == kNegInf || (tm - m_run) * a.scale_log2 > 8.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? fmaxf(m_run, tm) : m_run;
+        const float al = tc::ex2_approx((m_run - m_new) * a.scale_log2);   // 0 on a row's first tile
+        if (i > 0) {
+          if (!wait_pv(i - 1)) return false;       // O holds PV_0 .. PV_{i-1}
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t x[32];
+            tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * al);
+            tc::tmem_st_32x32b_x32(oa + (uint32_t)c0, x);
+          }
+          tc::tmem_st_wait();
+        }
+        l_run *= al;
+        m_run = m_new;
+      }
+      const float ms = m_run * a.scale_log2;
       unsigned char *pb = p_s + j * CF::P_BYTES;
       float lt = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < kTile; c0 += 32) {
+      for (int c0 = 0; c0 < kKeys; c0 += 32) {
         uint32_t x[32];
         tc::tmem_ld_32x32b_x32(sa + (uint32_t)c0, x);
         tc::tmem_ld_wait();
-        // 32 keys = 4 chunks of 8 in the 128-byte row of swizzle atom column c0 / 64
-        unsigned char *rowp = pb + (c0 / 64) * (kTile * 128) + r * 128;
+        // 32 keys = 4 chunks of 8 in this row's 128 bytes (64 keys, one swizzle atom column)
+        unsigned char *rowp = pb + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const int ch = (c0 % 64) / 8 + cc;
+          const int ch = c0 / 8 + cc;
           uint32_t pk[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
@@ -298,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *(uint4 *)(rowp + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
-      l_run = l_run * al + lt;
+      l_run += lt;
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
@@ -308,101 +334,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    // O = O * alpha_i + PV_i
-    auto accumulate = [&](int i) -> bool {
-      const int j = i & 1;
-      if (!tc::mbar_wait(&br.pvfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 219); return false; }
-      tc::fence_after_sync();
-      const float al = j == 0 ? alpha0 : alpha1;
-      const uint32_t pa = tmem + lane_base + CF::PV_COL + (uint32_t)(j * kTile);
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 64) {
-        uint32_t x[32], y[32];
-        tc::tmem_ld_32x32b_x32(pa + (uint32_t)c0, x);
-        tc::tmem_ld_32x32b_x32(pa + (uint32_t)(c0 + 32), y);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          o[c0 + e] = fmaf(o[c0 + e], al, __uint_as_float(x[e]));
-          o[c0 + 32 + e] = fmaf(o[c0 + 32 + e], al, __uint_as_float(y[e]));
-        }
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&br.pvempty[j]);
-      return true;
-    };
-    if (nt > 0) ok = softmax(0);
-    for (int i = 0; i < nt && ok; ++i) {
-      if (i + 1 < nt && !(ok = softmax(i + 1))) break;
-      ok = accumulate(i);
-    }
+    for (int i = 0; i < nt && ok; ++i) ok = softmax(i);
+    if (ok && nt > 0) ok = wait_pv(nt - 1);        // O is complete
     if (!ok) l_run = 0.f;
     if (pl.nsplit == 1 && ok) {
       int hs, qi;
-      if (row_target(pl, a.nq, nh, q0, r, hs, qi)) {
-        const int h = kvh * a.group + h0 + hs;
-        const float inv = 1.f / l_run;
-        const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D;
+      const bool valid = row_target(pl, a.nq, nh, q0, r, hs, qi);
+      const int h = kvh * a.group + h0 + hs;
+      const float inv = 1.f / l_run;
+      const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t x[32];
+        tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
+        tc::tmem_ld_wait();
+        if (!valid) continue;
         if (a.out_f32) {
-          float4 *dst = (float4 *)((float *)a.out + obase);
+          float4 *dst = (float4 *)((float *)a.out + obase + c0);
 #pragma unroll
-          for (int i = 0; i < D / 4; ++i)
-            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(__uint_as_float(x[4 * q4]) * inv, __uint_as_float(x[4 * q4 + 1]) * inv,
+                                  __uint_as_float(x[4 * q4 + 2]) * inv, __uint_as_float(x[4 * q4 + 3]) * inv);
         } else {
-          uint4 *dst = (uint4 *)((__nv_bfloat16 *)a.out + obase);
+          uint4 *dst = (uint4 *)((__nv_bfloat16 *)a.out + obase + c0);
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
+          for (int q8 = 0; q8 < 4; ++q8) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * i + 2 * e] * inv, o[8 * i + 2 * e + 1] * inv);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(x[8 * q8 + 2 * e]) * inv,
+                                                        __uint_as_float(x[8 * q8 + 2 * e + 1]) * inv);
               w[e] = *(uint32_t *)&h2;
             }
-            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[q8] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
-        if (a.lse) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = m_run * a.scale + __logf(l_run);
       }
+      if (valid && a.lse) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = m_run * a.scale + __logf(l_run);
     }
-    br.ml[r] = l_run > 0.f ? make_float2(m_run * a.scale_log2, l_run) : make_float2(kNegInf, 0.f);
   }
 
   if (pl.nsplit > 1) {
-    // ---- merge the splits of this unit through the cluster's shared memory ----
+    // ---- merge the splits of this unit through the cluster's shared memory, stores only ----
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int C = pl.nsplit;
     const int crank = (int)cluster.block_rank();
-    constexpr int CH = D / 4;                    // float4 chunks per row
-    float *ored = (float *)kv_s;                 // [128][D] fp32 (the K/V ring is free now)
+    constexpr int CH = D / 4;                        // float4 chunks per row
+    (void)CH;
+    const int rpc = (kTile + C - 1) / C;             // rows owned per CTA
+    // the K/V ring is free once every CTA of the cluster has passed the first barrier
+    float *orecv = (float *)kv_s;                    // [C][rpc][D]: weighted rows received from each split
+    float2 *mlrecv = (float2 *)(kv_s + CF::MERGE_ROWS * D * 4);  // [C][128]: every split's (max, l) per row
     tc::fence_before_sync();
-    cluster.sync();                              // every split's (max, l) is published
+    cluster.sync();                                  // all MMAs and copies of every CTA are done
+    const float2 mine = l_run > 0.f ? make_float2(m_run * a.scale_log2, l_run) : make_float2(kNegInf, 0.f);
+    if (warp >= 4)
+      for (int c = 0; c < C; ++c) *cluster.map_shared_rank(mlrecv + crank * kTile + r, c) = mine;
+    cluster.sync();                                  // (max, l) of every split has arrived everywhere
     float M = kNegInf, L = 0.f;
     if (warp >= 4) {
-      for (int c = 0; c < C; ++c) M = fmaxf(M, cluster.map_shared_rank(&br.ml[r], c)->x);
+      for (int c = 0; c < C; ++c) M = fmaxf(M, mlrecv[c * kTile + r].x);
       for (int c = 0; c < C; ++c) {
-        const float2 v = *cluster.map_shared_rank(&br.ml[r], c);
+        const float2 v = mlrecv[c * kTile + r];
         if (v.y > 0.f) L += v.y * exp2f(v.x - M);
       }
-      const float2 mine = br.ml[r];
       const float w = (mine.y > 0.f && L > 0.f) ? exp2f(mine.x - M) / L : 0.f;
+      const int owner = r / rpc;
+      float4 *dst = (float4 *)cluster.map_shared_rank(orecv + ((size_t)crank * rpc + (r - owner * rpc)) * D, owner);
+      const uint32_t oa = tmem + ((uint32_t)((warp - 4) * 32) << 16) + CF::O_COL;
 #pragma unroll
-      for (int ch = 0; ch < CH; ++ch)
-        *(float4 *)(ored + r * D + ((ch ^ (r & (CH - 1))) * 4)) =
-            make_float4(o[4 * ch] * w, o[4 * ch + 1] * w, o[4 * ch + 2] * w, o[4 * ch + 3] * w);
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t x[32];
+        tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4)
+          dst[c0 / 4 + q4] = make_float4(__uint_as_float(x[4 * q4]) * w, __uint_as_float(x[4 * q4 + 1]) * w,
+                                         __uint_as_float(x[4 * q4 + 2]) * w, __uint_as_float(x[4 * q4 + 3]) * w);
+      }
     }
-    cluster.sync();                              // every split's weighted O is in its shared memory
-    const int rpc = (kTile + C - 1) / C;
+    cluster.sync();                                  // every weighted row is in its owner
     const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);
     for (int u = threadIdx.x; u < (r1 - r0) * CH; u += kThreads) {
-      const int row = r0 + u / CH, ch = u % CH;
+      const int lr = u / CH, ch = u % CH, row = r0 + lr;
       int hs, qi;
       if (!row_target(pl, a.nq, nh, q0, row, hs, qi)) continue;
-      const float *src = ored + row * D + ((ch ^ (row & (CH - 1))) * 4);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 0; c < C; ++c) {
-        const float4 v = *(const float4 *)cluster.map_shared_rank(src, c);
+        const float4 v = *(const float4 *)(orecv + ((size_t)c * rpc + lr) * D + ch * 4);
         acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
       const int64_t off = (((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs) * D + ch * 4;
@@ -418,7 +438,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_target(pl, a.nq, nh, q0, r, hs, qi))
         a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = (M + log2f(L)) * 0.6931471805599453f;
     }
-    cluster.sync();                              // no CTA leaves while a peer reads its shared memory
   }
 
   tc::fence_before_sync();
@@ -430,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_wait(&br.kvfull[i % NS], (uint32_t)(i / NS) & 1u);
   }
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+  if (warp == 1) tc::tmem_dealloc(tmem, CF::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -467,9 +486,9 @@ Plan make_plan(const AttnProblem &p) {
   Plan pl;
   pl.f0 = p.fresh0;
   pl.f1 = p.fresh0 + p.nq;
-  pl.ka = (pl.f0 + kTile - 1) / kTile;
-  pl.kf = (p.nq + kTile - 1) / kTile;
-  pl.kcn = (p.seq_len - pl.f1 + kTile - 1) / kTile;
+  pl.ka = (pl.f0 + kKeys - 1) / kKeys;
+  pl.kf = (p.nq + kKeys - 1) / kKeys;
+  pl.kcn = (p.seq_len - pl.f1 + kKeys - 1) / kKeys;
   pl.kt = pl.ka + pl.kf + pl.kcn;
   const int group = p.hq / p.hkv;
   if (p.nq <= kTile) {
@@ -530,12 +549,12 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
   const int64_t off_c = (int64_t)pl.f1 * p.hkv * p.d;
   if (!map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) ||
-      !map4(&maps[1], p.kc, p.d, p.hkv, pl.f0, p.batch, cstride, kTile) ||
-      !map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, kTile) ||
-      !map4(&maps[3], kc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, kTile) ||
-      !map4(&maps[4], p.vc, p.d, p.hkv, pl.f0, p.batch, cstride, kTile) ||
-      !map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, kTile) ||
-      !map4(&maps[6], vc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, kTile))
+      !map4(&maps[1], p.kc, p.d, p.hkv, pl.f0, p.batch, cstride, kKeys) ||
+      !map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, kKeys) ||
+      !map4(&maps[3], kc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, kKeys) ||
+      !map4(&maps[4], p.vc, p.d, p.hkv, pl.f0, p.batch, cstride, kKeys) ||
+      !map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, kKeys) ||
+      !map4(&maps[6], vc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, kKeys))
     return cudaErrorInvalidValue;
   Args a;
   a.pl = pl;

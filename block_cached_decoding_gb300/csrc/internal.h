@@ -58,10 +58,12 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st);
 int lmhead_simt_splits(const SelectProblem &p);
 cudaError_t launch_lmhead_simt(const SelectProblem &p, VocabStat *part, int splits, cudaStream_t st);
 
-// lmhead_tc.cu: the same partials from the tcgen05 kernel (bf16, batch * B <= 512)
+// lmhead_tc.cu: the tcgen05 kernel (bf16, batch * B <= 512) writes the partials
+// and runs the merge + select itself; `ticket` is 8 bytes of workspace
 bool lmhead_tc_supported(const SelectProblem &p);
 int lmhead_tc_grid(const SelectProblem &p);
-cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, int grid, cudaStream_t st);
+cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int grid,
+                             cudaStream_t st);
 
 // select.cu: merge partials [b * B, splits] over splits and unmask
 cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st);

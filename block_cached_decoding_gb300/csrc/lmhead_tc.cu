@@ -12,7 +12,14 @@
 //   warps 4-7 epilogue: tcgen05.ld of the accumulator (one thread per block
 //           row), folded into the row's VocabStat in increasing vocabulary order
 // At the end every masked row writes its VocabStat for this CTA's range to the
-// partials [b * B, grid]; the select kernel merges them.
+// partials [b * B, grid].  The kernel is launched cooperatively (all CTAs are
+// resident), and its tail runs in three phases separated by grid barriers on
+// 64-bit tickets in the workspace (high half: this call's epoch, low half:
+// count; a ticket left by another call or uninitialised memory is re-armed
+// first, so the workspace needs no zeroing):
+//   1. every CTA arrives after writing its partials and waits for all;
+//   2. one warp per masked block row merges that row's partials into a RowStat;
+//   3. after the second barrier, CTA b selects sequence b (select_impl.cuh).
 //
 // Template MT = 128-row tiles of block rows (1, 2 or 4): the vocabulary tile is
 // NV = 256 / MT rows so that 2 x MT x NV = 512 TMEM columns.  Rows of a tile
@@ -23,9 +30,14 @@
 // copies and MMAs it already issued, frees its TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <unistd.h>
+
+#include <atomic>
+#include <chrono>
 
 #include "common.cuh"
 #include "internal.h"
+#include "select_impl.cuh"
 #include "tc.cuh"
 
 namespace fdllm {
@@ -59,8 +71,40 @@ struct Shared {
   int32_t issued;     // stages issued by the producer
   int32_t consumed;   // stages consumed by the MMA issuer
   uint32_t active;    // bit m: 128-row tile m has a masked row
+  int32_t arrival;    // this CTA's arrival number on the ticket (1-based, 0 on failure)
   uint8_t masked[512];
 };
+
+// Arrival number (1-based) of this CTA in epoch `e` on the ticket word; 0 if the
+// ticket could not be taken.  A word from another epoch (an earlier call, or
+// uninitialised memory) is first re-armed to (e, 0) by compare-and-swap on the
+// value read -- one CTA wins, the others see epoch e on their next read, and
+// the word never holds a stale value again during this call -- then every CTA
+// counts itself with one atomic add.
+__device__ int arrive_ticket(unsigned long long *word, uint32_t e) {
+  const unsigned long long tag = (unsigned long long)e << 32;
+  for (int attempt = 0; attempt < 64; ++attempt) {
+    const unsigned long long v = *(volatile unsigned long long *)word;
+    if ((uint32_t)(v >> 32) != e) {
+      atomicCAS(word, v, tag);
+      continue;
+    }
+    const unsigned long long old = atomicAdd(word, 1ull);
+    if ((uint32_t)(old >> 32) == e) return (int)(uint32_t)old + 1;
+  }
+  return 0;
+}
+
+// Wait (bounded) until all `count` CTAs of epoch `e` have arrived.
+__device__ bool wait_ticket(const unsigned long long *word, uint32_t e, int count) {
+  const unsigned long long want = ((unsigned long long)e << 32) | (unsigned)count;
+  const uint64_t t0 = tc::globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (*(const volatile unsigned long long *)word == want) return true;
+    if ((i & 63u) == 0 && tc::globaltimer() - t0 > tc::kWaitLimitNs) return false;
+    __nanosleep(64);
+  }
+}
 
 __device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site) {
   record_device_error(err, site);
@@ -70,8 +114,11 @@ __device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site) {
 template <int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
-                     const int32_t *__restrict__ tokens, int batch, int seq_len, int s, int B, int mask_id, int H,
-                     int V, VocabStat *__restrict__ part, int32_t *err) {
+                     const SelectProblem sp, VocabStat *__restrict__ part, unsigned long long *ticket,
+                     uint32_t epoch) {
+  const int32_t *__restrict__ tokens = sp.tokens;
+  const int batch = sp.batch, seq_len = sp.seq_len, s = sp.s, B = sp.B, mask_id = sp.mask_id, H = sp.H, V = sp.V;
+  int32_t *err = sp.err;
   using C = Cfg<MT>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *tiles = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -245,6 +292,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+
+  // ---- tail: grid barrier, row merges across the grid, grid barrier, selection ----
+  RowStat *merged = (RowStat *)(ticket + 2);
+  if (threadIdx.x == 0) {
+    __threadfence();                                   // this CTA's partials before its arrival
+    if (arrive_ticket(ticket, epoch) == 0) record_device_error(err, 106);
+    if (!wait_ticket(ticket, epoch, G)) record_device_error(err, 107);
+    __threadfence();
+  }
+  __syncthreads();
+  for (int row = g * (kThreads / 32) + warp; row < rows; row += G * (kThreads / 32)) {
+    if (!sh.masked[row]) continue;
+    const VocabStat acc = merge_row(part + (int64_t)row * G, G);
+    if (lane == 0) {
+      RowStat rs;
+      rs.kappa = vs_kappa(acc);
+      rs.token = acc.a1;
+      merged[row] = rs;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (arrive_ticket(ticket + 1, epoch) == 0) record_device_error(err, 108);
+    if (g < batch && !wait_ticket(ticket + 1, epoch, G)) record_device_error(err, 109);
+    __threadfence();
+  }
+  __syncthreads();
+  SelectScratch &sc = *(SelectScratch *)tiles;         // the tile ring is free now
+  for (int seq = g; seq < batch; seq += G) select_sequence<kThreads>(sp, part, G, seq, sc, merged);
 }
 
 // ---------------------------------------------------------------------------
@@ -277,7 +354,8 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, 
 }
 
 template <int MT>
-cudaError_t launch_mt(const SelectProblem &p, VocabStat *part, int grid, cudaStream_t st) {
+cudaError_t launch_mt(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, uint32_t epoch, int grid,
+                      cudaStream_t st) {
   CUtensorMap mh, mw;
   if (!make_map(&mh, p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H, kABox) ||
       !make_map(&mw, p.w, (uint64_t)p.V, (uint64_t)p.H, kUnit))
@@ -285,10 +363,20 @@ cudaError_t launch_mt(const SelectProblem &p, VocabStat *part, int grid, cudaStr
   auto k = lmhead_tc_kernel<MT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, Cfg<MT>::SMEM, st>>>(mh, mw, p.tokens, p.batch, p.seq_len, p.s, p.B, p.mask_id, p.H, p.V,
-                                          part, p.err);
+  // cooperative launch: every CTA is resident, so the tail's grid barriers cannot wait on an unscheduled CTA
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg<MT>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k, mh, mw, p, part, ticket, epoch);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -303,11 +391,16 @@ int lmhead_tc_grid(const SelectProblem &p) {
   return units < sms ? units : sms;
 }
 
-cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, int grid, cudaStream_t st) {
+cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int grid,
+                             cudaStream_t st) {
+  static std::atomic<uint32_t> epochs{(uint32_t)std::chrono::steady_clock::now().time_since_epoch().count() ^
+                                      ((uint32_t)getpid() << 16)};
+  uint32_t e = epochs.fetch_add(1) + 1;
+  if (e == 0) e = epochs.fetch_add(1) + 1;
   const int rows = p.batch * p.B;
-  if (rows <= 128) return launch_mt<1>(p, part, grid, st);
-  if (rows <= 256) return launch_mt<2>(p, part, grid, st);
-  return launch_mt<4>(p, part, grid, st);
+  if (rows <= 128) return launch_mt<1>(p, part, ticket, e, grid, st);
+  if (rows <= 256) return launch_mt<2>(p, part, ticket, e, grid, st);
+  return launch_mt<4>(p, part, ticket, e, grid, st);
 }
 
 }  // namespace fdllm

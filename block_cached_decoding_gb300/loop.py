@@ -4,9 +4,12 @@ section 3.4.4), driving the three ABI calls in lock step over a batch.
 The model forward pass is out of scope, so each step's queries, fresh keys and
 values and hidden states are drawn by the device twin of the seeded generator
 (a stand-in keyed by (sequence, step, position)); caches are re-drawn for each
-refresh epoch (block index) and written with fdllm_kv_splice(REFRESH) at each
-block boundary, standing in for the fused recomputation of every position's
-K/V after a block completes.
+refresh epoch and written with fdllm_kv_splice(REFRESH) at each block
+boundary, standing in for the fused recomputation of every position's K/V
+after a block completes.  The refresh epoch is the block index; with
+`refresh_interval` r the cache is also refreshed every r steps inside a block
+(the refresh-every-r-steps variant the pages report for LLaDA-V), with epoch
+block * 1000 + (step in block) // r.
 """
 from __future__ import annotations
 
@@ -31,6 +34,7 @@ class StepResult:
     step: int
     block: int
     block_start: int
+    epoch: int                  # refresh epoch of the caches this step read
     unmasked: torch.Tensor      # uint8 [b, B]
     conf: torch.Tensor          # fp32 [b, B]
     kappa: torch.Tensor         # fp32 [b, B]
@@ -41,8 +45,10 @@ class StepResult:
 
 class BlockDecoder:
     def __init__(self, wl: Workload, *, tau: float = 0.9, strategy: int = F.SELECT_THRESHOLD,
-                 factor: float = 1.0, topk: int = 1, sigma_w: float | None = None, device: str = "cuda"):
+                 factor: float = 1.0, topk: int = 1, sigma_w: float | None = None, device: str = "cuda",
+                 refresh_interval: int | None = None):
         self.wl = wl
+        self.refresh_interval = refresh_interval
         self.tau, self.strategy, self.factor, self.topk = tau, strategy, factor, topk
         self.sigma_w = wl.sigma_w if sigma_w is None else sigma_w
         self.dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
@@ -102,7 +108,7 @@ class BlockDecoder:
         return 0, wl.seq_len
 
     def refresh(self, k: int):
-        """Block boundary: caches recomputed for refresh epoch k (drawn), written by REFRESH."""
+        """Caches recomputed for refresh epoch k (drawn), written by fdllm_kv_splice(REFRESH)."""
         wl = self.wl
         F.fdllm_synth_kv_cache(wl.seed, F.SYNTH_KCACHE, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, k, 1.0,
                                self.code, self.k_stage)
@@ -123,7 +129,12 @@ class BlockDecoder:
         F.fdllm_synth_hidden(wl.seed, b, g, s, wl.block_size, wl.hidden, wl.vocab, wl.p_plant, self.w, self.code,
                              self.hidden)
 
-    def step(self, g: int, k: int) -> StepResult:
+    def epoch(self, k: int, n: int) -> int:
+        """Refresh epoch of the caches at step n (0-based) of block k."""
+        r = self.refresh_interval
+        return k if not r else k * 1000 + n // r
+
+    def step(self, g: int, k: int, epoch: int | None = None) -> StepResult:
         """One denoising step of block k: attention over the cache, then confidence select."""
         wl = self.wl
         p0, p1 = self.query_range(k)
@@ -137,7 +148,8 @@ class BlockDecoder:
         s = wl.prompt_len + k * wl.block_size
         F.fdllm_confidence_select(self.select_desc(s), self.hidden, self.w, self.tokens, self.unmasked, self.conf,
                                   self.kappa, self.argmax, self.n_left, self.sel_ws)
-        return StepResult(g, k, s, self.unmasked, self.conf, self.kappa, self.argmax, self.n_left, out)
+        return StepResult(g, k, s, self.epoch(k, 0) if epoch is None else epoch, self.unmasked, self.conf, self.kappa,
+                          self.argmax, self.n_left, out)
 
     def run(self, hook=None, max_steps_per_block: int | None = None):
         """Decode every block left to right; returns (tokens, steps per block)."""
@@ -146,10 +158,14 @@ class BlockDecoder:
         g = 0
         cap = max_steps_per_block or wl.block_size
         for k in range(wl.gen_length // wl.block_size):
-            self.refresh(k)
             n = 0
+            ep = self.epoch(k, 0)
+            self.refresh(ep)
             while True:
-                r = self.step(g, k)
+                if n > 0 and self.epoch(k, n) != ep:
+                    ep = self.epoch(k, n)
+                    self.refresh(ep)
+                r = self.step(g, k, ep)
                 if hook is not None:
                     hook(self, r)
                 g += 1

@@ -95,8 +95,9 @@ typedef struct {
  * if the descriptor is invalid. */
 int64_t fdllm_attn_query_count(const fdllm_attn_desc *desc);
 
-/* Scratch bytes fdllm_block_attn needs for `desc` (split-KV partial results);
- * 0 on an invalid descriptor. */
+/* Scratch bytes fdllm_block_attn needs for `desc` (0 for every shape the
+ * current kernels take: split-KV partials are merged on chip); 0 on an invalid
+ * descriptor. */
 size_t fdllm_attn_workspace_size(const fdllm_attn_desc *desc);
 
 /* O_i = sum_j softmax_j(q_i . k_j * sm_scale) v_j over all N positions j.
@@ -143,8 +144,11 @@ typedef struct {
   int32_t dtype;        /* fdllm_dtype of hidden and lm_head_w */
 } fdllm_select_desc;
 
-/* Scratch bytes fdllm_confidence_select needs (per-split softmax partials for
- * up to batch * block_size rows); 0 on an invalid descriptor. */
+/* Scratch bytes fdllm_confidence_select needs (an arrival ticket plus the
+ * per-split softmax partials of up to batch * block_size rows); 0 on an invalid
+ * descriptor.  The workspace needs no initialisation and may be reused by
+ * consecutive calls, but two calls that may run at the same time (different
+ * streams) must not share one. */
 size_t fdllm_select_workspace_size(const fdllm_select_desc *desc);
 
 /* One confidence-aware unmask step.

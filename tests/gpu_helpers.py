@@ -94,7 +94,7 @@ def kappa_tol(k):
     return 1e-3 * max(1.0, abs(k)) + 1e-3
 
 
-def compare_select(ref: dict, got: dict, tau: float, strategy="threshold"):
+def compare_select(ref: dict, got: dict, tau: float, strategy="threshold", factor: float = 1.0):
     """Compare one step's GPU outputs with the oracle's `decode_step` info.
 
     Returns the number of exempted positions; raises AssertionError on a mismatch
@@ -132,6 +132,13 @@ def compare_select(ref: dict, got: dict, tau: float, strategy="threshold"):
             # near-threshold flips change whether the step falls back; accept when the only
             # disagreement is explained by positions within the tau band
             if any(abs(ref["conf"][bi, i] - tau) < TAU_EXEMPT for i in np.nonzero(masked[bi])[0]):
+                exempt += len(diff)
+                continue
+        if strategy == "factor":
+            # the rule compares (n + 1) (1 - c_(n)) with f; a value within the confidence
+            # tolerance of f may fall on either side
+            eps = np.sort(1.0 - ref["conf"][bi, np.nonzero(masked[bi])[0]])
+            if any(abs((n + 2) * e - factor) < (n + 2) * TAU_EXEMPT for n, e in enumerate(eps)):
                 exempt += len(diff)
                 continue
         raise AssertionError(f"sequence {bi}: unmask {np.nonzero(sel_g)[0]} vs oracle {np.nonzero(sel_r)[0]}")

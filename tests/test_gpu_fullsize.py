@@ -28,7 +28,7 @@ def _lib():
 
 
 def _check_attention(wl, dec, r, rng, n_seq=2, n_rows=12):
-    g, k, s = r.step, r.block, r.block_start
+    g, k, s, ep = r.step, r.block, r.block_start, r.epoch
     p0, p1 = dec.query_range(k)
     pos = list(range(p0, p1))
     out = r.attn_out.float().cpu().numpy().astype(np.float64)
@@ -36,9 +36,9 @@ def _check_attention(wl, dec, r, rng, n_seq=2, n_rows=12):
     for b in seqs:
         per = wl.seq_len * wl.n_kv_heads * wl.head_dim
         cshape = (1, wl.seq_len, wl.n_kv_heads, wl.head_dim)
-        kc = f64(synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_KCACHE, b, k), per, 1.0, wl.dtype),
+        kc = f64(synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_KCACHE, b, ep), per, 1.0, wl.dtype),
                  wl.dtype).reshape(cshape)
-        vc = f64(synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_VCACHE, b, k), per, 1.0, wl.dtype),
+        vc = f64(synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_VCACHE, b, ep), per, 1.0, wl.dtype),
                  wl.dtype).reshape(cshape)
         # this sequence's fresh K/V for every fresh position, queries for sampled positions
         kf = np.stack([synth.scaled_normals(synth.stream_key(wl.seed, synth.KIND_KFRESH, b, g, p),

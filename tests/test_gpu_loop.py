@@ -20,19 +20,20 @@ def _lib():
     ensure_built()
 
 
-def lockstep(wl, tau, strategy="threshold"):
-    dec = BlockDecoder(wl, tau=tau, strategy={"threshold": F.SELECT_THRESHOLD, "factor": F.SELECT_FACTOR}[strategy])
+def lockstep(wl, tau, strategy="threshold", refresh_interval=None):
+    dec = BlockDecoder(wl, tau=tau, strategy={"threshold": F.SELECT_THRESHOLD, "factor": F.SELECT_FACTOR}[strategy],
+                       refresh_interval=refresh_interval)
     w64 = f64(synth.lm_head_weight(wl.seed, wl.vocab, wl.hidden, wl.sigma_w, wl.dtype), wl.dtype)
     state = {"exempt": 0, "steps": 0, "unmasked": 0}
     caches = {}
 
     def hook(d, r):
-        g, k, s = r.step, r.block, r.block_start
-        if k not in caches:
+        g, k, s, ep = r.step, r.block, r.block_start, r.epoch
+        if ep not in caches:
             caches.clear()
-            caches[k] = [f64(synth.kv_cache(wl.seed, kind, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, k,
-                                             wl.dtype), wl.dtype) for kind in (synth.KIND_KCACHE, synth.KIND_VCACHE)]
-        kc, vc = caches[k]
+            caches[ep] = [f64(synth.kv_cache(wl.seed, kind, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, ep,
+                                              wl.dtype), wl.dtype) for kind in (synth.KIND_KCACHE, synth.KIND_VCACHE)]
+        kc, vc = caches[ep]
         p0, p1 = d.query_range(k)
         pos = range(p0, p1)
         b = wl.batch
@@ -89,3 +90,17 @@ def test_small_bf16_prefix_loop():
     wl = configs.LLADA_STEP.with_(prompt_len=30, gen_length=64, block_size=32, n_q_heads=4, n_kv_heads=4,
                                   head_dim=64, hidden=256, vocab=2000)
     lockstep(wl, 0.9)
+
+
+def test_refresh_every_two_steps():
+    """Cache refreshed every 2 steps inside a block (the LLaDA-V variant): each step's
+    attention must read the caches of its own refresh epoch."""
+    wl = configs.LLADA_BATCH.with_(batch=2, prompt_len=24, gen_length=32, block_size=16, n_q_heads=4,
+                                   n_kv_heads=4, head_dim=64, hidden=256, vocab=1500)
+    state, steps = lockstep(wl, 1.0, refresh_interval=2)           # tau = 1: 16 steps per block, 8 refreshes
+    assert steps == [16, 16]
+
+
+def test_factor_strategy_loop():
+    wl = configs.TINY.with_(gen_length=32)
+    lockstep(wl, 0.9, strategy="factor")
