@@ -14,8 +14,10 @@
 //              K=d) into one of two TMEM score buffers, then PV_i = P_i V_i
 //              (N=d, K=64 keys, V read MN-major) into one of two TMEM
 //              buffers; S_{i+1} is issued before PV_i; the K/V ring holds
-//              5 tiles (d = 128) so loads run ahead of the MMAs
-//   warps 4-7  one thread per query row, online softmax in base 2 with a lazy
+//              4 tiles (d = 128) so loads run ahead of the MMAs
+//   warps 4-11 two threads per query row (warps w and w + 4 share a TMEM lane
+//              quadrant and split the key and output columns; they exchange
+//              the half-row maxima through shared memory), online softmax in base 2 with a lazy
 //              reference max: P_i = 2^(S_i - m_ref) is written as bf16 (128-byte
 //              swizzle) into one of two P buffers and the tensor core
 //              accumulates O += P_i V_i in TMEM.  m_ref moves only when a row's
@@ -38,7 +40,7 @@
 namespace fdllm {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, idle; 4-11: softmax (two per TMEM lane quadrant)
 constexpr int kTile = 128;       // rows per query tile
 constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
@@ -65,12 +67,12 @@ struct Cfg {
   static constexpr int KVHALF = kKeys * 128;          // 64 rows x 64 bf16
   static constexpr int P_BYTES = kTile * kKeys * 2;   // 128 rows x 64 keys bf16 (one swizzle atom column)
   static constexpr int STAGE = 2 * KV_BYTES;          // K + V
-  static constexpr int NS = D == 128 ? 5 : 8;         // K/V ring stages
+  static constexpr int NS = D == 128 ? 4 : 8;         // K/V ring stages
   // cluster merge: weighted O rows received by an owner, C * ceil(128 / C) <= 136 rows, then (max, l) of 8 peers
   static constexpr int MERGE_ROWS = 136;
   static constexpr int MERGE_BYTES = MERGE_ROWS * D * 4 + 8 * kTile * 8;
   static constexpr int RING = NS * STAGE > MERGE_BYTES ? NS * STAGE : MERGE_BYTES;
-  static constexpr int SMEM = Q_BYTES + RING + 2 * P_BYTES + 1024 + 1024;
+  static constexpr int SMEM = Q_BYTES + RING + 2 * P_BYTES + 1024 + 4096;   // + alignment + Bars
   static constexpr uint32_t S_COL = 0;                // TMEM: S0, S1 (64 columns each), then O (D columns)
   static constexpr uint32_t O_COL = 2 * kKeys;
   static constexpr uint32_t TMEM_COLS = 256;
@@ -78,11 +80,16 @@ struct Cfg {
 
 struct Bars {
   uint64_t qfull, kvfull[8], kvempty[8], sfull[2], sempty[2], pfull[2], pvdone, drain;
-  uint32_t tmem_base;
+  uint32_t tmem_base;  // (the whole struct must fit the 4096 bytes reserved after the P buffers)
   int32_t abort;
   int32_t issued;     // K/V tiles issued by the producer
   int32_t consumed;   // K/V tiles whose arrival the MMA issuer waited for
+  float rowmax[2][2][kTile];  // [tile parity][column half][row] half-row maxima
+  float lhalf[2][kTile];      // [column half][row] partial softmax denominators
 };
+
+// The 256 softmax threads (warps 4-11) synchronise among themselves.
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 struct KeyTile {
   int range;   // 0 prefix cache, 1 fresh, 2 suffix cache
@@ -125,6 +132,8 @@ __device__ __forceinline__ bool row_target(const Plan &pl, int nq, int nh, int q
   return hs < nh && qi < nq;
 }
 
+static_assert(sizeof(Bars) <= 4096, "Bars must fit its shared-memory reservation");
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
@@ -161,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < NS; ++i) { tc::mbar_init(&br.kvfull[i], 1); tc::mbar_init(&br.kvempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&br.sfull[i], 1);
-      tc::mbar_init(&br.sempty[i], 4);
-      tc::mbar_init(&br.pfull[i], 4);
+      tc::mbar_init(&br.sempty[i], 8);
+      tc::mbar_init(&br.pfull[i], 8);
     }
     tc::mbar_init(&br.pvdone, 1);
     tc::mbar_init(&br.drain, 1);
@@ -174,8 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = br.tmem_base;
 
-  // thread of the softmax warps: its query row and running state (reference max, l)
-  const int r = (warp - 4) * 32 + lane;
+  // thread of the softmax warps: its query row, column half and running state (reference max, l)
+  const int r = (warp & 3) * 32 + lane;
+  const int half = (warp - 4) >> 2;
   float m_run = kNegInf, l_run = 0.f;
 
   if (warp == 0) {
@@ -248,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
     }
   } else if (warp >= 4) {
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
-    const uint32_t oa = tmem + lane_base + CF::O_COL;
+    constexpr int DHALF = D / 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t oa = tmem + lane_base + CF::O_COL + (uint32_t)(half * DHALF);   // this thread's O columns
     bool ok = true;
     // wait until PV_i has been accumulated into O (phases complete in order, one per tile)
     auto wait_pv = [&](int i) -> bool {
@@ -257,25 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       return true;
     };
-    // softmax of tile i: P_i = 2^((S_i - m_ref) * scale * log2 e) into shared memory, running l
+    // softmax of tile i over this thread's 32 key columns: P_i = 2^((S_i - m_ref) * scale * log2 e)
     auto softmax = [&](int i) -> bool {
       const int j = i & 1;
       if (!tc::mbar_wait(&br.sfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 218); return false; }
       tc::fence_after_sync();
-      const int nv = key_tile(pl, a.nq, a.n, k0 + i).nvalid;
-      const uint32_t sa = tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys);
+      const int nv = key_tile(pl, a.nq, a.n, k0 + i).nvalid - half * 32;   // valid columns of this half
+      uint32_t x[32];
+      tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys + half * 32), x);
+      tc::tmem_ld_wait();
       float tm = kNegInf;
-      {
-        uint32_t x[32], y[32];
-        tc::tmem_ld_32x32b_x32(sa, x);
-        tc::tmem_ld_32x32b_x32(sa + 32u, y);
-        tc::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (e < nv) tm = fmaxf(tm, __uint_as_float(x[e]));
-          if (32 + e < nv) tm = fmaxf(tm, __uint_as_float(y[e]));
-        }
-      }
+      for (int e = 0; e < 32; ++e)
+        if (e < nv) tm = fmaxf(tm, __uint_as_float(x[e]));
+      br.rowmax[j][half][r] = tm;
+      softmax_bar();
+      tm = fmaxf(br.rowmax[j][0][r], br.rowmax[j][1][r]);
       // move the reference max only when the row max outgrows it by more than 2^8
       const bool need = m_run == kNegInf || (tm - m_run) * a.scale_log2 > 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -284,13 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i > 0) {
           if (!wait_pv(i - 1)) return false;       // O holds PV_0 .. PV_{i-1}
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t x[32];
-            tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
+          for (int c0 = 0; c0 < DHALF; c0 += 32) {
+            uint32_t o[32];
+            tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, o);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(__uint_as_float(x[e]) * al);
-            tc::tmem_st_32x32b_x32(oa + (uint32_t)c0, x);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
+            tc::tmem_st_32x32b_x32(oa + (uint32_t)c0, o);
           }
           tc::tmem_st_wait();
         }
@@ -298,31 +306,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
       }
       const float ms = m_run * a.scale_log2;
-      unsigned char *pb = p_s + j * CF::P_BYTES;
+      // 32 keys = chunks 4 half .. 4 half + 3 of this row's 128 bytes in the 128-byte swizzle layout
+      unsigned char *rowp = p_s + j * CF::P_BYTES + r * 128;
       float lt = 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < kKeys; c0 += 32) {
-        uint32_t x[32];
-        tc::tmem_ld_32x32b_x32(sa + (uint32_t)c0, x);
-        tc::tmem_ld_wait();
-        // 32 keys = 4 chunks of 8 in this row's 128 bytes (64 keys, one swizzle atom column)
-        unsigned char *rowp = pb + r * 128;
+      for (int cc = 0; cc < 4; ++cc) {
+        const int ch = half * 4 + cc;
+        uint32_t pk[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const int ch = c0 / 8 + cc;
-          uint32_t pk[4];
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int e = cc * 8 + e2 * 2;
-            const float p0 = (c0 + e < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
-            const float p1 =
-                (c0 + e + 1 < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
-            lt += p0 + p1;
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            pk[e2] = *(uint32_t *)&h2;
-          }
-          *(uint4 *)(rowp + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const int e = cc * 8 + e2 * 2;
+          const float p0 = (e < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
+          const float p1 = (e + 1 < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
+          lt += p0 + p1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pk[e2] = *(uint32_t *)&h2;
         }
+        *(uint4 *)(rowp + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       l_run += lt;
       tc::fence_proxy_async_smem();
@@ -337,14 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nt && ok; ++i) ok = softmax(i);
     if (ok && nt > 0) ok = wait_pv(nt - 1);        // O is complete
     if (!ok) l_run = 0.f;
+    br.lhalf[half][r] = l_run;
+    softmax_bar();
+    l_run = ok ? br.lhalf[0][r] + br.lhalf[1][r] : 0.f;
     if (pl.nsplit == 1 && ok) {
       int hs, qi;
       const bool valid = row_target(pl, a.nq, nh, q0, r, hs, qi);
       const int h = kvh * a.group + h0 + hs;
       const float inv = 1.f / l_run;
-      const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D;
+      const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D + half * DHALF;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < DHALF; c0 += 32) {
         uint32_t x[32];
         tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
         tc::tmem_ld_wait();
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid && a.lse) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = m_run * a.scale + __logf(l_run);
+      if (valid && half == 0 && a.lse) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = m_run * a.scale + __logf(l_run);
     }
   }
 
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before_sync();
     cluster.sync();                                  // all MMAs and copies of every CTA are done
     const float2 mine = l_run > 0.f ? make_float2(m_run * a.scale_log2, l_run) : make_float2(kNegInf, 0.f);
-    if (warp >= 4)
+    if (warp >= 4 && half == 0)
       for (int c = 0; c < C; ++c) *cluster.map_shared_rank(mlrecv + crank * kTile + r, c) = mine;
     cluster.sync();                                  // (max, l) of every split has arrived everywhere
     float M = kNegInf, L = 0.f;
@@ -400,11 +403,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (v.y > 0.f) L += v.y * exp2f(v.x - M);
       }
       const float w = (mine.y > 0.f && L > 0.f) ? exp2f(mine.x - M) / L : 0.f;
+      // this thread's half row goes to the CTA that owns the row (itself: a plain store)
       const int owner = r / rpc;
-      float4 *dst = (float4 *)cluster.map_shared_rank(orecv + ((size_t)crank * rpc + (r - owner * rpc)) * D, owner);
-      const uint32_t oa = tmem + ((uint32_t)((warp - 4) * 32) << 16) + CF::O_COL;
+      float *slot = orecv + ((size_t)crank * rpc + (r - owner * rpc)) * D + half * (D / 2);
+      float4 *dst = (float4 *)(owner == crank ? slot : cluster.map_shared_rank(slot, owner));
+      const uint32_t oa = tmem + ((uint32_t)((warp & 3) * 32) << 16) + CF::O_COL + (uint32_t)(half * (D / 2));
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t x[32];
         tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
         tc::tmem_ld_wait();
@@ -433,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *(uint2 *)((__nv_bfloat16 *)a.out + off) = make_uint2(*(uint32_t *)&lo, *(uint32_t *)&hi);
       }
     }
-    if (warp >= 4 && a.lse && r >= r0 && r < r1 && L > 0.f) {
+    if (warp >= 4 && half == 0 && a.lse && r >= r0 && r < r1 && L > 0.f) {
       int hs, qi;
       if (row_target(pl, a.nq, nh, q0, r, hs, qi))
         a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = (M + log2f(L)) * 0.6931471805599453f;
