@@ -396,7 +396,7 @@ cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned l
   static std::atomic<uint32_t> epochs{(uint32_t)std::chrono::steady_clock::now().time_since_epoch().count() ^
                                       ((uint32_t)getpid() << 16)};
   uint32_t e = epochs.fetch_add(1) + 1;
-  if (e == 0) e = epochs.fetch_add(1) + 1;
+  while (e == 0 || e == 0xFFFFFFFFu) e = epochs.fetch_add(1) + 1;  // never the all-zero / all-one patterns
   const int rows = p.batch * p.B;
   if (rows <= 128) return launch_mt<1>(p, part, ticket, e, grid, st);
   if (rows <= 256) return launch_mt<2>(p, part, ticket, e, grid, st);

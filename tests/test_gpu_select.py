@@ -118,3 +118,43 @@ def test_nothing_masked_anywhere():
     info, got = one_step(batch=2, prompt_len=8, gen_length=32, block_size=32, block_idx=0, H=256, V=1000,
                          dtype="bf16", seed=7, premask=np.zeros((2, 32), bool))
     assert got["unmask"].sum() == 0 and np.all(got["n_left"] == 0)
+
+
+def _select_outputs(desc, hid, w, tokens0, ws):
+    out = SelectOutputs(desc, desc.batch, desc.block_size)
+    out.ws = ws
+    t = tokens0.clone()
+    out.run(desc, hid, w, t)
+    h = out.host()
+    h["tokens"] = t.cpu().numpy()
+    return h
+
+
+def test_workspace_needs_no_initialisation_and_can_be_shared():
+    """The workspace holds arrival tickets and merged rows; whatever it contains on
+    entry (all ones, random bytes, another shape's leftovers), the results are the
+    same as with a fresh workspace."""
+    rng = np.random.default_rng(11)
+    shapes = [(2, 32, 512, 5003), (1, 16, 256, 20000), (3, 32, 256, 4096)]
+    ws = torch.empty(max(F.fdllm_select_workspace_size(
+        F.select_desc(batch=b, seq_len=40 + B, block_start=40, block_size=B, hidden=H, vocab=V, mask_id=V))
+        for b, B, H, V in shapes), dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for b, B, H, V in shapes:
+            n = 40 + B
+            desc = F.select_desc(batch=b, seq_len=n, block_start=40, block_size=B, hidden=H, vocab=V, mask_id=V)
+            w_host = synth.lm_head_weight(12, V, H, float(np.sqrt(0.02)), "bf16")
+            hid_host, _, _ = synth.hidden_states(12, b, rep, range(40, 40 + B), H, V, float(np.sqrt(0.02)), "bf16", 0.4)
+            w, hid = dev(w_host, "bf16"), dev(hid_host, "bf16")
+            tokens0 = torch.full((b, n), V, dtype=torch.int32, device="cuda")
+            fresh = _select_outputs(desc, hid, w, tokens0, torch.zeros(F.fdllm_select_workspace_size(desc),
+                                                                      dtype=torch.uint8, device="cuda"))
+            for fill in ("ones", "random", "shared"):
+                if fill == "ones":
+                    ws.fill_(255)
+                elif fill == "random":
+                    ws.copy_(torch.from_numpy(rng.integers(0, 256, ws.numel(), dtype=np.uint8)).cuda())
+                got = _select_outputs(desc, hid, w, tokens0, ws)
+                for key in ("unmask", "token", "n_left", "tokens"):
+                    assert np.array_equal(got[key], fresh[key]), (fill, key, b, B, H, V)
+                assert np.allclose(got["conf"], fresh["conf"], equal_nan=True, rtol=0, atol=0)
