@@ -25,10 +25,11 @@
 //              rescaled in TMEM once the previous PV product has landed.
 //              Tile i+1's softmax runs while the tensor core computes PV_i.
 // Splits of one unit form a thread block cluster (<= 8) and merge through
-// distributed shared memory with stores only: every CTA writes its rows'
-// (max, l) into every peer, then its O rows weighted by l_s 2^(m_s - M) / L
-// into the peer that owns them (CTA c owns rows [c R/C, (c+1) R/C)), and each
-// owner sums its rows locally and writes them.
+// distributed shared memory with stores only, between two cluster barriers:
+// every CTA writes each of its O rows, unnormalised, with the row's (max, l)
+// into the CTA that owns the row (CTA c owns rows [c R/C, (c+1) R/C)), and each
+// owner combines the C copies of its rows with weights 2^(m_c - M) / L and
+// writes them.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -68,9 +69,12 @@ struct Cfg {
   static constexpr int P_BYTES = kTile * kKeys * 2;   // 128 rows x 64 keys bf16 (one swizzle atom column)
   static constexpr int STAGE = 2 * KV_BYTES;          // K + V
   static constexpr int NS = D == 128 ? 4 : 8;         // K/V ring stages
-  // cluster merge: weighted O rows received by an owner, C * ceil(128 / C) <= 136 rows, then (max, l) of 8 peers
+  // cluster merge: the O rows an owner receives, C * ceil(128 / C) <= 136 of them, fp32 with a row
+  // pitch of D + 4 floats (a column written by 8 consecutive rows falls in 8 different banks), then
+  // each received row's (max, l), then its combination weight
   static constexpr int MERGE_ROWS = 136;
-  static constexpr int MERGE_BYTES = MERGE_ROWS * D * 4 + 8 * kTile * 8;
+  static constexpr int DP = D + 4;
+  static constexpr int MERGE_BYTES = MERGE_ROWS * DP * 4 + MERGE_ROWS * 8 + MERGE_ROWS * 4;
   static constexpr int RING = NS * STAGE > MERGE_BYTES ? NS * STAGE : MERGE_BYTES;
   static constexpr int SMEM = Q_BYTES + RING + 2 * P_BYTES + 1024 + 4096;   // + alignment + Bars
   static constexpr uint32_t S_COL = 0;                // TMEM: S0, S1 (64 columns each), then O (D columns)
@@ -178,6 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
+  if (threadIdx.x == 0) {
+    for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc}) tc::prefetch_tensormap(m);
+  }
+  // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
+  // stream, which may produce q, the caches or the fresh K/V (or still read the output).
+  tc::pdl_wait_primary();
+  tc::pdl_launch_dependents();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -384,29 +395,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int C = pl.nsplit;
     const int crank = (int)cluster.block_rank();
     constexpr int CH = D / 4;                        // float4 chunks per row
-    (void)CH;
+    constexpr int DP = CF::DP;
     const int rpc = (kTile + C - 1) / C;             // rows owned per CTA
-    // the K/V ring is free once every CTA of the cluster has passed the first barrier
-    float *orecv = (float *)kv_s;                    // [C][rpc][D]: weighted rows received from each split
-    float2 *mlrecv = (float2 *)(kv_s + CF::MERGE_ROWS * D * 4);  // [C][128]: every split's (max, l) per row
+    // receive area in the K/V ring: [C][rpc] O rows (unnormalised), then [C][rpc] (max * log2 e, l)
+    float *orecv = (float *)kv_s;
+    float2 *mlrecv = (float2 *)(kv_s + (size_t)CF::MERGE_ROWS * DP * 4);
     tc::fence_before_sync();
-    cluster.sync();                                  // all MMAs and copies of every CTA are done
-    const float2 mine = l_run > 0.f ? make_float2(m_run * a.scale_log2, l_run) : make_float2(kNegInf, 0.f);
-    if (warp >= 4 && half == 0)
-      for (int c = 0; c < C; ++c) *cluster.map_shared_rank(mlrecv + crank * kTile + r, c) = mine;
-    cluster.sync();                                  // (max, l) of every split has arrived everywhere
-    float M = kNegInf, L = 0.f;
+    cluster.sync();                                  // every CTA's MMAs and copies are done: rings are free
     if (warp >= 4) {
-      for (int c = 0; c < C; ++c) M = fmaxf(M, mlrecv[c * kTile + r].x);
-      for (int c = 0; c < C; ++c) {
-        const float2 v = mlrecv[c * kTile + r];
-        if (v.y > 0.f) L += v.y * exp2f(v.x - M);
-      }
-      const float w = (mine.y > 0.f && L > 0.f) ? exp2f(mine.x - M) / L : 0.f;
-      // this thread's half row goes to the CTA that owns the row (itself: a plain store)
+      // this thread's half row, as accumulated, and the row's (max, l) go to the CTA that owns the row
       const int owner = r / rpc;
-      float *slot = orecv + ((size_t)crank * rpc + (r - owner * rpc)) * D + half * (D / 2);
-      float4 *dst = (float4 *)(owner == crank ? slot : cluster.map_shared_rank(slot, owner));
+      const int slot = crank * rpc + (r - owner * rpc);
+      float *orow = orecv + (size_t)slot * DP + half * (D / 2);
+      float4 *dst = (float4 *)(owner == crank ? orow : cluster.map_shared_rank(orow, owner));
+      if (half == 0) {
+        const float2 mine = l_run > 0.f ? make_float2(m_run * a.scale_log2, l_run) : make_float2(kNegInf, 0.f);
+        *(owner == crank ? mlrecv + slot : cluster.map_shared_rank(mlrecv + slot, owner)) = mine;
+      }
       const uint32_t oa = tmem + ((uint32_t)((warp & 3) * 32) << 16) + CF::O_COL + (uint32_t)(half * (D / 2));
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -415,20 +420,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_ld_wait();
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
-          dst[c0 / 4 + q4] = make_float4(__uint_as_float(x[4 * q4]) * w, __uint_as_float(x[4 * q4 + 1]) * w,
-                                         __uint_as_float(x[4 * q4 + 2]) * w, __uint_as_float(x[4 * q4 + 3]) * w);
+          dst[c0 / 4 + q4] = make_float4(__uint_as_float(x[4 * q4]), __uint_as_float(x[4 * q4 + 1]),
+                                         __uint_as_float(x[4 * q4 + 2]), __uint_as_float(x[4 * q4 + 3]));
       }
     }
-    cluster.sync();                                  // every weighted row is in its owner
+    cluster.sync();                                  // every row is in its owner
+    // owner: out = sum_c O_c w_c with w_c = 2^(m_c - M) / L, M = max_c m_c, L = sum_c l_c 2^(m_c - M)
     const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);
-    for (int u = threadIdx.x; u < (r1 - r0) * CH; u += kThreads) {
-      const int lr = u / CH, ch = u % CH, row = r0 + lr;
+    float *wrecv = (float *)(mlrecv + CF::MERGE_ROWS);   // [C][rpc] weights, 0 for an empty or aborted split
+    for (int lr = threadIdx.x; lr < r1 - r0; lr += kThreads) {
+      float M = kNegInf, L = 0.f;
+      for (int c = 0; c < C; ++c) M = fmaxf(M, mlrecv[c * rpc + lr].x);
+      for (int c = 0; c < C; ++c) {
+        const float2 ml = mlrecv[c * rpc + lr];
+        if (ml.y > 0.f) L += ml.y * exp2f(ml.x - M);
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (int c = 0; c < C; ++c) {
+        const float2 ml = mlrecv[c * rpc + lr];
+        wrecv[c * rpc + lr] = ml.y > 0.f ? exp2f(ml.x - M) * inv : 0.f;
+      }
       int hs, qi;
-      if (!row_target(pl, a.nq, nh, q0, row, hs, qi)) continue;
+      if (a.lse && L > 0.f && row_target(pl, a.nq, nh, q0, r0 + lr, hs, qi))
+        a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = (M + log2f(L)) * 0.6931471805599453f;
+    }
+    __syncthreads();
+    for (int u = threadIdx.x; u < (r1 - r0) * CH; u += kThreads) {
+      const int lr = u / CH, ch = u % CH;
+      int hs, qi;
+      if (!row_target(pl, a.nq, nh, q0, r0 + lr, hs, qi)) continue;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 0; c < C; ++c) {
-        const float4 v = *(const float4 *)(orecv + ((size_t)c * rpc + lr) * D + ch * 4);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        const float w = wrecv[c * rpc + lr];
+        if (w == 0.f) continue;                      // its rows may hold anything
+        const float4 v = *(const float4 *)(orecv + (size_t)(c * rpc + lr) * DP + ch * 4);
+        acc.x = fmaf(v.x, w, acc.x); acc.y = fmaf(v.y, w, acc.y);
+        acc.z = fmaf(v.z, w, acc.z); acc.w = fmaf(v.w, w, acc.w);
       }
       const int64_t off = (((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs) * D + ch * 4;
       if (a.out_f32) {
@@ -437,11 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
         *(uint2 *)((__nv_bfloat16 *)a.out + off) = make_uint2(*(uint32_t *)&lo, *(uint32_t *)&hi);
       }
-    }
-    if (warp >= 4 && half == 0 && a.lse && r >= r0 && r < r1 && L > 0.f) {
-      int hs, qi;
-      if (row_target(pl, a.nq, nh, q0, r, hs, qi))
-        a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = (M + log2f(L)) * 0.6931471805599453f;
     }
   }
 
@@ -526,13 +548,15 @@ cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cud
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<D>::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)pl.nsplit;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // prologue overlaps the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a);
   count_launches(1);
   return e;

@@ -31,7 +31,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // commutative up to rounding; the winner rule (larger m1, then lower id) makes
 // a1 independent of the merge order.
 // ---------------------------------------------------------------------------
-struct VocabStat {
+struct __align__(16) VocabStat {
   float m1;
   int32_t a1;
   float m2;

@@ -13,13 +13,12 @@
 //           row), folded into the row's VocabStat in increasing vocabulary order
 // At the end every masked row writes its VocabStat for this CTA's range to the
 // partials [b * B, grid].  The kernel is launched cooperatively (all CTAs are
-// resident), and its tail runs in three phases separated by grid barriers on
-// 64-bit tickets in the workspace (high half: this call's epoch, low half:
-// count; a ticket left by another call or uninitialised memory is re-armed
-// first, so the workspace needs no zeroing):
-//   1. every CTA arrives after writing its partials and waits for all;
-//   2. one warp per masked block row merges that row's partials into a RowStat;
-//   3. after the second barrier, CTA b selects sequence b (select_impl.cuh).
+// resident).  Its tail is one grid barrier on a 64-bit ticket in the workspace
+// (high half: this call's epoch, low half: count; a ticket left by another call
+// or uninitialised memory is re-armed first, so the workspace needs no
+// zeroing): every CTA arrives after writing its partials; CTAs b < batch wait
+// for all arrivals, then merge the partials of sequence b's masked rows and
+// select its unmasked positions (select_impl.cuh); the others exit.
 //
 // Template MT = 128-row tiles of block rows (1, 2 or 4): the vocabulary tile is
 // NV = 256 / MT rows so that 2 x MT x NV = 512 TMEM columns.  Rows of a tile
@@ -95,12 +94,16 @@ __device__ int arrive_ticket(unsigned long long *word, uint32_t e) {
   return 0;
 }
 
-// Wait (bounded) until all `count` CTAs of epoch `e` have arrived.
+// Wait (bounded) until all `count` CTAs of epoch `e` have arrived.  The polling
+// load has acquire semantics: the partials written before the arrivals are
+// visible to this thread, and to the rest of its CTA after a __syncthreads.
 __device__ bool wait_ticket(const unsigned long long *word, uint32_t e, int count) {
   const unsigned long long want = ((unsigned long long)e << 32) | (unsigned)count;
   const uint64_t t0 = tc::globaltimer();
   for (uint32_t i = 0;; ++i) {
-    if (*(const volatile unsigned long long *)word == want) return true;
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(word) : "memory");
+    if (v == want) return true;
     if ((i & 63u) == 0 && tc::globaltimer() - t0 > tc::kWaitLimitNs) return false;
     __nanosleep(64);
   }
@@ -133,19 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (u1 - u0 + C::UNITS - 1) / C::UNITS;
   const int kchunks = H / kKChunk;
 
-  // masked block rows (same on every CTA)
-  if (threadIdx.x == 0) { sh.abort = 0; sh.issued = 0; sh.consumed = 0; sh.active = 0; }
-  __syncthreads();
-  for (int r = threadIdx.x; r < MT * kABox; r += kThreads) {
-    bool m = false;
-    if (r < rows) {
-      const int bb = r / B, i = r - bb * B;
-      m = tokens[(int64_t)bb * seq_len + s + i] == mask_id;
-    }
-    sh.masked[r] = m;
-    if (m) atomicOr(&sh.active, 1u << (r / kABox));
-  }
-  if (warp == 0 && lane == 0) {
+  if (threadIdx.x == 0) {
+    sh.abort = 0; sh.issued = 0; sh.consumed = 0; sh.active = 0;
     for (int i = 0; i < C::STAGES; ++i) {
       tc::mbar_init(&sh.full[i], 1);
       tc::mbar_init(&sh.empty[i], 1);
@@ -160,10 +152,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tensormap(&map_w);
   }
   if (warp == 1) tc::tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+  // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
+  // stream, which may produce the tokens, hidden rows or W (or still read the workspace).
+  tc::pdl_wait_primary();
+  tc::pdl_launch_dependents();
+  __syncthreads();
+  // masked block rows (same on every CTA)
+  for (int r = threadIdx.x; r < MT * kABox; r += kThreads) {
+    bool m = false;
+    if (r < rows) {
+      const int bb = r / B, i = r - bb * B;
+      m = tokens[(int64_t)bb * seq_len + s + i] == mask_id;
+    }
+    sh.masked[r] = m;
+    if (m) atomicOr(&sh.active, 1u << (r / kABox));
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  tc::pdl_launch_dependents();
   const uint32_t active = sh.active;
   const uint32_t tmem = sh.tmem_base;
   int nact = 0;
@@ -293,35 +299,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
 
-  // ---- tail: grid barrier, row merges across the grid, grid barrier, selection ----
-  RowStat *merged = (RowStat *)(ticket + 2);
+  // ---- tail: one grid barrier, then CTA b merges and selects sequence b ----
   if (threadIdx.x == 0) {
     __threadfence();                                   // this CTA's partials before its arrival
     if (arrive_ticket(ticket, epoch) == 0) record_device_error(err, 106);
-    if (!wait_ticket(ticket, epoch, G)) record_device_error(err, 107);
-    __threadfence();
   }
-  __syncthreads();
-  for (int row = g * (kThreads / 32) + warp; row < rows; row += G * (kThreads / 32)) {
-    if (!sh.masked[row]) continue;
-    const VocabStat acc = merge_row(part + (int64_t)row * G, G);
-    if (lane == 0) {
-      RowStat rs;
-      rs.kappa = vs_kappa(acc);
-      rs.token = acc.a1;
-      merged[row] = rs;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (arrive_ticket(ticket + 1, epoch) == 0) record_device_error(err, 108);
-    if (g < batch && !wait_ticket(ticket + 1, epoch, G)) record_device_error(err, 109);
-    __threadfence();
-  }
-  __syncthreads();
+  if (g >= batch) return;                              // no sequence to select: done once arrived
   SelectScratch &sc = *(SelectScratch *)tiles;         // the tile ring is free now
-  for (int seq = g; seq < batch; seq += G) select_sequence<kThreads>(sp, part, G, seq, sc, merged);
+  select_prepare<kThreads>(sp, g, sc);                 // inputs only: overlaps the wait below
+  if (threadIdx.x == 0 && !wait_ticket(ticket, epoch, G)) record_device_error(err, 107);
+  __syncthreads();
+  select_finish<kThreads>(sp, part, G, g, sc);
+  for (int seq = g + G; seq < batch; seq += G) select_sequence<kThreads>(sp, part, G, seq, sc);
 }
 
 // ---------------------------------------------------------------------------
@@ -363,17 +352,19 @@ cudaError_t launch_mt(const SelectProblem &p, VocabStat *part, unsigned long lon
   auto k = lmhead_tc_kernel<MT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
   if (e != cudaSuccess) return e;
-  // cooperative launch: every CTA is resident, so the tail's grid barriers cannot wait on an unscheduled CTA
+  // cooperative launch: every CTA is resident, so the tail's grid barrier cannot wait on an unscheduled CTA
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg<MT>::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // prologue overlaps the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, mh, mw, p, part, ticket, epoch);
   count_launches(1);
   return e;

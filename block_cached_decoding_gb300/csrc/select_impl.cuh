@@ -1,7 +1,8 @@
 // Merge of the per-split vocabulary partials of one sequence's masked rows into
 // confidence / log-odds / argmax, then the unmask decision for its block.
 // Shared by select_kernel (one CTA per sequence) and the tail of the
-// tensor-core LM-head kernel (the last CTAs to finish take one sequence each).
+// tensor-core LM-head kernel (CTA b takes sequence b once every CTA's partials
+// are written).
 //
 // Selection ranks masked positions by kappa = log((1 - c) / c), lowest
 // position first on ties:
@@ -17,12 +18,7 @@ namespace fdllm {
 
 constexpr int kSelectMaxBlock = 256;
 constexpr int kSelectMaxSplitsPerLane = 10;  // splits <= 320 merged with independent preloads
-
-// A masked row's merged statistics (written by the LM-head tail, one warp per row).
-struct RowStat {
-  float kappa;
-  int32_t token;
-};
+constexpr int kSelectBatchedSplitsPerLane = 5;  // splits <= 160: several rows' loads in flight at once
 
 // Merge the `splits` partials of one row (called by a whole warp; lane 0 gets the result).
 __device__ __forceinline__ VocabStat merge_row(const VocabStat *__restrict__ pr, int splits) {
@@ -46,25 +42,33 @@ __device__ __forceinline__ VocabStat merge_row(const VocabStat *__restrict__ pr,
 }
 
 struct SelectScratch {
-  int mpos[kSelectMaxBlock];
+  int mpos[kSelectMaxBlock];   // masked positions in increasing order
+  float kapc[kSelectMaxBlock]; // kappa of the j-th masked position
   float kap[kSelectMaxBlock];
   float cf[kSelectMaxBlock];
   int tok[kSelectMaxBlock];
   int m, any, nbest, nsel;
 };
 
-// Called by all NT threads of the CTA (NT >= block size, a multiple of 32).
-// Either `part` holds the VocabStat partials [b * B + i][splits] and the rows are
-// merged here, or `merged` (not null) already holds each masked row's RowStat.
+// The merged statistics of the j-th masked position into the scratch (lane 0 of the merging warp).
+__device__ __forceinline__ void store_row(SelectScratch &sc, int j, const VocabStat &acc) {
+  const int i = sc.mpos[j];
+  const float k = vs_kappa(acc);
+  sc.kapc[j] = k;
+  sc.kap[i] = k;
+  sc.cf[i] = 1.f / (1.f + __expf(k));
+  sc.tok[i] = acc.a1;
+}
+
+// The two phases below are called by all NT threads of the CTA (NT >= block
+// size, a multiple of 32).  select_prepare reads only the tokens (an input):
+// this sequence's masked positions, in order, and a cleared scratch.
 template <int NT>
-__device__ __forceinline__ void select_sequence(const SelectProblem &p, const VocabStat *__restrict__ part,
-                                                int splits, int b, SelectScratch &sc,
-                                                const RowStat *__restrict__ merged = nullptr) {
+__device__ __forceinline__ void select_prepare(const SelectProblem &p, int b, SelectScratch &sc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
   const int32_t *trow = p.tokens + (int64_t)b * p.seq_len + p.s;
   if (tid == 0) { sc.any = 0; sc.nbest = 0; sc.nsel = 0; }
-  // this sequence's masked positions in order
   if (warp == 0) {
     int base = 0;
     for (int c = 0; c < B; c += 32) {
@@ -82,27 +86,111 @@ __device__ __forceinline__ void select_sequence(const SelectProblem &p, const Vo
     sc.tok[i] = -1;
   }
   __syncthreads();
+}
+
+// select_finish (after select_prepare for the same b and scratch): `part` holds
+// the VocabStat partials [b * B + i][splits]; each masked row of sequence b is
+// merged by one warp with a fixed reduction tree (lane-strided partials in
+// increasing split order, then an xor butterfly), so the result does not
+// depend on which warp or how many rows at a time; then the selection rule and
+// the outputs.
+template <int NT>
+__device__ __forceinline__ void select_finish(const SelectProblem &p, const VocabStat *__restrict__ part,
+                                              int splits, int b, SelectScratch &sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = NT / 32;
+  const int B = p.B;
   const int M = sc.m;
 
-  if (merged != nullptr) {
-    for (int j = tid; j < M; j += NT) {
-      const int i = sc.mpos[j];
-      const RowStat rs = merged[(int64_t)b * B + i];
-      sc.kap[i] = rs.kappa;
-      sc.cf[i] = 1.f / (1.f + __expf(rs.kappa));
-      sc.tok[i] = rs.token;
+  const VocabStat *__restrict__ pseq = part + (int64_t)b * B * splits;
+  if (splits <= 32 * kSelectBatchedSplitsPerLane) {
+    // R rows per warp per round; every load is issued before the first use, and each row is
+    // reduced in three flat passes (no chain of pairwise merges):
+    //   (M1, A1) = the largest m1, lowest id on ties;
+    //   M2 = the largest value other than the winner: every m2, and every other split's m1;
+    //   S = sum of s2 e^(m2 - M2) over all splits + e^(m1 - M2) over the other splits;
+    // then kappa = (M2 - M1) + log S.  Lane-strided partials in increasing split order, then
+    // an xor butterfly: the result does not depend on which warp or how many rows at a time.
+    constexpr int R = NT <= 256 ? 4 : 2;
+    constexpr int KP = kSelectBatchedSplitsPerLane;
+    for (int j0 = warp; j0 < M; j0 += NW * R) {
+      VocabStat v[R][KP];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int j = j0 + r * NW;
+        const VocabStat *pr = pseq + (int64_t)(j < M ? sc.mpos[j] : 0) * splits;
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+          const int gi = lane + 32 * k;
+          v[r][k] = (j < M && gi < splits) ? pr[gi] : vs_identity();
+        }
+      }
+      float m1[R], m2[R], sum[R];
+      int a1[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        m1[r] = kNegInf;
+        a1[r] = 0x7fffffff;
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+          const bool w = v[r][k].m1 > m1[r] || (v[r][k].m1 == m1[r] && v[r][k].a1 < a1[r]);
+          m1[r] = w ? v[r][k].m1 : m1[r];
+          a1[r] = w ? v[r][k].a1 : a1[r];
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float om = __shfl_xor_sync(0xffffffffu, m1[r], o);
+          const int oa = __shfl_xor_sync(0xffffffffu, a1[r], o);
+          const bool w = om > m1[r] || (om == m1[r] && oa < a1[r]);
+          m1[r] = w ? om : m1[r];
+          a1[r] = w ? oa : a1[r];
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        m2[r] = kNegInf;
+#pragma unroll
+        for (int k = 0; k < KP; ++k)
+          m2[r] = fmaxf(m2[r], fmaxf(v[r][k].m2, v[r][k].a1 == a1[r] ? kNegInf : v[r][k].m1));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) m2[r] = fmaxf(m2[r], __shfl_xor_sync(0xffffffffu, m2[r], o));
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        sum[r] = 0.f;
+        if (m2[r] != kNegInf) {
+#pragma unroll
+          for (int k = 0; k < KP; ++k) {
+            if (v[r][k].s2 != 0.f) sum[r] += v[r][k].s2 * __expf(v[r][k].m2 - m2[r]);
+            if (v[r][k].a1 != a1[r] && v[r][k].m1 != kNegInf) sum[r] += __expf(v[r][k].m1 - m2[r]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int j = j0 + r * NW;
+        if (lane == 0 && j < M) {
+          VocabStat acc;
+          acc.m1 = m1[r]; acc.a1 = a1[r]; acc.m2 = m2[r]; acc.s2 = sum[r];
+          store_row(sc, j, acc);
+        }
+      }
     }
   } else {
-    // merge the splits of each masked row: one warp per row, fixed reduction tree
-    for (int j = warp; j < M; j += NT / 32) {
-      const VocabStat acc = merge_row(part + ((int64_t)b * B + sc.mpos[j]) * splits, splits);
-      if (lane == 0) {
-        const int i = sc.mpos[j];
-        const float k = vs_kappa(acc);
-        sc.kap[i] = k;
-        sc.cf[i] = 1.f / (1.f + __expf(k));
-        sc.tok[i] = acc.a1;
-      }
+    for (int j = warp; j < M; j += NW) {
+      const VocabStat acc = merge_row(pseq + (int64_t)sc.mpos[j] * splits, splits);
+      if (lane == 0) store_row(sc, j, acc);
     }
   }
   __syncthreads();
@@ -115,9 +203,10 @@ __device__ __forceinline__ void select_sequence(const SelectProblem &p, const Vo
     masked = sc.tok[i] >= 0;
     if (masked) {
       const float ki = sc.kap[i];
+#pragma unroll 8
       for (int j = 0; j < M; ++j) {
+        const float kj = sc.kapc[j];
         const int pj = sc.mpos[j];
-        const float kj = sc.kap[pj];
         rank += (kj < ki) || (kj == ki && pj < i);
       }
     }
@@ -151,6 +240,14 @@ __device__ __forceinline__ void select_sequence(const SelectProblem &p, const Vo
   __syncthreads();
   if (tid == 0) p.n_left[b] = M - sc.nsel;
   __syncthreads();
+}
+
+// Both phases for sequence b.
+template <int NT>
+__device__ __forceinline__ void select_sequence(const SelectProblem &p, const VocabStat *__restrict__ part,
+                                                int splits, int b, SelectScratch &sc) {
+  select_prepare<NT>(p, b, sc);
+  select_finish<NT>(p, part, splits, b, sc);
 }
 
 }  // namespace fdllm

@@ -3,6 +3,7 @@
 // grid sized to the SM count, both tensors in one launch.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace fdllm {
 
@@ -11,6 +12,10 @@ __global__ void __launch_bounds__(256) splice_kernel(int batch, int64_t cache_ve
                                                       uint4 *__restrict__ kc, uint4 *__restrict__ vc,
                                                       const uint4 *__restrict__ ks,
                                                       const uint4 *__restrict__ vs) {
+  // launched as a programmatic dependent: the sources may come from the previous kernel in the
+  // stream, which may also still read the cache rows written here
+  tc::pdl_wait_primary();
+  tc::pdl_launch_dependents();
   const int64_t per_tensor = (int64_t)batch * len_vecs;
   const int64_t total = 2 * per_tensor;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -34,11 +39,19 @@ cudaError_t launch_splice(int batch, int64_t cache_rows, int64_t row_bytes, int6
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap;
-  splice_kernel<<<(unsigned)blocks, 256, 0, st>>>(batch, cache_rows * rv, start * rv, len * rv,
-                                                  (uint4 *)kc, (uint4 *)vc, (const uint4 *)ks,
-                                                  (const uint4 *)vs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, splice_kernel, batch, cache_rows * rv, start * rv, len * rv,
+                                           (uint4 *)kc, (uint4 *)vc, (const uint4 *)ks, (const uint4 *)vs);
   count_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace fdllm
