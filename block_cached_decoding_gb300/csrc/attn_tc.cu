@@ -17,7 +17,8 @@
 //              4 tiles (d = 128) so loads run ahead of the MMAs
 //   warps 4-11 two threads per query row (warps w and w + 4 share a TMEM lane
 //              quadrant and split the key and output columns; they exchange
-//              the half-row maxima through shared memory), online softmax in base 2 with a lazy
+//              the half-row maxima through shared memory under a barrier of
+//              the two warps only), online softmax in base 2 with a lazy
 //              reference max: P_i = 2^(S_i - m_ref) is written as bf16 (128-byte
 //              swizzle) into one of two P buffers and the tensor core
 //              accumulates O += P_i V_i in TMEM.  m_ref moves only when a row's
@@ -94,6 +95,8 @@ struct Bars {
 
 // The 256 softmax threads (warps 4-11) synchronise among themselves.
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The two softmax warps of TMEM lane quadrant q (warps 4 + q and 8 + q) synchronise as a pair.
+__device__ __forceinline__ void quadrant_bar(int q) { asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory"); }
 
 struct KeyTile {
   int range;   // 0 prefix cache, 1 fresh, 2 suffix cache
@@ -288,13 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t x[32];
       tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys + half * 32), x);
       tc::tmem_ld_wait();
-      float tm = kNegInf;
+      float mx[16];                                  // half-row max as a tree (no 32-long chain)
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        if (e < nv) tm = fmaxf(tm, __uint_as_float(x[e]));
-      br.rowmax[j][half][r] = tm;
-      softmax_bar();
-      tm = fmaxf(br.rowmax[j][0][r], br.rowmax[j][1][r]);
+      for (int e = 0; e < 16; ++e)
+        mx[e] = fmaxf(e < nv ? __uint_as_float(x[e]) : kNegInf, e + 16 < nv ? __uint_as_float(x[e + 16]) : kNegInf);
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
+      br.rowmax[j][half][r] = mx[0];
+      quadrant_bar(warp & 3);                        // the other half of these 32 rows
+      float tm = fmaxf(br.rowmax[j][0][r], br.rowmax[j][1][r]);
       // move the reference max only when the row max outgrows it by more than 2^8
       const bool need = m_run == kNegInf || (tm - m_run) * a.scale_log2 > 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ms = m_run * a.scale_log2;
       // 32 keys = chunks 4 half .. 4 half + 3 of this row's 128 bytes in the 128-byte swizzle layout
       unsigned char *rowp = p_s + j * CF::P_BYTES + r * 128;
-      float lt = 0.f;
+      float lt[4] = {0.f, 0.f, 0.f, 0.f};           // four independent partial sums
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int ch = half * 4 + cc;
@@ -329,13 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = cc * 8 + e2 * 2;
           const float p0 = (e < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
           const float p1 = (e + 1 < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
-          lt += p0 + p1;
+          lt[cc] += p0 + p1;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pk[e2] = *(uint32_t *)&h2;
         }
         *(uint4 *)(rowp + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l_run += lt;
+      l_run += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
