@@ -59,10 +59,11 @@ int lmhead_simt_splits(const SelectProblem &p);
 cudaError_t launch_lmhead_simt(const SelectProblem &p, VocabStat *part, int splits, cudaStream_t st);
 
 // lmhead_tc.cu: the tcgen05 kernel (bf16, batch * B <= 512) writes the partials
-// and runs the merge + select itself; `ticket` is 8 bytes of workspace
+// [b * B, splits] and runs the merge + select itself; `ticket` is 8 bytes of
+// workspace.  lmhead_tc_grid gives the number of vocabulary splits (clusters).
 bool lmhead_tc_supported(const SelectProblem &p);
 int lmhead_tc_grid(const SelectProblem &p);
-cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int grid,
+cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int splits,
                              cudaStream_t st);
 
 // select.cu: merge partials [b * B, splits] over splits and unmask

@@ -1,28 +1,31 @@
 // LM head + online vocabulary reduction on the 5th-generation tensor cores.
 //
-// logits = h W^T for the block rows (b * B <= 512), never stored: each CTA owns
-// a contiguous range of the vocabulary in units of 64 rows of W and streams
-// them through shared memory once.  Per CTA (one per SM, 256 threads):
-//   warp 0  TMA producer: W tiles (64-row boxes, 128-byte swizzle, L2
-//           evict-first) and the hidden-row tiles (128-row boxes) per 64-wide
-//           K chunk, into an S-stage ring guarded by full/empty mbarriers
+// logits = h W^T for the block rows (b * B <= 512), never stored.  The grid is
+// one CTA per SM, in clusters of CS = 1, 2 or 4 CTAs (CS 128-row tiles cover
+// the block rows): CTA c of a cluster owns block rows [128 c, 128 c + 128),
+// and each cluster owns a contiguous range of the vocabulary in units of 64
+// rows of W, streamed through shared memory once: every CTA of the cluster
+// loads 1/CS of each W tile and multicasts it to all of them, so W leaves HBM
+// once per cluster and each CTA reads only its own hidden rows.  Per CTA (256
+// threads):
+//   warp 0  TMA producer: its hidden-row tile (128-row box) and its share of
+//           the W tile (64-row boxes, 128-byte swizzle, L2 evict-first) per
+//           64-wide K chunk, into an S-stage ring guarded by full/empty
+//           mbarriers; a stage is refilled only when every CTA of the cluster
+//           has consumed it (the MMA commits arrive on all their empty barriers)
 //   warp 1  TMEM owner and MMA issuer: tcgen05.mma M=128 (block rows) x
 //           N=64..256 (vocabulary) x K=16, fp32 accumulator in TMEM, double
 //           buffered so the epilogue of tile t overlaps the MMAs of tile t+1
 //   warps 4-7 epilogue: tcgen05.ld of the accumulator (one thread per block
 //           row), folded into the row's VocabStat in increasing vocabulary order
-// At the end every masked row writes its VocabStat for this CTA's range to the
-// partials [b * B, grid].  The kernel is launched cooperatively (all CTAs are
+// At the end every masked row writes its VocabStat for its cluster's range to
+// the partials [b * B, clusters].  The kernel is launched cooperatively (all CTAs are
 // resident).  Its tail is one grid barrier on a 64-bit ticket in the workspace
 // (high half: this call's epoch, low half: count; a ticket left by another call
 // or uninitialised memory is re-armed first, so the workspace needs no
 // zeroing): every CTA arrives after writing its partials; CTAs b < batch wait
 // for all arrivals, then merge the partials of sequence b's masked rows and
 // select its unmasked positions (select_impl.cuh); the others exit.
-//
-// Template MT = 128-row tiles of block rows (1, 2 or 4): the vocabulary tile is
-// NV = 256 / MT rows so that 2 x MT x NV = 512 TMEM columns.  Rows of a tile
-// with no masked position are neither loaded nor multiplied.
 //
 // Every mbarrier wait is bounded; a wait that gives up records a site code in
 // the device error word, the CTA stops issuing work, waits (bounded) for the
@@ -47,15 +50,14 @@ constexpr int kUnit = 64;        // vocabulary rows per W box
 constexpr int kKChunk = 64;      // K elements per stage (one 128-byte swizzle atom)
 constexpr int kABox = 128;       // block rows per hidden-tile box
 
-template <int MT>
 struct Cfg {
-  static constexpr int NV = 256 / MT;                       // vocabulary rows per tile
+  static constexpr int NV = 256;                            // vocabulary rows per tile
   static constexpr int UNITS = NV / kUnit;                  // W boxes per tile
-  static constexpr int A_BYTES = MT * kABox * kKChunk * 2;  // hidden tiles per stage
+  static constexpr int A_BYTES = kABox * kKChunk * 2;       // this CTA's hidden tile per stage
   static constexpr int W_BYTES = NV * kKChunk * 2;          // W tile per stage
   static constexpr int STAGE = A_BYTES + W_BYTES;
-  static constexpr int STAGES = MT == 4 ? 3 : 4;
-  static constexpr int TMEM_COLS = 512;
+  static constexpr int STAGES = 4;
+  static constexpr int TMEM_COLS = 512;                     // two accumulators of 256 columns
   static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 1024 /*barriers, flags*/;
 };
 
@@ -114,7 +116,7 @@ __device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site) {
   atomicExch(&sh.abort, 1);
 }
 
-template <int MT>
+template <int CS>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                      const SelectProblem sp, VocabStat *__restrict__ part, unsigned long long *ticket,
@@ -122,17 +124,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int32_t *__restrict__ tokens = sp.tokens;
   const int batch = sp.batch, seq_len = sp.seq_len, s = sp.s, B = sp.B, mask_id = sp.mask_id, H = sp.H, V = sp.V;
   int32_t *err = sp.err;
-  using C = Cfg<MT>;
+  using C = Cfg;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *tiles = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Shared &sh = *(Shared *)(tiles + C::STAGES * C::STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = batch * B;
   const int G = gridDim.x, g = blockIdx.x;
+  const int c = CS > 1 ? (int)tc::cluster_ctarank() : 0;   // this CTA's row tile
+  const int ncl = G / CS, k = g / CS;                      // vocabulary splits = clusters; this cluster
+  constexpr uint16_t kAll = (uint16_t)((1u << CS) - 1u);   // every CTA of the cluster
 
-  // vocabulary units [u0, u1) of this CTA
+  // vocabulary units [u0, u1) of this cluster
   const int units = (V + kUnit - 1) / kUnit;
-  const int u0 = (int)((int64_t)units * g / G), u1 = (int)((int64_t)units * (g + 1) / G);
+  const int u0 = (int)((int64_t)units * k / ncl), u1 = (int)((int64_t)units * (k + 1) / ncl);
   const int ntiles = (u1 - u0 + C::UNITS - 1) / C::UNITS;
   const int kchunks = H / kKChunk;
 
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.abort = 0; sh.issued = 0; sh.consumed = 0; sh.active = 0;
     for (int i = 0; i < C::STAGES; ++i) {
       tc::mbar_init(&sh.full[i], 1);
-      tc::mbar_init(&sh.empty[i], 1);
+      tc::mbar_init(&sh.empty[i], CS);               // one MMA commit from each CTA of the cluster
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sh.accf[i], 1);
@@ -158,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::pdl_launch_dependents();
   __syncthreads();
   // masked block rows (same on every CTA)
-  for (int r = threadIdx.x; r < MT * kABox; r += kThreads) {
+  for (int r = threadIdx.x; r < CS * kABox; r += kThreads) {
     bool m = false;
     if (r < rows) {
       const int bb = r / B, i = r - bb * B;
@@ -168,15 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (m) atomicOr(&sh.active, 1u << (r / kABox));
   }
   tc::fence_before_sync();
-  __syncthreads();
+  if (CS > 1) tc::cluster_sync();                      // every CTA's barriers exist before any multicast
+  else __syncthreads();
   tc::fence_after_sync();
   const uint32_t active = sh.active;
   const uint32_t tmem = sh.tmem_base;
-  int nact = 0;
-#pragma unroll
-  for (int m = 0; m < MT; ++m) nact += (active >> m) & 1;
+  // The whole cluster runs the pipeline when any of its row tiles has a masked row (a CTA whose own
+  // tile has none still loads its share of W and releases the stages); only masked rows are kept.
+  const bool run = active != 0 && ntiles > 0;
 
-  if (active != 0 && ntiles > 0) {
+  if (run) {
     if (warp == 0) {
       // ---------------- TMA producer ----------------
       if (lane == 0) {
@@ -186,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < ntiles && !sh.abort; ++t) {
           const int tu0 = u0 + t * C::UNITS;
           const int nu = min(C::UNITS, u1 - tu0);
-          const uint32_t bytes = (uint32_t)(nact * kABox * kKChunk * 2 + nu * kUnit * kKChunk * 2);
+          const uint32_t bytes = (uint32_t)(kABox * kKChunk * 2 + nu * kUnit * kKChunk * 2);
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int st = it % C::STAGES;
             const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
@@ -194,15 +200,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char *a = tiles + st * C::STAGE;
             unsigned char *w = a + C::A_BYTES;
             tc::mbar_arrive_expect_tx(&sh.full[st], bytes);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-              if ((active >> m) & 1)
-                tc::tma_load_2d(a + m * kABox * kKChunk * 2, &map_h, &sh.full[st], kc * kKChunk, m * kABox, pol_h);
-            for (int u = 0; u < nu; ++u)
-              tc::tma_load_2d(w + u * kUnit * kKChunk * 2, &map_w, &sh.full[st], kc * kKChunk, (tu0 + u) * kUnit,
-                              pol_w);
+            tc::tma_load_2d(a, &map_h, &sh.full[st], kc * kKChunk, c * kABox, pol_h);
+            for (int u = c; u < nu; u += CS) {
+              if (CS == 1)
+                tc::tma_load_2d(w + u * kUnit * kKChunk * 2, &map_w, &sh.full[st], kc * kKChunk, (tu0 + u) * kUnit,
+                                pol_w);
+              else
+                tc::tma_load_2d_multicast(w + u * kUnit * kKChunk * 2, &map_w, &sh.full[st], kc * kKChunk,
+                                          (tu0 + u) * kUnit, kAll, pol_w);
+            }
             atomicExch(&sh.issued, it + 1);
           }
+        }
+        if (CS > 1 && !sh.abort) {
+          // every CTA of the cluster has released every stage: no commit of theirs is still on its
+          // way to this CTA's barriers when it leaves
+          for (int i = 0; i < C::STAGES; ++i, ++it)
+            if (!tc::mbar_wait(&sh.empty[it % C::STAGES], ((uint32_t)(it / C::STAGES) & 1u) ^ 1u)) {
+              set_abort(sh, err, 110);
+              break;
+            }
         }
       }
     } else if (warp == 1) {
@@ -224,16 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             const uint32_t a = tc::smem_u32(tiles + st * C::STAGE);
             const uint32_t w = a + C::A_BYTES;
+            const uint32_t d = tmem + (uint32_t)(j * C::NV);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              if (!((active >> m) & 1)) continue;
-              const uint32_t d = tmem + (uint32_t)(j * MT * C::NV + m * C::NV);
-#pragma unroll
-              for (int kk = 0; kk < kKChunk / 16; ++kk)
-                tc::mma_bf16(d, tc::sw128_desc(a + m * kABox * kKChunk * 2 + kk * 32), tc::sw128_desc(w + kk * 32),
-                             idesc, (kc | kk) != 0);
-            }
-            tc::mma_commit(&sh.empty[st]);
+            for (int kk = 0; kk < kKChunk / 16; ++kk)
+              tc::mma_bf16(d, tc::sw128_desc(a + kk * 32), tc::sw128_desc(w + kk * 32), idesc, (kc | kk) != 0);
+            if (CS == 1) tc::mma_commit(&sh.empty[st]);
+            else tc::mma_commit_multicast(&sh.empty[st], kAll);
             atomicExch(&sh.consumed, it + 1);
           }
           if (!ok) break;
@@ -246,9 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
       // ---------------- epilogue ----------------
       const int q = warp - 4;  // TMEM lane quadrant of this warp
-      VocabStat st[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) st[m] = vs_identity();
+      const int row = c * kABox + q * 32 + lane;
+      const bool valid = ((active >> c) & 1) && sh.masked[row] != 0;
+      const bool any = __ballot_sync(0xffffffffu, valid) != 0u;
+      VocabStat st = vs_identity();
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
         const int tu0 = u0 + t * C::UNITS;
@@ -257,13 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = t & 1;
         if (!tc::mbar_wait(&sh.accf[j], (uint32_t)(t >> 1) & 1u)) { set_abort(sh, err, 105); ok = false; break; }
         tc::fence_after_sync();
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (!((active >> m) & 1)) continue;
-          const int row = m * kABox + q * 32 + lane;
-          const bool valid = sh.masked[row] != 0;
-          if (__ballot_sync(0xffffffffu, valid) == 0u) continue;
-          const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * MT * C::NV + m * C::NV);
+        if (any) {
+          const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * C::NV);
           for (int c0 = 0; c0 < ncol; c0 += 32) {
             uint32_t r[32];
             tc::tmem_ld_32x32b_x32(base + (uint32_t)c0, r);
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
                 const int v = v0 + c0 + e;
-                if (v < V) vs_push(st[m], __uint_as_float(r[e]), v);
+                if (v < V) vs_push(st, __uint_as_float(r[e]), v);
               }
             }
           }
@@ -281,11 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sh.acce[j]);
       }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const int row = m * kABox + q * 32 + lane;
-        if (((active >> m) & 1) && row < rows && sh.masked[row]) part[(int64_t)row * G + g] = st[m];
-      }
+      if (valid && row < rows) part[(int64_t)row * ncl + k] = st;
     }
   }
   tc::fence_before_sync();
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  if (CS > 1) tc::cluster_sync();                      // no CTA leaves while a peer may still address it
 
   // ---- tail: one grid barrier, then CTA b merges and selects sequence b ----
   if (threadIdx.x == 0) {
@@ -309,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   select_prepare<kThreads>(sp, g, sc);                 // inputs only: overlaps the wait below
   if (threadIdx.x == 0 && !wait_ticket(ticket, epoch, G)) record_device_error(err, 107);
   __syncthreads();
-  select_finish<kThreads>(sp, part, G, g, sc);
-  for (int seq = g + G; seq < batch; seq += G) select_sequence<kThreads>(sp, part, G, seq, sc);
+  select_finish<kThreads>(sp, part, ncl, g, sc);
+  for (int seq = g + G; seq < batch; seq += G) select_sequence<kThreads>(sp, part, ncl, seq, sc);
 }
 
 // ---------------------------------------------------------------------------
@@ -342,32 +348,72 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MT>
-cudaError_t launch_mt(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, uint32_t epoch, int grid,
-                      cudaStream_t st) {
+template <int CS>
+cudaError_t launch_cs(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, uint32_t epoch,
+                      int splits, cudaStream_t st) {
   CUtensorMap mh, mw;
   if (!make_map(&mh, p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H, kABox) ||
       !make_map(&mw, p.w, (uint64_t)p.V, (uint64_t)p.H, kUnit))
     return cudaErrorInvalidValue;
-  auto k = lmhead_tc_kernel<MT>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MT>::SMEM);
+  auto kfn = lmhead_tc_kernel<CS>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   // cooperative launch: every CTA is resident, so the tail's grid barrier cannot wait on an unscheduled CTA
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)(splits * CS));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<MT>::SMEM;
+  cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // prologue overlaps the previous kernel
   attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[2].id = cudaLaunchAttributeClusterDimension;
+  attr[2].val.clusterDim.x = CS;
+  attr[2].val.clusterDim.y = 1;
+  attr[2].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, k, mh, mw, p, part, ticket, epoch);
+  cfg.numAttrs = CS > 1 ? 3 : 2;
+  e = cudaLaunchKernelEx(&cfg, kfn, mh, mw, p, part, ticket, epoch);
   count_launches(1);
   return e;
+}
+
+// CTAs per cluster: one per 128-row tile of block rows
+int cluster_size(const SelectProblem &p) {
+  const int rows = p.batch * p.B;
+  return rows <= 128 ? 1 : (rows <= 256 ? 2 : 4);
+}
+
+// Clusters of CS CTAs that can be resident at once on the current device (a cluster must fit in one
+// GPC, so this can be below SMs / CS); 0 if the query fails.  Cached per device.
+template <int CS>
+int max_active_clusters() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev] > 0) return cache[dev];
+  auto kfn = lmhead_tc_kernel<CS>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sm_count() / CS * CS));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kfn, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cache[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -377,21 +423,30 @@ bool lmhead_tc_supported(const SelectProblem &p) {
 }
 
 int lmhead_tc_grid(const SelectProblem &p) {
+  // vocabulary splits = clusters: as many as can be resident at once (one CTA per SM), at least one
+  // 64-row unit each
   const int units = (p.V + kUnit - 1) / kUnit;
-  const int sms = sm_count();
-  return units < sms ? units : sms;
+  const int cs = cluster_size(p);
+  int ncl = sm_count() / cs;
+  if (cs > 1) {
+    const int m = cs == 2 ? max_active_clusters<2>() : max_active_clusters<4>();
+    if (m > 0 && m < ncl) ncl = m;
+  }
+  if (ncl < 1) ncl = 1;
+  return units < ncl ? units : ncl;
 }
 
-cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int grid,
+cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int splits,
                              cudaStream_t st) {
   static std::atomic<uint32_t> epochs{(uint32_t)std::chrono::steady_clock::now().time_since_epoch().count() ^
                                       ((uint32_t)getpid() << 16)};
   uint32_t e = epochs.fetch_add(1) + 1;
   while (e == 0 || e == 0xFFFFFFFFu) e = epochs.fetch_add(1) + 1;  // never the all-zero / all-one patterns
-  const int rows = p.batch * p.B;
-  if (rows <= 128) return launch_mt<1>(p, part, ticket, e, grid, st);
-  if (rows <= 256) return launch_mt<2>(p, part, ticket, e, grid, st);
-  return launch_mt<4>(p, part, ticket, e, grid, st);
+  switch (cluster_size(p)) {
+    case 1: return launch_cs<1>(p, part, ticket, e, splits, st);
+    case 2: return launch_cs<2>(p, part, ticket, e, splits, st);
+    default: return launch_cs<4>(p, part, ticket, e, splits, st);
+  }
 }
 
 }  // namespace fdllm
