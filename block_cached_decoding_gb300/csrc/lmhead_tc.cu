@@ -173,14 +173,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (m) atomicOr(&sh.active, 1u << (r / kABox));
   }
   tc::fence_before_sync();
-  if (CS > 1) tc::cluster_sync();                      // every CTA's barriers exist before any multicast
+  if (CS > 1 && tc::cluster_nctarank() == (uint32_t)CS) tc::cluster_sync();   // barriers exist before any multicast
   else __syncthreads();
   tc::fence_after_sync();
   const uint32_t active = sh.active;
   const uint32_t tmem = sh.tmem_base;
   // The whole cluster runs the pipeline when any of its row tiles has a masked row (a CTA whose own
   // tile has none still loads its share of W and releases the stages); only masked rows are kept.
-  const bool run = active != 0 && ntiles > 0;
+  // A launch whose clusters are not CS CTAs (never from this file's launcher) multicasts nothing:
+  // it records an error and produces no partials.
+  const bool shape_ok = CS == 1 || tc::cluster_nctarank() == (uint32_t)CS;
+  if (!shape_ok && threadIdx.x == 0) record_device_error(err, 111);
+  const bool run = shape_ok && active != 0 && ntiles > 0;
 
   if (run) {
     if (warp == 0) {
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
-  if (CS > 1) tc::cluster_sync();                      // no CTA leaves while a peer may still address it
+  if (CS > 1 && shape_ok) tc::cluster_sync();          // no CTA leaves while a peer may still address it
 
   // ---- tail: one grid barrier, then CTA b merges and selects sequence b ----
   if (threadIdx.x == 0) {
