@@ -19,13 +19,13 @@
 //   warps 4-7 epilogue: tcgen05.ld of the accumulator (one thread per block
 //           row), folded into the row's VocabStat in increasing vocabulary order
 // At the end every masked row writes its VocabStat for its cluster's range to
-// the partials [b * B, clusters].  The kernel is launched cooperatively (all CTAs are
-// resident).  Its tail is one grid barrier on a 64-bit ticket in the workspace
+// the partials [b * B, clusters] and arrives on a 64-bit ticket in the workspace
 // (high half: this call's epoch, low half: count; a ticket left by another call
 // or uninitialised memory is re-armed first, so the workspace needs no
-// zeroing): every CTA arrives after writing its partials; CTAs b < batch wait
-// for all arrivals, then merge the partials of sequence b's masked rows and
-// select its unmasked positions (select_impl.cuh); the others exit.
+// zeroing).  The last min(batch, 8) CTAs to arrive wait for the rest, then merge
+// the partials of their sequences' masked rows and select the unmasked
+// positions (select_impl.cuh); the others exit.  No CTA ever waits for one that
+// cannot be scheduled, so the launch is an ordinary (programmatic dependent) one.
 //
 // Every mbarrier wait is bounded; a wait that gives up records a site code in
 // the device error word, the CTA stops issuing work, waits (bounded) for the
@@ -49,6 +49,7 @@ constexpr int kThreads = 256;
 constexpr int kUnit = 64;        // vocabulary rows per W box
 constexpr int kKChunk = 64;      // K elements per stage (one 128-byte swizzle atom)
 constexpr int kABox = 128;       // block rows per hidden-tile box
+constexpr int kMaxSelectors = 8; // CTAs that run the merge + select at the end
 
 struct Cfg {
   static constexpr int NV = 256;                            // vocabulary rows per tile
@@ -309,18 +310,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
   if (CS > 1 && shape_ok) tc::cluster_sync();          // no CTA leaves while a peer may still address it
 
-  // ---- tail: one grid barrier, then CTA b merges and selects sequence b ----
+  // ---- tail: the last W CTAs to arrive select (W = min(batch, 8, grid)) ----
+  // Selector w (arrival G - W + 1 + w) takes sequences w, w + W, ...  When it arrives, at most W - 1
+  // CTAs have not, and the G - W CTAs that arrived before it have left their SMs, so whatever has
+  // not arrived can always be scheduled: the kernel needs no co-residency guarantee.  With one
+  // sequence the selector is the last CTA and never waits.
   if (threadIdx.x == 0) {
     __threadfence();                                   // this CTA's partials before its arrival
-    if (arrive_ticket(ticket, epoch) == 0) record_device_error(err, 106);
+    const int a = arrive_ticket(ticket, epoch);
+    if (a == 0) record_device_error(err, 106);
+    sh.arrival = a;
   }
-  if (g >= batch) return;                              // no sequence to select: done once arrived
+  __syncthreads();
+  const int W = min(min(batch, kMaxSelectors), G);
+  const int sel = sh.arrival - (G - W) - 1;            // selector index, < 0 for the first G - W arrivals
+  if (sh.arrival == 0 || sel < 0) return;
   SelectScratch &sc = *(SelectScratch *)tiles;         // the tile ring is free now
-  select_prepare<kThreads>(sp, g, sc);                 // inputs only: overlaps the wait below
+  select_prepare<kThreads>(sp, sel, sc);               // inputs only: overlaps the wait below
   if (threadIdx.x == 0 && !wait_ticket(ticket, epoch, G)) record_device_error(err, 107);
   __syncthreads();
-  select_finish<kThreads>(sp, part, ncl, g, sc);
-  for (int seq = g + G; seq < batch; seq += G) select_sequence<kThreads>(sp, part, ncl, seq, sc);
+  select_finish<kThreads>(sp, part, ncl, sel, sc);
+  for (int seq = sel + W; seq < batch; seq += W) select_sequence<kThreads>(sp, part, ncl, seq, sc);
 }
 
 // ---------------------------------------------------------------------------
@@ -362,23 +372,21 @@ cudaError_t launch_cs(const SelectProblem &p, VocabStat *part, unsigned long lon
   auto kfn = lmhead_tc_kernel<CS>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
-  // cooperative launch: every CTA is resident, so the tail's grid barrier cannot wait on an unscheduled CTA
+  // an ordinary launch: the tail's waiting CTAs never hold an SM that an unscheduled CTA needs
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(splits * CS));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[3];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // prologue overlaps the previous kernel
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  attr[2].id = cudaLaunchAttributeClusterDimension;
-  attr[2].val.clusterDim.x = CS;
-  attr[2].val.clusterDim.y = 1;
-  attr[2].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // prologue overlaps the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CS;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CS > 1 ? 3 : 2;
+  cfg.numAttrs = CS > 1 ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kfn, mh, mw, p, part, ticket, epoch);
   count_launches(1);
   return e;

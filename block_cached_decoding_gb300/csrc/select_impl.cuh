@@ -1,8 +1,8 @@
 // Merge of the per-split vocabulary partials of one sequence's masked rows into
 // confidence / log-odds / argmax, then the unmask decision for its block.
 // Shared by select_kernel (one CTA per sequence) and the tail of the
-// tensor-core LM-head kernel (CTA b takes sequence b once every CTA's partials
-// are written).
+// tensor-core LM-head kernel (its last CTAs to arrive take the sequences once
+// every CTA's partials are written).
 //
 // Selection ranks masked positions by kappa = log((1 - c) / c), lowest
 // position first on ties:
