@@ -181,8 +181,8 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   return FDLLM_OK;
 }
 
-// workspace: [8-byte arrival ticket] [partials VocabStat [b * B, splits], 16 bytes
-// each, from byte 256]; the tensor-core kernel serves bf16
+// workspace: [8-byte arrival ticket, 8-byte start ticket] [partials VocabStat
+// [b * B, splits], 16 bytes each, from byte 256]; the tensor-core kernel serves bf16
 // blocks of up to 512 rows (and runs the select itself), the CUDA-core kernel the
 // rest (followed by select_kernel)
 struct SelectLayout {
@@ -195,7 +195,7 @@ SelectLayout select_layout(const SelectProblem &p) {
   SelectLayout L;
   L.tc = lmhead_tc_supported(p);
   L.splits = L.tc ? lmhead_tc_grid(p) : lmhead_simt_splits(p);
-  // the ticket, then the partials
+  // the tickets, then the partials
   L.part_off = 256;
   L.total = L.part_off + align_up((size_t)p.batch * p.B * L.splits * sizeof(VocabStat), 256);
   return L;

@@ -50,6 +50,8 @@ constexpr int kUnit = 64;        // vocabulary rows per W box
 constexpr int kKChunk = 64;      // K elements per stage (one 128-byte swizzle atom)
 constexpr int kABox = 128;       // block rows per hidden-tile box
 constexpr int kMaxSelectors = 8; // CTAs that run the merge + select at the end
+constexpr int kPrefetchers = 24; // first CTAs to start that warm L2 with the head of every CTA's W range
+constexpr int kPrefetchChunks = 12;   // K chunks (128 bytes of a W row each) warmed per row of a first tile
 
 struct Cfg {
   static constexpr int NV = 256;                            // vocabulary rows per tile
@@ -158,6 +160,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tensormap(&map_w);
   }
   if (warp == 1) tc::tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+  if (CS == 1 && warp == 3) {
+    // The first CTAs to start usually run beside the previous kernel (programmatic dependent
+    // launch, on SMs it leaves idle): they ask L2 for the first K chunks of the first W tile of
+    // every CTA's range, so the main loops begin on L2 hits while HBM is otherwise little used.
+    // A prefetch returns no data, so it is safe even before the previous kernel has finished.
+    int e = 0;
+    if (lane == 0) e = arrive_ticket(ticket + 1, epoch);
+    e = __shfl_sync(0xffffffffu, e, 0);
+    if (e >= 1 && e <= kPrefetchers) {
+      // one W box (64 rows x 64 K) per prefetch: the boxes of the first kPrefetchChunks K chunks of
+      // the first tile of CTA ranges e - 1, e - 1 + kPrefetchers, ...
+      const int nchunk = min(kPrefetchChunks, kchunks);
+      for (int j = e - 1; j < G; j += kPrefetchers) {
+        const int ju0 = (int)((int64_t)units * j / ncl), ju1 = (int)((int64_t)units * (j + 1) / ncl);
+        const int nu = min(C::UNITS, ju1 - ju0);
+        for (int q = lane; q < nu * nchunk; q += 32)
+          tc::prefetch_l2_tile_2d(&map_w, (q / nu) * kKChunk, (ju0 + q % nu) * kUnit);
+      }
+    }
+  }
   // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
   // stream, which may produce the tokens, hidden rows or W (or still read the workspace).
   tc::pdl_wait_primary();

@@ -144,7 +144,7 @@ typedef struct {
   int32_t dtype;        /* fdllm_dtype of hidden and lm_head_w */
 } fdllm_select_desc;
 
-/* Scratch bytes fdllm_confidence_select needs (an arrival ticket plus the
+/* Scratch bytes fdllm_confidence_select needs (two 8-byte tickets plus the
  * per-split softmax partials of up to batch * block_size rows); 0 on an invalid
  * descriptor.  The workspace needs no initialisation and may be reused by
  * consecutive calls, but two calls that may run at the same time (different
