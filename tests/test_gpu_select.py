@@ -114,6 +114,18 @@ def test_batched_row_tiles(batch, B, H, V):
              seed=6, premask=pm)
 
 
+@pytest.mark.parametrize("batch,B,H,V", [(32, 4, 128, 200),     # 4 vocabulary splits: 4 selectors, 8 sequences each
+                                         (100, 1, 192, 5000),    # 8 selectors, 12-13 sequences each
+                                         (160, 2, 128, 3000)])   # 320 rows (clusters of 4), 20 sequences each
+def test_many_sequences_per_selector(batch, B, H, V):
+    """The last CTAs to finish select: at most 8 of them, and never more than there are CTAs, so
+    each may take many sequences."""
+    rng = np.random.default_rng(batch + B)
+    pm = rng.random((batch, B)) < 0.7
+    one_step(batch=batch, prompt_len=5, gen_length=B, block_size=B, block_idx=0, H=H, V=V, dtype="bf16",
+             seed=8, premask=pm)
+
+
 def test_nothing_masked_anywhere():
     info, got = one_step(batch=2, prompt_len=8, gen_length=32, block_size=32, block_idx=0, H=256, V=1000,
                          dtype="bf16", seed=7, premask=np.zeros((2, 32), bool))
