@@ -56,8 +56,10 @@ struct Plan {
   int qr;               // query rows per head slot in a tile (multiple of 8)
   int ht;               // head slots per tile
   int qtiles_per_head;  // tiles per head when nq > 128 (0 when heads are packed)
-  int nqt;              // query tiles per KV head
-  int units;            // batch * Hkv * nqt
+  int nqt;              // query tiles per KV head group
+  int kvp;              // KV heads per tile (1, or 2 / 4 for MHA with few queries)
+  int tk;               // keys per KV head per key tile (64 / kvp)
+  int units;            // batch * (Hkv / kvp) * nqt
 };
 
 template <int D>
@@ -101,17 +103,17 @@ __device__ __forceinline__ void quadrant_bar(int q) { asm volatile("bar.sync %0,
 struct KeyTile {
   int range;   // 0 prefix cache, 1 fresh, 2 suffix cache
   int row0;    // first row within the range's map
-  int nvalid;  // valid keys in the tile
+  int nvalid;  // valid keys in the tile (per KV head)
 };
 
 __device__ __forceinline__ KeyTile key_tile(const Plan &pl, int nq, int n, int k) {
   KeyTile t;
   if (k < pl.ka) {
-    t.range = 0; t.row0 = k * kKeys; t.nvalid = min(kKeys, pl.f0 - t.row0);
+    t.range = 0; t.row0 = k * pl.tk; t.nvalid = min(pl.tk, pl.f0 - t.row0);
   } else if (k < pl.ka + pl.kf) {
-    t.range = 1; t.row0 = (k - pl.ka) * kKeys; t.nvalid = min(kKeys, nq - t.row0);
+    t.range = 1; t.row0 = (k - pl.ka) * pl.tk; t.nvalid = min(pl.tk, nq - t.row0);
   } else {
-    t.range = 2; t.row0 = (k - pl.ka - pl.kf) * kKeys; t.nvalid = min(kKeys, n - pl.f1 - t.row0);
+    t.range = 2; t.row0 = (k - pl.ka - pl.kf) * pl.tk; t.nvalid = min(pl.tk, n - pl.f1 - t.row0);
   }
   return t;
 }
@@ -141,7 +143,7 @@ __device__ __forceinline__ bool row_target(const Plan &pl, int nq, int nh, int q
 
 static_assert(sizeof(Bars) <= 4096, "Bars must fit its shared-memory reservation");
 
-template <int D>
+template <int D, int KVP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
@@ -159,13 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int split = blockIdx.x % pl.nsplit;
   const int unit = blockIdx.x / pl.nsplit;
+  const int nkvg = a.hkv / KVP;                        // KV head groups
   const int qt = unit % pl.nqt;
-  const int kvh = (unit / pl.nqt) % a.hkv;
-  const int b = unit / (pl.nqt * a.hkv);
+  const int kvh = ((unit / pl.nqt) % nkvg) * KVP;        // first KV head of this tile
+  const int b = unit / (pl.nqt * nkvg);
   const int k0 = (int)((int64_t)pl.kt * split / pl.nsplit);
   const int nt = (int)((int64_t)pl.kt * (split + 1) / pl.nsplit) - k0;
   int h0, nh, q0;
-  if (pl.qtiles_per_head == 0) {
+  if (KVP > 1) {
+    h0 = 0; nh = KVP; q0 = 0;                          // head slot s = KV head kvh + s (MHA)
+  } else if (pl.qtiles_per_head == 0) {
     h0 = qt * pl.ht; nh = min(pl.ht, a.group - h0); q0 = 0;
   } else {
     h0 = qt / pl.qtiles_per_head; nh = 1; q0 = (qt % pl.qtiles_per_head) * kTile;
@@ -187,6 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
   if (threadIdx.x == 0) {
     for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc}) tc::prefetch_tensormap(m);
+  }
+  if (KVP > 1) {
+    // each row writes only its own head's block of a P tile: the rest stays zero
+    for (int i = threadIdx.x; i < 2 * CF::P_BYTES / 16; i += kThreads) ((uint4 *)p_s)[i] = make_uint4(0u, 0u, 0u, 0u);
+    tc::fence_proxy_async_smem();
   }
   // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
   // stream, which may produce q, the caches or the fresh K/V (or still read the output).
@@ -219,10 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap *mv = kt.range == 0 ? &mva : (kt.range == 1 ? &mvf : &mvc);
         unsigned char *ks = kv_s + st * CF::STAGE;
         tc::mbar_arrive_expect_tx(&br.kvfull[st], (uint32_t)CF::STAGE);
-        for (int dh = 0; dh < CF::DH; ++dh) {
-          tc::tma_load_4d(ks + dh * CF::KVHALF, mk, &br.kvfull[st], dh * 64, kvh, kt.row0, b, pol_kv);
-          tc::tma_load_4d(ks + CF::KV_BYTES + dh * CF::KVHALF, mv, &br.kvfull[st], dh * 64, kvh, kt.row0, b, pol_kv);
-        }
+        for (int dh = 0; dh < CF::DH; ++dh)
+#pragma unroll
+          for (int p = 0; p < KVP; ++p) {   // the tile's 64 key rows: KVP heads x (64 / KVP) keys
+            const int off = dh * CF::KVHALF + p * (kKeys / KVP) * 128;
+            tc::tma_load_4d(ks + off, mk, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
+            tc::tma_load_4d(ks + CF::KV_BYTES + off, mv, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
+          }
         atomicExch(&br.issued, i + 1);
       }
     }
@@ -287,16 +300,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = i & 1;
       if (!tc::mbar_wait(&br.sfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 218); return false; }
       tc::fence_after_sync();
-      const int nv = key_tile(pl, a.nq, a.n, k0 + i).nvalid - half * 32;   // valid columns of this half
-      uint32_t x[32];
-      tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys + half * 32), x);
+      // this thread's CW score columns: half `half` of its row's head block (the whole tile when
+      // KVP == 1; with KVP heads packed, row r's head owns columns [s TK, s TK + TK), s = r / qr)
+      constexpr int TK = kKeys / KVP, CW = TK / 2;
+      const int c0 = (KVP > 1 ? r / pl.qr : 0) * TK + half * CW;
+      const int nv = key_tile(pl, a.nq, a.n, k0 + i).nvalid - half * CW;   // valid columns of this thread
+      uint32_t x[CW];
+      const uint32_t sa = tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys + c0);
+      if constexpr (CW == 32) tc::tmem_ld_32x32b_x32(sa, x);
+      else if constexpr (CW == 16) tc::tmem_ld_32x32b_x16(sa, x);
+      else tc::tmem_ld_32x32b_x8(sa, x);
       tc::tmem_ld_wait();
-      float mx[16];                                  // half-row max as a tree (no 32-long chain)
+      float mx[CW / 2];                              // half-row max as a tree
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        mx[e] = fmaxf(e < nv ? __uint_as_float(x[e]) : kNegInf, e + 16 < nv ? __uint_as_float(x[e + 16]) : kNegInf);
+      for (int e = 0; e < CW / 2; ++e)
+        mx[e] = fmaxf(e < nv ? __uint_as_float(x[e]) : kNegInf,
+                      e + CW / 2 < nv ? __uint_as_float(x[e + CW / 2]) : kNegInf);
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = CW / 4; w >= 1; w >>= 1)
 #pragma unroll
         for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
       br.rowmax[j][half][r] = mx[0];
@@ -324,19 +345,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
       }
       const float ms = m_run * a.scale_log2;
-      // 32 keys = chunks 4 half .. 4 half + 3 of this row's 128 bytes in the 128-byte swizzle layout
+      // CW keys = chunks c0 / 8 .. c0 / 8 + CW / 8 - 1 of this row's 128 bytes in the 128-byte swizzle
+      // layout (with KVP heads packed, the row's other chunks hold zeros from the prologue)
       unsigned char *rowp = p_s + j * CF::P_BYTES + r * 128;
       float lt[4] = {0.f, 0.f, 0.f, 0.f};           // four independent partial sums
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int ch = half * 4 + cc;
+      for (int cc = 0; cc < CW / 8; ++cc) {
+        const int ch = c0 / 8 + cc;
         uint32_t pk[4];
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2) {
           const int e = cc * 8 + e2 * 2;
           const float p0 = (e < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
           const float p1 = (e + 1 < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
-          lt[cc] += p0 + p1;
+          lt[cc & 3] += p0 + p1;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pk[e2] = *(uint32_t *)&h2;
         }
@@ -520,12 +542,32 @@ Plan make_plan(const AttnProblem &p) {
   Plan pl;
   pl.f0 = p.fresh0;
   pl.f1 = p.fresh0 + p.nq;
-  pl.ka = (pl.f0 + kKeys - 1) / kKeys;
-  pl.kf = (p.nq + kKeys - 1) / kKeys;
-  pl.kcn = (p.seq_len - pl.f1 + kKeys - 1) / kKeys;
-  pl.kt = pl.ka + pl.kf + pl.kcn;
   const int group = p.hq / p.hkv;
-  if (p.nq <= kTile) {
+  // MHA with few queries may pack 2 or 4 KV heads into the 128 rows (each a block of the score tile):
+  // no padding rows and fewer CTAs, but 2-4x the key tiles per CTA.  Measured on GB300, it pays only
+  // when the unpacked units (one per sequence and KV head) need more than one wave of CTAs; then the
+  // smallest packing that fits them in one wave is best (batch 8: 2 heads per tile, 43.6 us instead of
+  // 52.6; batch 16: 2 or 4, 60.8 us instead of 75.4; batch 1 or 4: unpacked).
+  pl.kvp = 1;
+  if (group == 1) {
+    const int sms = sm_count();
+    for (int kvp = 1; kvp <= 4; kvp *= 2) {
+      if (p.nq > kTile / kvp || p.hkv % kvp != 0) break;
+      pl.kvp = kvp;
+      if (p.batch * (p.hkv / kvp) <= sms) break;
+    }
+  }
+  pl.tk = kKeys / pl.kvp;
+  pl.ka = (pl.f0 + pl.tk - 1) / pl.tk;
+  pl.kf = (p.nq + pl.tk - 1) / pl.tk;
+  pl.kcn = (p.seq_len - pl.f1 + pl.tk - 1) / pl.tk;
+  pl.kt = pl.ka + pl.kf + pl.kcn;
+  if (pl.kvp > 1) {
+    pl.qr = kTile / pl.kvp;
+    pl.ht = pl.kvp;
+    pl.qtiles_per_head = 0;
+    pl.nqt = 1;
+  } else if (p.nq <= kTile) {
     pl.qr = (p.nq + 7) / 8 * 8;
     pl.ht = kTile / pl.qr;
     pl.qtiles_per_head = 0;
@@ -536,7 +578,7 @@ Plan make_plan(const AttnProblem &p) {
     pl.qtiles_per_head = (p.nq + kTile - 1) / kTile;
     pl.nqt = group * pl.qtiles_per_head;
   }
-  pl.units = p.batch * p.hkv * pl.nqt;
+  pl.units = p.batch * (p.hkv / pl.kvp) * pl.nqt;
   // split the key tiles of a unit over a cluster only as far as it fills idle SMs
   int ns = sm_count() / pl.units;
   if (ns > kMaxCluster) ns = kMaxCluster;
@@ -545,9 +587,9 @@ Plan make_plan(const AttnProblem &p) {
   return pl;
 }
 
-template <int D>
+template <int D, int KVP>
 cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cudaStream_t st) {
-  auto k = attn_tc_kernel<D>;
+  auto k = attn_tc_kernel<D, KVP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -585,12 +627,12 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
   const int64_t off_c = (int64_t)pl.f1 * p.hkv * p.d;
   if (!map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) ||
-      !map4(&maps[1], p.kc, p.d, p.hkv, pl.f0, p.batch, cstride, kKeys) ||
-      !map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, kKeys) ||
-      !map4(&maps[3], kc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, kKeys) ||
-      !map4(&maps[4], p.vc, p.d, p.hkv, pl.f0, p.batch, cstride, kKeys) ||
-      !map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, kKeys) ||
-      !map4(&maps[6], vc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, kKeys))
+      !map4(&maps[1], p.kc, p.d, p.hkv, pl.f0, p.batch, cstride, pl.tk) ||
+      !map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) ||
+      !map4(&maps[3], kc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, pl.tk) ||
+      !map4(&maps[4], p.vc, p.d, p.hkv, pl.f0, p.batch, cstride, pl.tk) ||
+      !map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) ||
+      !map4(&maps[6], vc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, pl.tk))
     return cudaErrorInvalidValue;
   Args a;
   a.pl = pl;
@@ -601,7 +643,14 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   a.out = p.out;
   a.lse = p.lse;
   a.err = p.err;
-  return p.d == 128 ? launch_d<128>(pl, maps, a, st) : launch_d<64>(pl, maps, a, st);
+  if (p.d == 128) {
+    if (pl.kvp == 4) return launch_d<128, 4>(pl, maps, a, st);
+    if (pl.kvp == 2) return launch_d<128, 2>(pl, maps, a, st);
+    return launch_d<128, 1>(pl, maps, a, st);
+  }
+  if (pl.kvp == 4) return launch_d<64, 4>(pl, maps, a, st);
+  if (pl.kvp == 2) return launch_d<64, 2>(pl, maps, a, st);
+  return launch_d<64, 1>(pl, maps, a, st);
 }
 
 }  // namespace fdllm

@@ -61,6 +61,19 @@ def test_bf16_modes(mode, d):
              dtype="bf16", seed=3)
 
 
+@pytest.mark.parametrize("batch,hq,d,block,prompt,gen,out_f32", [
+    (40, 8, 64, 16, 100, 64, 0),     # 320 head units > 152 SMs: 4 KV heads per tile, bf16 output
+    (24, 8, 128, 32, 90, 96, 1),     # 192 units: 2 per tile
+    (30, 6, 128, 20, 77, 60, 0),     # 6 heads: 2 per tile; ragged block and key counts
+    (48, 4, 64, 64, 40, 128, 1)])    # 64 queries: 2 per tile at most
+def test_mha_heads_packed_per_tile(batch, hq, d, block, prompt, gen, out_f32):
+    """MHA with a block of at most 64 queries and more (sequence, head) units than one wave of
+    CTAs packs 2 or 4 KV heads into one 128-row tile: row r's head owns a block of each score tile
+    and of P (the rest of the row is zero)."""
+    run_case(batch=batch, prompt_len=prompt, gen_length=gen, block_size=block, block_idx=1, hq=hq, hkv=hq, d=d,
+             mode="dual", dtype="bf16", seed=9, out_f32=out_f32)
+
+
 @pytest.mark.parametrize("hq,hkv", [(28, 4), (8, 1), (6, 2)])
 def test_bf16_gqa(hq, hkv):
     run_case(batch=2, prompt_len=130, gen_length=64, block_size=32, block_idx=0, hq=hq, hkv=hkv, d=128,
