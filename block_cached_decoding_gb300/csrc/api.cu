@@ -94,6 +94,9 @@ fdllm_status resolve_attn(const fdllm_attn_desc *d, AttnProblem &p) {
   const int s = d->prompt_len + d->block_idx * d->block_size;
   p.batch = d->batch;
   p.seq_len = (int)n;
+  p.blocks = nullptr;
+  p.prompt_len = d->prompt_len;
+  p.nblocks = nblocks;
   p.hq = d->n_q_heads;
   p.hkv = d->n_kv_heads;
   p.d = d->head_dim;
@@ -167,6 +170,7 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   p.batch = d->batch;
   p.seq_len = d->seq_len;
   p.s = d->block_start;
+  p.starts = nullptr;
   p.B = d->block_size;
   p.H = d->hidden;
   p.V = d->vocab;
@@ -217,7 +221,7 @@ using namespace fdllm;
 
 extern "C" {
 
-int32_t fdllm_version(void) { return 100; }
+int32_t fdllm_version(void) { return 101; }
 
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
   if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");
@@ -257,6 +261,7 @@ fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail) {
     if (st != FDLLM_OK) return st;
   }
   if (detail) *detail = v;
+  if (v >= 231 && v <= 233) return fail(FDLLM_EINVAL, "per-sequence block index out of range (site %d)", v);
   return v ? fail(FDLLM_ETIMEOUT, "device wait gave up at site %d", v) : FDLLM_OK;
 }
 
@@ -276,13 +281,18 @@ size_t fdllm_attn_workspace_size(const fdllm_attn_desc *desc) {
   return attn_workspace(p);
 }
 
-fdllm_status fdllm_block_attn(const fdllm_attn_desc *desc, const void *q, const void *k_cache,
-                              const void *v_cache, const void *k_fresh, const void *v_fresh,
-                              void *out, float *lse, void *workspace, size_t ws_bytes,
-                              fdllm_stream_t stream) {
+static fdllm_status block_attn(const fdllm_attn_desc *desc, const int32_t *blocks, const void *q,
+                               const void *k_cache, const void *v_cache, const void *k_fresh,
+                               const void *v_fresh, void *out, float *lse, void *workspace, size_t ws_bytes,
+                               fdllm_stream_t stream) {
   AttnProblem p;
   fdllm_status st = resolve_attn(desc, p);
   if (st != FDLLM_OK) return st;
+  if (blocks) {
+    if (!desc->use_cache || !desc->dual_cache || !attn_tc_supported(p))
+      return fail(FDLLM_EUNSUPPORTED, "attn: per-sequence blocks need DualCache and bf16");
+    p.blocks = blocks;
+  }
   const void *req[] = {q, k_cache, v_cache, k_fresh, v_fresh, out};
   const char *names[] = {"q", "k_cache", "v_cache", "k_fresh", "v_fresh", "out"};
   for (int i = 0; i < 6; ++i) {
@@ -300,20 +310,35 @@ fdllm_status fdllm_block_attn(const fdllm_attn_desc *desc, const void *q, const 
   return cuda_status(attn_tc_supported(p) ? launch_attn_tc(p, cs) : launch_attn_simt(p, cs), "attn launch");
 }
 
+fdllm_status fdllm_block_attn(const fdllm_attn_desc *desc, const void *q, const void *k_cache,
+                              const void *v_cache, const void *k_fresh, const void *v_fresh,
+                              void *out, float *lse, void *workspace, size_t ws_bytes,
+                              fdllm_stream_t stream) {
+  return block_attn(desc, nullptr, q, k_cache, v_cache, k_fresh, v_fresh, out, lse, workspace, ws_bytes, stream);
+}
+
+fdllm_status fdllm_block_attn_ragged(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
+                                     const void *k_cache, const void *v_cache, const void *k_fresh,
+                                     const void *v_fresh, void *out, float *lse, void *workspace,
+                                     size_t ws_bytes, fdllm_stream_t stream) {
+  if (!block_idx) return fail(FDLLM_EINVAL, "attn: block_idx is null");
+  return block_attn(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fresh, out, lse, workspace, ws_bytes, stream);
+}
+
 size_t fdllm_select_workspace_size(const fdllm_select_desc *desc) {
   SelectProblem p;
   if (resolve_select(desc, p) != FDLLM_OK) return 0;
   return select_layout(p).total;
 }
 
-fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *hidden,
-                                     const void *lm_head_w, int32_t *tokens, uint8_t *unmasked,
-                                     float *conf, float *kappa, int32_t *argmax,
-                                     int32_t *n_masked_left, void *workspace, size_t ws_bytes,
-                                     fdllm_stream_t stream) {
+static fdllm_status confidence_select(const fdllm_select_desc *desc, const int32_t *starts, const void *hidden,
+                                      const void *lm_head_w, int32_t *tokens, uint8_t *unmasked, float *conf,
+                                      float *kappa, int32_t *argmax, int32_t *n_masked_left, void *workspace,
+                                      size_t ws_bytes, fdllm_stream_t stream) {
   SelectProblem p;
   fdllm_status st = resolve_select(desc, p);
   if (st != FDLLM_OK) return st;
+  p.starts = starts;
   const void *req[] = {hidden, lm_head_w, tokens, unmasked, conf, argmax, n_masked_left, workspace};
   const char *names[] = {"hidden", "lm_head_w", "tokens", "unmasked", "conf", "argmax", "n_masked_left", "workspace"};
   for (int i = 0; i < 8; ++i)
@@ -328,6 +353,25 @@ fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *
   p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
   p.err = error_word_ptr();
   return cuda_status(run_select(p, L, workspace, (cudaStream_t)stream), "lm-head / select launch");
+}
+
+fdllm_status fdllm_confidence_select(const fdllm_select_desc *desc, const void *hidden,
+                                     const void *lm_head_w, int32_t *tokens, uint8_t *unmasked,
+                                     float *conf, float *kappa, int32_t *argmax,
+                                     int32_t *n_masked_left, void *workspace, size_t ws_bytes,
+                                     fdllm_stream_t stream) {
+  return confidence_select(desc, nullptr, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax, n_masked_left,
+                           workspace, ws_bytes, stream);
+}
+
+fdllm_status fdllm_confidence_select_ragged(const fdllm_select_desc *desc, const int32_t *block_start,
+                                            const void *hidden, const void *lm_head_w, int32_t *tokens,
+                                            uint8_t *unmasked, float *conf, float *kappa, int32_t *argmax,
+                                            int32_t *n_masked_left, void *workspace, size_t ws_bytes,
+                                            fdllm_stream_t stream) {
+  if (!block_start) return fail(FDLLM_EINVAL, "select: block_start is null");
+  return confidence_select(desc, block_start, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax,
+                           n_masked_left, workspace, ws_bytes, stream);
 }
 
 fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
@@ -352,6 +396,26 @@ fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32
   }
   return cuda_status(launch_splice(batch, seq_len, row_bytes, start, len, k_cache, v_cache, k_src,
                                    v_src, (cudaStream_t)stream),
+                     "splice launch");
+}
+
+fdllm_status fdllm_kv_splice_ragged(int32_t batch, int32_t seq_len, int32_t n_kv_heads, int32_t head_dim,
+                                    const int32_t *start, int32_t len, int32_t dtype, void *k_cache,
+                                    void *v_cache, const void *k_src, const void *v_src, fdllm_stream_t stream) {
+  if (!start) return fail(FDLLM_EINVAL, "splice: start is null");
+  if (batch < 1 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1)
+    return fail(FDLLM_EINVAL, "splice: batch, seq_len, n_kv_heads and head_dim must be >= 1");
+  if (dtype != FDLLM_BF16 && dtype != FDLLM_F32) return fail(FDLLM_EINVAL, "splice: bad dtype %d", dtype);
+  if (len < 0 || len > seq_len) return fail(FDLLM_EINVAL, "splice: len %d outside [0, %d]", len, seq_len);
+  const int64_t row_bytes = (int64_t)n_kv_heads * head_dim * (dtype == FDLLM_BF16 ? 2 : 4);
+  if (row_bytes % 16 != 0) return fail(FDLLM_EINVAL, "splice: Hkv * d * element size must be a multiple of 16 bytes");
+  const void *ptrs[] = {k_cache, v_cache, k_src, v_src};
+  for (int i = 0; i < 4; ++i) {
+    if (!ptrs[i]) return fail(FDLLM_EINVAL, "splice: null pointer");
+    if (!aligned16(ptrs[i])) return fail(FDLLM_EINVAL, "splice: pointers must be 16-byte aligned");
+  }
+  return cuda_status(launch_splice(batch, seq_len, row_bytes, 0, len, k_cache, v_cache, k_src, v_src,
+                                   (cudaStream_t)stream, start, error_word_ptr()),
                      "splice launch");
 }
 

@@ -59,6 +59,7 @@ struct Plan {
   int nqt;              // query tiles per KV head group
   int kvp;              // KV heads per tile (1, or 2 / 4 for MHA with few queries)
   int tk;               // keys per KV head per key tile (64 / kvp)
+  int abs_suffix;       // suffix rows are absolute cache rows (per-sequence blocks: full-cache maps)
   int units;            // batch * (Hkv / kvp) * nqt
 };
 
@@ -113,7 +114,8 @@ __device__ __forceinline__ KeyTile key_tile(const Plan &pl, int nq, int n, int k
   } else if (k < pl.ka + pl.kf) {
     t.range = 1; t.row0 = (k - pl.ka) * pl.tk; t.nvalid = min(pl.tk, nq - t.row0);
   } else {
-    t.range = 2; t.row0 = (k - pl.ka - pl.kf) * pl.tk; t.nvalid = min(pl.tk, n - pl.f1 - t.row0);
+    const int r2 = (k - pl.ka - pl.kf) * pl.tk;    // row within the suffix
+    t.range = 2; t.row0 = (pl.abs_suffix ? pl.f1 : 0) + r2; t.nvalid = min(pl.tk, n - pl.f1 - r2);
   }
   return t;
 }
@@ -127,6 +129,8 @@ struct Args {
   void *out;
   float *lse;
   int32_t *err;
+  const int32_t *blocks;   // per-sequence DualCache block indices (null: the plan's window for all)
+  int prompt_len, nblocks;
 };
 
 __device__ __forceinline__ void fail(Bars &br, int32_t *err, int site) {
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char *p_s = kv_s + CF::RING;                 // 2 P buffers
   Bars &br = *(Bars *)(p_s + 2 * CF::P_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Plan &pl = a.pl;
+  Plan pl = a.pl;   // per-sequence blocks fill in this CTA's ranges after the dependency wait
 
   const int split = blockIdx.x % pl.nsplit;
   const int unit = blockIdx.x / pl.nsplit;
@@ -165,8 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = unit % pl.nqt;
   const int kvh = ((unit / pl.nqt) % nkvg) * KVP;        // first KV head of this tile
   const int b = unit / (pl.nqt * nkvg);
-  const int k0 = (int)((int64_t)pl.kt * split / pl.nsplit);
-  const int nt = (int)((int64_t)pl.kt * (split + 1) / pl.nsplit) - k0;
   int h0, nh, q0;
   if (KVP > 1) {
     h0 = 0; nh = KVP; q0 = 0;                          // head slot s = KV head kvh + s (MHA)
@@ -206,6 +208,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = br.tmem_base;
+  if (a.blocks != nullptr) {
+    // this sequence's own block: cached prefix [0, f0), fresh window [f0, f1), cached suffix [f1, N);
+    // an index outside [0, nblocks) gives no key tiles (and device error 232)
+    const int bi = a.blocks[b];
+    if (bi >= 0 && bi < a.nblocks) {
+      pl.f0 = a.prompt_len + bi * a.nq;
+      pl.f1 = pl.f0 + a.nq;
+      pl.ka = (pl.f0 + pl.tk - 1) / pl.tk;
+      pl.kf = (a.nq + pl.tk - 1) / pl.tk;
+      pl.kcn = (a.n - pl.f1 + pl.tk - 1) / pl.tk;
+      pl.kt = pl.ka + pl.kf + pl.kcn;
+    } else {
+      pl.kt = 0;
+      if (threadIdx.x == 0 && split == 0) record_device_error(a.err, 232);
+    }
+  }
+  const int k0 = (int)((int64_t)pl.kt * split / pl.nsplit);
+  const int nt = (int)((int64_t)pl.kt * (split + 1) / pl.nsplit) - k0;
 
   // thread of the softmax warps: its query row, column half and running state (reference max, l)
   const int r = (warp & 3) * 32 + lane;
@@ -380,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     br.lhalf[half][r] = l_run;
     softmax_bar();
     l_run = ok ? br.lhalf[0][r] + br.lhalf[1][r] : 0.f;
-    if (pl.nsplit == 1 && ok) {
+    if (pl.nsplit == 1 && ok && l_run > 0.f) {
       int hs, qi;
       const bool valid = row_target(pl, a.nq, nh, q0, r, hs, qi);
       const int h = kvh * a.group + h0 + hs;
@@ -579,10 +599,13 @@ Plan make_plan(const AttnProblem &p) {
     pl.nqt = group * pl.qtiles_per_head;
   }
   pl.units = p.batch * (p.hkv / pl.kvp) * pl.nqt;
+  pl.abs_suffix = p.blocks != nullptr;
+  // per-sequence blocks: a sequence has at most ceil(N / tk) + 2 key tiles (two ragged boundaries)
+  const int kt_max = p.blocks != nullptr ? (p.seq_len + pl.tk - 1) / pl.tk + 2 : pl.kt;
   // split the key tiles of a unit over a cluster only as far as it fills idle SMs
   int ns = sm_count() / pl.units;
   if (ns > kMaxCluster) ns = kMaxCluster;
-  if (ns > pl.kt) ns = pl.kt;
+  if (ns > kt_max) ns = kt_max;
   pl.nsplit = ns < 1 ? 1 : ns;
   return pl;
 }
@@ -625,14 +648,18 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t qstride = (int64_t)p.nq * p.hq * p.d;
   CUtensorMap maps[7];
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
-  const int64_t off_c = (int64_t)pl.f1 * p.hkv * p.d;
+  // per-sequence blocks: prefix and suffix tiles are read through maps of the whole cache; rows of a
+  // sequence's own window that fall in a boundary tile are read and weighted by exactly zero
+  const bool per_seq = p.blocks != nullptr;
+  const int64_t off_c = per_seq ? 0 : (int64_t)pl.f1 * p.hkv * p.d;
+  const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
   if (!map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) ||
-      !map4(&maps[1], p.kc, p.d, p.hkv, pl.f0, p.batch, cstride, pl.tk) ||
+      !map4(&maps[1], p.kc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) ||
       !map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) ||
-      !map4(&maps[3], kc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, pl.tk) ||
-      !map4(&maps[4], p.vc, p.d, p.hkv, pl.f0, p.batch, cstride, pl.tk) ||
+      !map4(&maps[3], kc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk) ||
+      !map4(&maps[4], p.vc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) ||
       !map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) ||
-      !map4(&maps[6], vc + off_c, p.d, p.hkv, p.seq_len - pl.f1, p.batch, cstride, pl.tk))
+      !map4(&maps[6], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk))
     return cudaErrorInvalidValue;
   Args a;
   a.pl = pl;
@@ -643,6 +670,9 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   a.out = p.out;
   a.lse = p.lse;
   a.err = p.err;
+  a.blocks = p.blocks;
+  a.prompt_len = p.prompt_len;
+  a.nblocks = p.nblocks;
   if (p.d == 128) {
     if (pl.kvp == 4) return launch_d<128, 4>(pl, maps, a, st);
     if (pl.kvp == 2) return launch_d<128, 2>(pl, maps, a, st);

@@ -15,6 +15,10 @@ struct VocabStat;  // common.cuh
 struct AttnProblem {
   int batch, seq_len, nq, hq, hkv, d;
   int fresh0;       // first position with fresh K/V (== first query position)
+  // per-sequence DualCache blocks (null: every sequence at fresh0): sequence b's block is
+  // blocks[b], its window [prompt_len + blocks[b] * nq, + nq); nblocks bounds the index
+  const int32_t *blocks;
+  int prompt_len, nblocks;
   float scale;      // softmax scale
   int in_bf16;      // q / k / v storage
   int out_f32;
@@ -29,6 +33,7 @@ struct AttnProblem {
 // Resolved select problem.
 struct SelectProblem {
   int batch, seq_len, s, B, H, V, mask_id, strategy, topk;
+  const int32_t *starts;  // device [batch]: sequence b's block starts at starts[b] (null: every block at s)
   float kappa_tau;  // c > tau  <=>  kappa < kappa_tau
   float factor;
   int in_bf16;
@@ -41,6 +46,16 @@ struct SelectProblem {
   size_t ws_bytes;
   int32_t *err;
 };
+
+#ifdef __CUDACC__
+// Block start of sequence b: its own when the problem gives one per sequence, else the shared one;
+// -1 when a per-sequence start does not fit the sequence (the select records device error 231).
+__device__ __forceinline__ int seq_block_start(const SelectProblem &p, int b) {
+  if (p.starts == nullptr) return p.s;
+  const int v = p.starts[b];
+  return (v >= 0 && v <= p.seq_len - p.B) ? v : -1;
+}
+#endif
 
 int sm_count();  // SMs of the current device (cached per device)
 void count_launches(int n);  // adds to fdllm_launch_counter()
@@ -69,9 +84,11 @@ cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned l
 // select.cu: merge partials [b * B, splits] over splits and unmask
 cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st);
 
-// splice.cu
+// splice.cu: cache[b, start_b : start_b + len] <- src[b] for K and V, start_b = starts[b] when
+// `starts` (device) is given, else `start`; a start outside [0, cache_rows - len] skips the sequence
+// and records device error 233 in `err`
 cudaError_t launch_splice(int batch, int64_t cache_rows, int64_t row_bytes, int64_t start,
                           int64_t len, void *kc, void *vc, const void *ks, const void *vs,
-                          cudaStream_t st);
+                          cudaStream_t st, const int32_t *starts = nullptr, int32_t *err = nullptr);
 
 }  // namespace fdllm

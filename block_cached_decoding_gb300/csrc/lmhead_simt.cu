@@ -17,16 +17,18 @@ constexpr int kRowGroup = 4;  // masked rows sharing one pass over a W row
 
 // Masked rows of the block in (sequence, position) order, compacted with warp
 // ballots; returns the count.  rows[r] = b * B + i.
-__device__ int compact_masked_rows(const int32_t *tokens, int batch, int seq_len, int s, int B,
-                                   int mask_id, int *rows) {
+__device__ int compact_masked_rows(const SelectProblem &p, int *rows) {
+  const int32_t *tokens = p.tokens;
+  const int batch = p.batch, seq_len = p.seq_len, B = p.B, mask_id = p.mask_id;
   __shared__ int count;
   if (threadIdx.x < 32) {
     int base = 0;
     const int lane = threadIdx.x;
     for (int b = 0; b < batch; ++b) {
+      const int sb = seq_block_start(p, b);
       for (int c = 0; c < B; c += 32) {
         const int i = c + lane;
-        const bool m = i < B && tokens[(int64_t)b * seq_len + s + i] == mask_id;
+        const bool m = sb >= 0 && i < B && tokens[(int64_t)b * seq_len + sb + i] == mask_id;
         const unsigned bal = __ballot_sync(0xffffffffu, m);
         if (m) rows[base + __popc(bal & ((1u << lane) - 1u))] = b * B + i;
         base += __popc(bal);
@@ -63,7 +65,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   extern __shared__ unsigned char smem_raw[];
   int *rows = (int *)smem_raw;                                        // [batch * B]
   VocabStat *st = (VocabStat *)(smem_raw + ((p.batch * p.B * 4 + 15) & ~15));  // [kWarps][R]
-  const int R = compact_masked_rows(p.tokens, p.batch, p.seq_len, p.s, p.B, p.mask_id, rows);
+  const int R = compact_masked_rows(p, rows);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   tc::pdl_launch_dependents();
   for (int r = threadIdx.x; r < kWarps * R; r += blockDim.x) st[r] = vs_identity();

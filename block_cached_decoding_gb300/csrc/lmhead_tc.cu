@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const SelectProblem sp, VocabStat *__restrict__ part, unsigned long long *ticket,
                      uint32_t epoch) {
   const int32_t *__restrict__ tokens = sp.tokens;
-  const int batch = sp.batch, seq_len = sp.seq_len, s = sp.s, B = sp.B, mask_id = sp.mask_id, H = sp.H, V = sp.V;
+  const int batch = sp.batch, seq_len = sp.seq_len, B = sp.B, mask_id = sp.mask_id, H = sp.H, V = sp.V;
   int32_t *err = sp.err;
   using C = Cfg;
   extern __shared__ unsigned char smem_raw[];
@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool m = false;
     if (r < rows) {
       const int bb = r / B, i = r - bb * B;
-      m = tokens[(int64_t)bb * seq_len + s + i] == mask_id;
+      const int sb = seq_block_start(sp, bb);
+      m = sb >= 0 && tokens[(int64_t)bb * seq_len + sb + i] == mask_id;
     }
     sh.masked[r] = m;
     if (m) atomicOr(&sh.active, 1u << (r / kABox));

@@ -47,7 +47,7 @@ struct SelectScratch {
   float kap[kSelectMaxBlock];
   float cf[kSelectMaxBlock];
   int tok[kSelectMaxBlock];
-  int m, any, nbest, nsel;
+  int m, any, nbest, nsel, start;
 };
 
 // The merged statistics of the j-th masked position into the scratch (lane 0 of the merging warp).
@@ -67,13 +67,17 @@ template <int NT>
 __device__ __forceinline__ void select_prepare(const SelectProblem &p, int b, SelectScratch &sc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
-  const int32_t *trow = p.tokens + (int64_t)b * p.seq_len + p.s;
-  if (tid == 0) { sc.any = 0; sc.nbest = 0; sc.nsel = 0; }
+  const int sb = seq_block_start(p, b);
+  const int32_t *trow = p.tokens + (int64_t)b * p.seq_len + (sb < 0 ? 0 : sb);
+  if (tid == 0) {
+    sc.any = 0; sc.nbest = 0; sc.nsel = 0; sc.start = sb;
+    if (sb < 0) record_device_error(p.err, 231);
+  }
   if (warp == 0) {
     int base = 0;
     for (int c = 0; c < B; c += 32) {
       const int i = c + lane;
-      const bool m = i < B && trow[i] == p.mask_id;
+      const bool m = sb >= 0 && i < B && trow[i] == p.mask_id;
       const unsigned bal = __ballot_sync(0xffffffffu, m);
       if (m) sc.mpos[base + __popc(bal & ((1u << lane) - 1u))] = i;
       base += __popc(bal);
@@ -233,7 +237,7 @@ __device__ __forceinline__ void select_finish(const SelectProblem &p, const Voca
     if (p.kappa) p.kappa[o] = masked ? sc.kap[i] : __int_as_float(0x7fffffff);
     p.argmax[o] = masked ? sc.tok[i] : -1;
     if (sel) {
-      p.tokens[(int64_t)b * p.seq_len + p.s + i] = sc.tok[i];
+      p.tokens[(int64_t)b * p.seq_len + sc.start + i] = sc.tok[i];
       atomicAdd(&sc.nsel, 1);
     }
   }

@@ -25,7 +25,8 @@ EXPORTS = (
     "fdllm_status_string", "fdllm_last_error", "fdllm_last_device_error", "fdllm_version",
     "fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
     "fdllm_synth_prompt", "fdllm_launch_counter", "fdllm_confidence_select_noalloc",
-    "fdllm_selftest_bounded_wait",
+    "fdllm_selftest_bounded_wait", "fdllm_block_attn_ragged", "fdllm_confidence_select_ragged",
+    "fdllm_kv_splice_ragged",
 )
 
 NOALLOC_SCRATCH_BYTES = 2 << 20
@@ -78,6 +79,12 @@ def lib() -> C.CDLL:
         L.fdllm_confidence_select_noalloc.restype = i32
         L.fdllm_kv_splice.argtypes = [i32] * 8 + [vp] * 5
         L.fdllm_kv_splice.restype = i32
+        L.fdllm_block_attn_ragged.argtypes = [C.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.fdllm_block_attn_ragged.restype = i32
+        L.fdllm_confidence_select_ragged.argtypes = [C.POINTER(SelectDesc)] + [vp] * 10 + [sz, vp]
+        L.fdllm_confidence_select_ragged.restype = i32
+        L.fdllm_kv_splice_ragged.argtypes = [i32] * 4 + [vp, i32, i32] + [vp] * 5
+        L.fdllm_kv_splice_ragged.restype = i32
         L.fdllm_status_string.argtypes = [i32]
         L.fdllm_status_string.restype = C.c_char_p
         L.fdllm_last_error.argtypes = []
@@ -189,6 +196,34 @@ def fdllm_kv_splice(mode, batch, seq_len, n_kv_heads, head_dim, start, length, d
                     k_src, v_src, stream=None):
     _check(lib().fdllm_kv_splice(mode, batch, seq_len, n_kv_heads, head_dim, start, length, dtype,
                                  _ptr(k_cache), _ptr(v_cache), _ptr(k_src), _ptr(v_src), _stream(stream)))
+
+
+def fdllm_block_attn_ragged(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fresh, out, lse=None,
+                            workspace=None, ws_bytes=None, stream=None):
+    """fdllm_block_attn (DualCache) with sequence b at block block_idx[b] (device int32 [batch])."""
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_block_attn_ragged(C.byref(desc), _ptr(block_idx), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(k_fresh), _ptr(v_fresh), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         ws_bytes, _stream(stream)))
+
+
+def fdllm_confidence_select_ragged(desc, block_start, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax,
+                                   n_masked_left, workspace, ws_bytes=None, stream=None):
+    """fdllm_confidence_select with sequence b's block at block_start[b] (device int32 [batch])."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_confidence_select_ragged(C.byref(desc), _ptr(block_start), _ptr(hidden), _ptr(lm_head_w),
+                                                _ptr(tokens), _ptr(unmasked), _ptr(conf), _ptr(kappa),
+                                                _ptr(argmax), _ptr(n_masked_left), _ptr(workspace), ws_bytes,
+                                                _stream(stream)))
+
+
+def fdllm_kv_splice_ragged(batch, seq_len, n_kv_heads, head_dim, start, length, dtype, k_cache, v_cache,
+                           k_src, v_src, stream=None):
+    """Window splice with sequence b's window at start[b] (device int32 [batch])."""
+    _check(lib().fdllm_kv_splice_ragged(batch, seq_len, n_kv_heads, head_dim, _ptr(start), length, dtype,
+                                        _ptr(k_cache), _ptr(v_cache), _ptr(k_src), _ptr(v_src), _stream(stream)))
 
 
 def fdllm_last_device_error(stream=None) -> tuple[int, int]:

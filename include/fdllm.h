@@ -237,6 +237,48 @@ fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32
                              fdllm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Per-sequence (non-lock-step) blocks                                       */
+/* ------------------------------------------------------------------------ */
+/* Batched decoding (summary, "Throughput scaling with batch size", Appendix C.5,
+ * Figure 9) where each sequence is at its own block: a sequence whose block is
+ * done moves to its next block without waiting for the others.  The pages do
+ * not describe the batched loop; these calls are the plain per-sequence reading.
+ * Each takes the per-sequence block as a device array, so a decode loop can
+ * advance it on the GPU.  Indices are checked on the device: a sequence whose
+ * index is out of range is skipped and fdllm_last_device_error then reports
+ * FDLLM_EINVAL (site 231 select, 232 attention, 233 splice). */
+
+/* fdllm_block_attn with DualCache (desc->dual_cache = 1, use_cache = 1, bf16),
+ * sequence b at block block_idx[b] (device int32 [batch], in
+ * [0, gen_length / block_size)); desc->block_idx is only validated.  q, k_fresh,
+ * v_fresh and out are [b, block_size, H, d] as for fdllm_block_attn.  Rows of
+ * sequence b's own window [s_b, s_b + block_size) in the caches are read where
+ * a key tile crosses the window's edge and weighted by exactly zero, so they
+ * must hold finite values (any earlier keys and values, or zeros).  Needs the
+ * workspace of fdllm_attn_workspace_size(desc).  FDLLM_EUNSUPPORTED for fp32 or
+ * without DualCache. */
+fdllm_status fdllm_block_attn_ragged(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
+                                     const void *k_cache, const void *v_cache, const void *k_fresh,
+                                     const void *v_fresh, void *out, float *lse, void *workspace,
+                                     size_t ws_bytes, fdllm_stream_t stream);
+
+/* fdllm_confidence_select with sequence b's block starting at block_start[b]
+ * (device int32 [batch], in [0, seq_len - block_size]); desc->block_start is
+ * only validated.  Same workspace (fdllm_select_workspace_size(desc)) and
+ * outputs; hidden row (b, i) is the state of position block_start[b] + i. */
+fdllm_status fdllm_confidence_select_ragged(const fdllm_select_desc *desc, const int32_t *block_start,
+                                            const void *hidden, const void *lm_head_w, int32_t *tokens,
+                                            uint8_t *unmasked, float *conf, float *kappa, int32_t *argmax,
+                                            int32_t *n_masked_left, void *workspace, size_t ws_bytes,
+                                            fdllm_stream_t stream);
+
+/* FDLLM_SPLICE_WINDOW with sequence b's window at start[b] (device int32
+ * [batch], in [0, seq_len - len]): cache[b, start[b] : start[b] + len] <- src[b]. */
+fdllm_status fdllm_kv_splice_ragged(int32_t batch, int32_t seq_len, int32_t n_kv_heads, int32_t head_dim,
+                                    const int32_t *start, int32_t len, int32_t dtype, void *k_cache,
+                                    void *v_cache, const void *k_src, const void *v_src, fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
 
@@ -248,8 +290,9 @@ const char *fdllm_status_string(int32_t status);
 const char *fdllm_last_error(void);
 
 /* Synchronises `stream`, then reads and clears the current device's error
- * word: FDLLM_OK if no device wait gave up since the last read, else
- * FDLLM_ETIMEOUT (`detail`, if not NULL, receives the site code). */
+ * word: FDLLM_OK if nothing was recorded since the last read; FDLLM_EINVAL if a
+ * per-sequence block index was out of range (sites 231-233); else FDLLM_ETIMEOUT,
+ * a device wait that gave up (`detail`, if not NULL, receives the site code). */
 fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
 
 /* Failure-detection self-test: launches one CTA that waits, through the same
@@ -260,7 +303,7 @@ fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
  * usable.  Returns FDLLM_EINVAL for a limit outside 1..1000. */
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream);
 
-/* ABI version: 100 * major + minor. */
+/* ABI version: 100 * major + minor (101: the per-sequence block calls). */
 int32_t fdllm_version(void);
 
 /* Number of kernels this library has launched in the process so far (all

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert F.fdllm_version() == 100
+    assert F.fdllm_version() == 101
     for s in range(5):
         assert lib.fdllm_status_string(s).decode().startswith("FDLLM_")
 
@@ -117,3 +117,21 @@ def test_splice_rejects_bad_windows(lib, args):
     with pytest.raises(F.FdllmError) as e:
         F.fdllm_kv_splice(mode, b, n, hkv, d, start, ln, dtype, 16, 16, 16, 16, stream=0)
     assert e.value.status == F.EINVAL
+
+
+def test_per_sequence_block_calls_validate_on_the_host(lib):
+    """The per-sequence calls reject a missing index array and unsupported modes before any launch."""
+    def st(fn, *args):
+        return fn(*args)
+    d = _attn(dtype=F.BF16, head_dim=128)
+    v = C.c_void_p(16)                       # never dereferenced: validation fails first
+    assert lib.fdllm_block_attn_ragged(C.byref(d), None, v, v, v, v, v, v, None, v, 1 << 20, None) == F.EINVAL
+    fp32 = _attn()
+    assert lib.fdllm_block_attn_ragged(C.byref(fp32), v, v, v, v, v, v, v, None, v, 1 << 20, None) == F.EUNSUPPORTED
+    prefix = _attn(dtype=F.BF16, head_dim=128, dual_cache=0)
+    assert lib.fdllm_block_attn_ragged(C.byref(prefix), v, v, v, v, v, v, v, None, v, 1 << 20, None) == F.EUNSUPPORTED
+    sd = F.select_desc(batch=2, seq_len=64, block_start=0, block_size=16, hidden=128, vocab=100, mask_id=100)
+    assert lib.fdllm_confidence_select_ragged(C.byref(sd), None, v, v, v, v, v, v, v, v, v, 1 << 20,
+                                              None) == F.EINVAL
+    assert lib.fdllm_kv_splice_ragged(2, 64, 4, 64, None, 16, F.BF16, v, v, v, v, None) == F.EINVAL
+    assert lib.fdllm_kv_splice_ragged(2, 64, 4, 64, v, 65, F.BF16, v, v, v, v, None) == F.EINVAL
