@@ -24,7 +24,10 @@ Readings where the pages are silent (listed again in the design doc):
   fallback pick.
 * R4 softmax scale 1/sqrt(head_dim); no causal mask (bidirectional).
 * R5 PrefixCache queries are the block *and* the suffix positions [s, N).
-* R6 batched decoding runs in lock step over a shared block index.
+* R6 batched decoding runs in lock step over a shared block index; with
+  per-sequence blocks each sequence is this oracle run alone at its own window.
+* R13 FP8 weight cache: E4M3 codes, one power-of-two scale per row, round to
+  nearest even; hidden rows quantised the same way per step.
 """
 from __future__ import annotations
 
@@ -319,3 +322,100 @@ def greedy(table):
 def kv_cache_bytes(seq_len, layers, heads, head_dim, bytes_per_elem):
     """Key plus value cache size (section 6, Limitation 6): N x layers x heads x d x 2 (K and V) x bytes."""
     return seq_len * layers * heads * head_dim * 2 * bytes_per_elem
+
+
+# ---------------------------------------------------------------------------
+# f4: FP8 weight cache.  The summary proposes storing cached activations in
+# INT8 or FP8 (section 6, the memory-overhead limitation; section 7, future
+# direction 3 "KV cache quantization and memory-efficient DualCache") without
+# fixing a scheme.  Reading R13, applied to the LM-head weight (the largest
+# per-step read of the path): E4M3 values (OCP FP8: 1 sign, 4 exponent bits
+# with bias 7, 3 mantissa bits, subnormals, largest finite 448, no infinity),
+# one power-of-two scale per row -- the smallest 2^k with max|row| <= 448 * 2^k
+# -- and round to nearest, ties to even.  Hidden rows are quantised the same
+# way, per row, at each step (the FP8 tensor-core product takes both operands
+# in FP8).  The logits are (s_h s_w) * sum_k qh_k qw_k, evaluated here in float64.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes):
+    """Values of E4M3 byte codes (uint8 array); the two NaN codes (S.1111.111) give NaN."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_round(y):
+    """Nearest E4M3 value to each y (|y| <= 448), ties to the even mantissa.
+
+    The grid step in [2^e, 2^(e+1)) is 2^(e-3) for e >= -6; below 2^-6
+    (subnormals) it is 2^-9."""
+    y = np.asarray(y, dtype=np.float64)
+    assert np.all(np.abs(y) <= E4M3_MAX), "outside the E4M3 range"
+    a = np.abs(y)
+    out = np.zeros_like(a)
+    nz = a > 0
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    # log2 may land one off at exact powers of two: fix e so that 2^e <= a < 2^(e+1)
+    e = np.where(np.exp2(e) > a, e - 1, e)
+    e = np.where(np.exp2(e + 1) <= a, e + 1, e)
+    step = np.exp2(np.maximum(e, -6.0) - 3.0)
+    out = np.where(nz, np.round(a / step) * step, 0.0)      # np.round: half to even, a / step exact
+    return np.sign(y) * out
+
+
+def e4m3_encode(v):
+    """Byte codes of E4M3 values (exactly representable, finite)."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    sign = np.where(np.signbit(v), 0x80, 0)
+    codes = np.zeros(v.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    codes = np.where(sub, np.round(a / 2.0 ** -9), 0).astype(np.int64)
+    e = np.floor(np.log2(np.where(sub, 1.0, a)))
+    e = np.where(np.exp2(e) > a, e - 1, e)
+    e = np.where(np.exp2(e + 1) <= a, e + 1, e)
+    m = np.where(sub, 0, a / np.exp2(e) * 8.0 - 8.0)
+    normal = ((e + 7).astype(np.int64) << 3) | m.astype(np.int64)
+    codes = np.where(sub, codes, normal)
+    assert np.array_equal(e4m3_decode(codes | sign), v), "not an E4M3 value"
+    return (codes | sign).astype(np.uint8)
+
+
+def fp8_scale_exponent(amax):
+    """Smallest integer k with amax <= 448 * 2^k (0 for amax = 0), decided exactly:
+    amax = f 2^x with f in [0.5, 1) (frexp) and 448 = 0.875 * 2^9."""
+    if amax == 0:
+        return 0
+    f, x = math.frexp(float(amax))
+    return x - 9 if f <= 0.875 else x - 8
+
+
+def quantize_fp8_rows(x):
+    """Per-row FP8 quantisation of x [R, C] (finite float values): returns (codes uint8 [R, C],
+    scales float64 [R] = 2^k); the row's values are codes' values times its scale."""
+    x = np.asarray(x, dtype=np.float64)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    scales = np.ones(x.shape[0])
+    for r in range(x.shape[0]):
+        k = fp8_scale_exponent(np.abs(x[r]).max() if x.shape[1] else 0.0)
+        scales[r] = 2.0 ** k
+        codes[r] = e4m3_encode(e4m3_round(x[r] * 2.0 ** -k))
+    return codes, scales
+
+
+def dequantize_fp8_rows(codes, scales):
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[:, None]
+
+
+def lm_head_confidence_fp8(h, w_codes, w_scales):
+    """lm_head_confidence with the FP8 weight cache: the hidden rows h [R, H] are quantised
+    per row, then both operands are their exact FP8 values times their scales."""
+    hq, hs = quantize_fp8_rows(h)
+    return lm_head_confidence(dequantize_fp8_rows(hq, hs), dequantize_fp8_rows(w_codes, w_scales))
