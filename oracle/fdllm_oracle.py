@@ -367,7 +367,7 @@ def e4m3_round(y):
     e = np.where(np.exp2(e + 1) <= a, e + 1, e)
     step = np.exp2(np.maximum(e, -6.0) - 3.0)
     out = np.where(nz, np.round(a / step) * step, 0.0)      # np.round: half to even, a / step exact
-    return np.sign(y) * out
+    return np.copysign(out, y)                              # the sign of y, also on zero (IEEE 754 6.3)
 
 
 def e4m3_encode(v):

@@ -75,6 +75,19 @@ def test_round_matches_torch_on_float32_inputs():
     assert np.array_equal(O.e4m3_round(y), torch.from_numpy(y).to(torch.float8_e4m3fn).double().numpy())
 
 
+def test_round_codes_match_torch_including_signed_zero():
+    """Byte codes, not values: a negative input that rounds to zero gives -0 (0x80), as IEEE
+    rounding keeps the operand's sign."""
+    rng = np.random.default_rng(8)
+    y = (rng.standard_normal(20000) * np.exp2(rng.integers(-14, 9, 20000))).astype(np.float32)
+    y = np.concatenate([np.clip(y, -448, 448), np.array([-0.0, 0.0, -1e-5, 1e-5, -2.0 ** -10, 2.0 ** -10],
+                                                         dtype=np.float32)]).astype(np.float64)
+    ours = O.e4m3_encode(O.e4m3_round(y))
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    assert ours[-6] == 0x80 and ours[-5] == 0x00 and ours[-4] == 0x80
+
+
 @pytest.mark.parametrize("amax,k", [(448.0, 0), (np.nextafter(448.0, 1e9), 1), (224.0, -1), (224.5, 0),
                                     (1.0, -8), (0.0, 0), (896.0, 1), (897.0, 2), (2.0 ** -20, -28)])
 def test_scale_exponent_hand_values(amax, k):
