@@ -182,6 +182,10 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   // c > tau  <=>  log((1 - c) / c) < log((1 - tau) / tau)
   p.kappa_tau = tau >= 1.0 ? -INFINITY : (tau <= 0.0 ? INFINITY : (float)log((1.0 - tau) / tau));
   p.in_bf16 = d->dtype == FDLLM_BF16;
+  p.fp8w = 0;
+  p.w_scale = nullptr;
+  p.h_scale = nullptr;
+  p.hq = nullptr;
   return FDLLM_OK;
 }
 
@@ -191,6 +195,7 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
 // rest (followed by select_kernel)
 struct SelectLayout {
   size_t part_off, total;
+  size_t hq_off, hs_off;   // FP8 weight cache: the quantised hidden rows and their scales
   int splits;
   bool tc;
 };
@@ -202,12 +207,29 @@ SelectLayout select_layout(const SelectProblem &p) {
   // the tickets, then the partials
   L.part_off = 256;
   L.total = L.part_off + align_up((size_t)p.batch * p.B * L.splits * sizeof(VocabStat), 256);
+  L.hq_off = L.hs_off = 0;
+  if (p.fp8w) {
+    const size_t rows = (size_t)p.batch * p.B;
+    L.hq_off = L.total;
+    L.hs_off = L.hq_off + align_up(rows * p.H, 256);
+    L.total = L.hs_off + align_up(rows * sizeof(float), 256);
+  }
   return L;
 }
 
 // LM head + select on the partials at `ws` (laid out by select_layout)
 cudaError_t run_select(const SelectProblem &p, const SelectLayout &L, void *ws, cudaStream_t st) {
   VocabStat *part = (VocabStat *)((char *)ws + L.part_off);
+  if (p.fp8w) {
+    // the block's hidden rows in E4M3 (per-row scales), then the E4M3 LM head
+    SelectProblem q = p;
+    q.hq = (char *)ws + L.hq_off;
+    q.h_scale = (const float *)((char *)ws + L.hs_off);
+    cudaError_t e = launch_quantize_fp8(p.hidden, true, (int64_t)p.batch * p.B, p.H, (uint8_t *)q.hq,
+                                        (float *)q.h_scale, st);
+    if (e != cudaSuccess) return e;
+    return launch_lmhead_tc(q, part, (unsigned long long *)ws, L.splits, st);
+  }
   if (L.tc) return launch_lmhead_tc(p, part, (unsigned long long *)ws, L.splits, st);
   cudaError_t e = launch_lmhead_simt(p, part, L.splits, st);
   if (e != cudaSuccess) return e;
@@ -221,7 +243,7 @@ using namespace fdllm;
 
 extern "C" {
 
-int32_t fdllm_version(void) { return 101; }
+int32_t fdllm_version(void) { return 102; }
 
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
   if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");
@@ -372,6 +394,57 @@ fdllm_status fdllm_confidence_select_ragged(const fdllm_select_desc *desc, const
   if (!block_start) return fail(FDLLM_EINVAL, "select: block_start is null");
   return confidence_select(desc, block_start, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax,
                            n_masked_left, workspace, ws_bytes, stream);
+}
+
+// ---- FP8 weight cache ----
+fdllm_status fdllm_quantize_fp8_rows(int64_t rows, int32_t cols, int32_t dtype, const void *src, uint8_t *q,
+                                     float *scale, fdllm_stream_t stream) {
+  if (rows < 0 || cols < 0) return fail(FDLLM_EINVAL, "quantize: negative shape");
+  if (dtype != FDLLM_BF16 && dtype != FDLLM_F32) return fail(FDLLM_EINVAL, "quantize: bad dtype %d", dtype);
+  if (rows == 0 || cols == 0) return FDLLM_OK;
+  if (!src || !q || !scale) return fail(FDLLM_EINVAL, "quantize: null pointer");
+  return cuda_status(launch_quantize_fp8(src, dtype == FDLLM_BF16, rows, cols, q, scale, (cudaStream_t)stream),
+                     "quantize launch");
+}
+
+static fdllm_status resolve_select_fp8w(const fdllm_select_desc *desc, SelectProblem &p) {
+  fdllm_status st = resolve_select(desc, p);
+  if (st != FDLLM_OK) return st;
+  p.fp8w = 1;
+  if (!p.in_bf16 || !lmhead_tc_supported(p))
+    return fail(FDLLM_EUNSUPPORTED,
+                "select fp8w: needs bf16 hidden rows, hidden a multiple of 128 and batch * block_size <= 512");
+  return FDLLM_OK;
+}
+
+size_t fdllm_select_fp8w_workspace_size(const fdllm_select_desc *desc) {
+  SelectProblem p;
+  if (resolve_select_fp8w(desc, p) != FDLLM_OK) return 0;
+  return select_layout(p).total;
+}
+
+fdllm_status fdllm_confidence_select_fp8w(const fdllm_select_desc *desc, const void *hidden, const uint8_t *w_q,
+                                          const float *w_scale, int32_t *tokens, uint8_t *unmasked, float *conf,
+                                          float *kappa, int32_t *argmax, int32_t *n_masked_left, void *workspace,
+                                          size_t ws_bytes, fdllm_stream_t stream) {
+  SelectProblem p;
+  fdllm_status st = resolve_select_fp8w(desc, p);
+  if (st != FDLLM_OK) return st;
+  const void *req[] = {hidden, w_q, w_scale, tokens, unmasked, conf, argmax, n_masked_left, workspace};
+  const char *names[] = {"hidden", "w_q", "w_scale", "tokens", "unmasked", "conf", "argmax", "n_masked_left",
+                         "workspace"};
+  for (int i = 0; i < 9; ++i)
+    if (!req[i]) return fail(FDLLM_EINVAL, "select fp8w: %s is null", names[i]);
+  if (!aligned16(hidden) || !aligned16(w_q) || !aligned16(workspace))
+    return fail(FDLLM_EINVAL, "select fp8w: hidden, w_q and workspace must be 16-byte aligned");
+  const SelectLayout L = select_layout(p);
+  if (ws_bytes < L.total)
+    return fail(FDLLM_EINVAL, "select fp8w: workspace of %zu bytes is smaller than the %zu required", ws_bytes,
+                L.total);
+  p.hidden = hidden; p.w = w_q; p.w_scale = w_scale; p.tokens = tokens; p.unmasked = unmasked; p.conf = conf;
+  p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
+  p.err = error_word_ptr();
+  return cuda_status(run_select(p, L, workspace, (cudaStream_t)stream), "fp8 quantize / lm-head / select launch");
 }
 
 fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,

@@ -88,6 +88,47 @@ __device__ __forceinline__ void vs_push(VocabStat &s, float x, int32_t v) {
   }
 }
 
+// Statistics of 32 logits x[e] with ids v0 + e (in increasing order), without data-dependent
+// branches: a pairwise tree of (max, lowest id of the max, second value) over adjacent ranges --
+// the left range holds the lower ids, so it wins ties -- then the 31 other terms' exponentials
+// relative to the second value, summed as a tree.  Entries of -inf (ids past the vocabulary) never
+// win unless all are -inf, which gives the empty statistics.
+__device__ __forceinline__ VocabStat vs_chunk32(const float (&x)[32], int32_t v0) {
+  float m1[16], m2[16];
+  int i1[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const bool ge = x[2 * e] >= x[2 * e + 1];
+    m1[e] = ge ? x[2 * e] : x[2 * e + 1];
+    m2[e] = ge ? x[2 * e + 1] : x[2 * e];
+    i1[e] = ge ? 2 * e : 2 * e + 1;
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int e = 0; e < w; ++e) {   // node e <- nodes 2e (lower ids) and 2e + 1
+      const bool ge = m1[2 * e] >= m1[2 * e + 1];
+      const float a2 = fmaxf(m2[2 * e], m1[2 * e + 1]), b2 = fmaxf(m2[2 * e + 1], m1[2 * e]);
+      m1[e] = ge ? m1[2 * e] : m1[2 * e + 1];
+      i1[e] = ge ? i1[2 * e] : i1[2 * e + 1];
+      m2[e] = ge ? a2 : b2;
+    }
+  }
+  VocabStat c;
+  c.m1 = m1[0];
+  c.a1 = c.m1 == kNegInf ? 0x7fffffff : v0 + i1[0];
+  c.m2 = m2[0];
+  float t[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) t[e] = e == i1[0] ? 0.f : __expf(x[e] - c.m2);
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int e = 0; e < w; ++e) t[e] += t[e + w];
+  c.s2 = c.m2 == kNegInf ? 0.f : t[0];
+  return c;
+}
+
 __device__ __forceinline__ VocabStat vs_shfl_xor(const VocabStat &s, int mask) {
   VocabStat o;
   o.m1 = __shfl_xor_sync(0xffffffffu, s.m1, mask);

@@ -38,6 +38,11 @@ struct SelectProblem {
   float factor;
   int in_bf16;
   const void *hidden, *w;
+  // FP8 weight cache (fp8w = 1): w holds E4M3 codes [V, H] with w_scale [V]; the hidden rows are
+  // quantised per row into hq [b * B, H] (E4M3) with h_scale [b * B] before the LM head
+  int fp8w;
+  const float *w_scale, *h_scale;
+  const void *hq;
   int32_t *tokens;
   uint8_t *unmasked;
   float *conf, *kappa;
@@ -80,6 +85,11 @@ bool lmhead_tc_supported(const SelectProblem &p);
 int lmhead_tc_grid(const SelectProblem &p);
 cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int splits,
                              cudaStream_t st);
+
+// fp8.cu: per-row E4M3 quantisation q [rows, cols], scale [rows] of a bf16 / fp32 matrix (the
+// rounding and scale rule of the FP8 weight cache); programmatic-dependent launch
+cudaError_t launch_quantize_fp8(const void *src, bool src_bf16, int64_t rows, int cols, uint8_t *q, float *scale,
+                                cudaStream_t st);
 
 // select.cu: merge partials [b * B, splits] over splits and unmask
 cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st);

@@ -47,17 +47,24 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kUnit = 64;        // vocabulary rows per W box
-constexpr int kKChunk = 64;      // K elements per stage (one 128-byte swizzle atom)
+constexpr int kRowBytes = 128;   // bytes of an operand row per stage (one 128-byte swizzle atom)
+// The tensor maps describe both operands as rows of kMapElemBytes-byte integers: TMA only copies
+// bytes, and the 128-byte swizzle is defined on bytes, so the shared-memory tiles are the same for
+// any width.  x coordinates are in these units.
+constexpr int kMapElemBytes = 2;
+constexpr int kMapX = kRowBytes / kMapElemBytes;   // map units per stage along a row
+template <bool F8>
+constexpr int kChunk = F8 ? 128 : 64;   // K elements per stage: E4M3 or bf16
 constexpr int kABox = 128;       // block rows per hidden-tile box
 constexpr int kMaxSelectors = 8; // CTAs that run the merge + select at the end
 constexpr int kPrefetchers = 24; // first CTAs to start that warm L2 with the head of every CTA's W range
-constexpr int kPrefetchChunks = 12;   // K chunks (128 bytes of a W row each) warmed per row of a first tile
+constexpr int kPrefetchBytes = 1536;  // bytes of each W row of a first tile warmed in L2
 
 struct Cfg {
   static constexpr int NV = 256;                            // vocabulary rows per tile
   static constexpr int UNITS = NV / kUnit;                  // W boxes per tile
-  static constexpr int A_BYTES = kABox * kKChunk * 2;       // this CTA's hidden tile per stage
-  static constexpr int W_BYTES = NV * kKChunk * 2;          // W tile per stage
+  static constexpr int A_BYTES = kABox * kRowBytes;        // this CTA's hidden tile per stage
+  static constexpr int W_BYTES = NV * kRowBytes;           // W tile per stage
   static constexpr int STAGE = A_BYTES + W_BYTES;
   static constexpr int STAGES = 4;
   static constexpr int TMEM_COLS = 512;                     // two accumulators of 256 columns
@@ -119,11 +126,14 @@ __device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site) {
   atomicExch(&sh.abort, 1);
 }
 
-template <int CS>
+// F8: E4M3 operands (the hidden rows quantised per row in the workspace, the FP8 weight cache) with
+// per-row power-of-two scales h_scale [b * B] and w_scale [V]: logit = acc * h_scale * w_scale.
+template <int CS, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                      const SelectProblem sp, VocabStat *__restrict__ part, unsigned long long *ticket,
-                     uint32_t epoch) {
+                     uint32_t epoch, const float *__restrict__ h_scale, const float *__restrict__ w_scale) {
+  constexpr int KC = kChunk<F8>;                           // K elements per stage
   const int32_t *__restrict__ tokens = sp.tokens;
   const int batch = sp.batch, seq_len = sp.seq_len, B = sp.B, mask_id = sp.mask_id, H = sp.H, V = sp.V;
   int32_t *err = sp.err;
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int units = (V + kUnit - 1) / kUnit;
   const int u0 = (int)((int64_t)units * k / ncl), u1 = (int)((int64_t)units * (k + 1) / ncl);
   const int ntiles = (u1 - u0 + C::UNITS - 1) / C::UNITS;
-  const int kchunks = H / kKChunk;
+  const int kchunks = H / KC;
 
   if (threadIdx.x == 0) {
     sh.abort = 0; sh.issued = 0; sh.consumed = 0; sh.active = 0;
@@ -169,14 +179,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) e = arrive_ticket(ticket + 1, epoch);
     e = __shfl_sync(0xffffffffu, e, 0);
     if (e >= 1 && e <= kPrefetchers) {
-      // one W box (64 rows x 64 K) per prefetch: the boxes of the first kPrefetchChunks K chunks of
-      // the first tile of CTA ranges e - 1, e - 1 + kPrefetchers, ...
-      const int nchunk = min(kPrefetchChunks, kchunks);
+      // one W box (64 rows x 128 bytes) per prefetch: the boxes of the first kPrefetchBytes of each
+      // row of the first tile of CTA ranges e - 1, e - 1 + kPrefetchers, ...
+      const int nchunk = min(kPrefetchBytes / kRowBytes, kchunks);
       for (int j = e - 1; j < G; j += kPrefetchers) {
         const int ju0 = (int)((int64_t)units * j / ncl), ju1 = (int)((int64_t)units * (j + 1) / ncl);
         const int nu = min(C::UNITS, ju1 - ju0);
         for (int q = lane; q < nu * nchunk; q += 32)
-          tc::prefetch_l2_tile_2d(&map_w, (q / nu) * kKChunk, (ju0 + q % nu) * kUnit);
+          tc::prefetch_l2_tile_2d(&map_w, (q / nu) * kMapX, (ju0 + q % nu) * kUnit);
       }
     }
   }
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < ntiles && !sh.abort; ++t) {
           const int tu0 = u0 + t * C::UNITS;
           const int nu = min(C::UNITS, u1 - tu0);
-          const uint32_t bytes = (uint32_t)(kABox * kKChunk * 2 + nu * kUnit * kKChunk * 2);
+          const uint32_t bytes = (uint32_t)(kABox * kRowBytes + nu * kUnit * kRowBytes);
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int st = it % C::STAGES;
             const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
@@ -228,13 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char *a = tiles + st * C::STAGE;
             unsigned char *w = a + C::A_BYTES;
             tc::mbar_arrive_expect_tx(&sh.full[st], bytes);
-            tc::tma_load_2d(a, &map_h, &sh.full[st], kc * kKChunk, c * kABox, pol_h);
+            tc::tma_load_2d(a, &map_h, &sh.full[st], kc * kMapX, c * kABox, pol_h);
             for (int u = c; u < nu; u += CS) {
               if (CS == 1)
-                tc::tma_load_2d(w + u * kUnit * kKChunk * 2, &map_w, &sh.full[st], kc * kKChunk, (tu0 + u) * kUnit,
+                tc::tma_load_2d(w + u * kUnit * kRowBytes, &map_w, &sh.full[st], kc * kMapX, (tu0 + u) * kUnit,
                                 pol_w);
               else
-                tc::tma_load_2d_multicast(w + u * kUnit * kKChunk * 2, &map_w, &sh.full[st], kc * kKChunk,
+                tc::tma_load_2d_multicast(w + u * kUnit * kRowBytes, &map_w, &sh.full[st], kc * kMapX,
                                           (tu0 + u) * kUnit, kAll, pol_w);
             }
             atomicExch(&sh.issued, it + 1);
@@ -257,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < ntiles && !sh.abort; ++t) {
           const int tu0 = u0 + t * C::UNITS;
           const int nu = min(C::UNITS, u1 - tu0);
-          const uint32_t idesc = tc::idesc_bf16_f32(128, (uint32_t)(nu * kUnit));
+          const uint32_t idesc =
+              F8 ? tc::idesc_e4m3_f32(128, (uint32_t)(nu * kUnit)) : tc::idesc_bf16_f32(128, (uint32_t)(nu * kUnit));
           const int j = t & 1;
           if (!tc::mbar_wait(&sh.acce[j], ((uint32_t)(t >> 1) & 1u) ^ 1u)) { set_abort(sh, err, 102); break; }
           tc::fence_after_sync();
@@ -271,8 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t w = a + C::A_BYTES;
             const uint32_t d = tmem + (uint32_t)(j * C::NV);
 #pragma unroll
-            for (int kk = 0; kk < kKChunk / 16; ++kk)
-              tc::mma_bf16(d, tc::sw128_desc(a + kk * 32), tc::sw128_desc(w + kk * 32), idesc, (kc | kk) != 0);
+            for (int kk = 0; kk < kRowBytes / 32; ++kk) {    // 32 bytes of K per instruction
+              if constexpr (F8)
+                tc::mma_e4m3(d, tc::sw128_desc(a + kk * 32), tc::sw128_desc(w + kk * 32), idesc, (kc | kk) != 0);
+              else
+                tc::mma_bf16(d, tc::sw128_desc(a + kk * 32), tc::sw128_desc(w + kk * 32), idesc, (kc | kk) != 0);
+            }
             if (CS == 1) tc::mma_commit(&sh.empty[st]);
             else tc::mma_commit_multicast(&sh.empty[st], kAll);
             atomicExch(&sh.consumed, it + 1);
@@ -291,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = ((active >> c) & 1) && sh.masked[row] != 0;
       const bool any = __ballot_sync(0xffffffffu, valid) != 0u;
       VocabStat st = vs_identity();
+      const float hs = F8 && row < rows ? h_scale[row] : 1.f;   // this row's scale
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
         const int tu0 = u0 + t * C::UNITS;
@@ -300,18 +316,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc::mbar_wait(&sh.accf[j], (uint32_t)(t >> 1) & 1u)) { set_abort(sh, err, 105); ok = false; break; }
         tc::fence_after_sync();
         if (any) {
+          // 32 columns at a time, reduced without branches and merged into the row's statistics (every
+          // lane computes; rows without a masked position are simply not stored)
           const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * C::NV);
           for (int c0 = 0; c0 < ncol; c0 += 32) {
             uint32_t r[32];
             tc::tmem_ld_32x32b_x32(base + (uint32_t)c0, r);
+            // F8: lane e holds the scale of column v0 + c0 + e (both scales are powers of two, so the
+            // scaled logit is exact)
+            const float wsl = F8 && v0 + c0 + lane < V ? __ldg(w_scale + v0 + c0 + lane) : 0.f;
             tc::tmem_ld_wait();
-            if (valid) {
+            float x[32];
 #pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int v = v0 + c0 + e;
-                if (v < V) vs_push(st, __uint_as_float(r[e]), v);
-              }
+            for (int e = 0; e < 32; ++e) {
+              const float a = F8 ? __uint_as_float(r[e]) * hs * __shfl_sync(0xffffffffu, wsl, e) : __uint_as_float(r[e]);
+              x[e] = v0 + c0 + e < V ? a : kNegInf;
             }
+            st = vs_merge(st, vs_chunk32(x, v0 + c0));
           }
         }
         tc::fence_before_sync();
@@ -372,27 +393,33 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] as a 2-D map with box [box_cols, box_rows], 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Row-major matrix [rows, cols] of bf16 (or, with f8, E4M3 bytes) as a 2-D map of kMapElemBytes-byte
+// units with box [128 bytes of a row, box_rows], 128-byte swizzle.  Row bytes are a multiple of 128.
+bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows, bool f8) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kKChunk, box_rows};
+  const uint64_t row_bytes = cols * (f8 ? 1 : 2);
+  const cuuint64_t dims[2] = {row_bytes / kMapElemBytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)kMapX, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+  const CUtensorMapDataType unit = kMapElemBytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : kMapElemBytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                   : kMapElemBytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                                        : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+  return fn(map, unit, 2, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int CS>
+template <int CS, bool F8>
 cudaError_t launch_cs(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, uint32_t epoch,
                       int splits, cudaStream_t st) {
   CUtensorMap mh, mw;
-  if (!make_map(&mh, p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H, kABox) ||
-      !make_map(&mw, p.w, (uint64_t)p.V, (uint64_t)p.H, kUnit))
+  if (!make_map(&mh, F8 ? p.hq : p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H, kABox, F8) ||
+      !make_map(&mw, p.w, (uint64_t)p.V, (uint64_t)p.H, kUnit, F8))
     return cudaErrorInvalidValue;
-  auto kfn = lmhead_tc_kernel<CS>;
+  auto kfn = lmhead_tc_kernel<CS, F8>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
   if (e != cudaSuccess) return e;
   // an ordinary launch: the tail's waiting CTAs never hold an SM that an unscheduled CTA needs
@@ -410,7 +437,8 @@ cudaError_t launch_cs(const SelectProblem &p, VocabStat *part, unsigned long lon
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CS > 1 ? 2 : 1;
-  e = cudaLaunchKernelEx(&cfg, kfn, mh, mw, p, part, ticket, epoch);
+  e = cudaLaunchKernelEx(&cfg, kfn, mh, mw, p, part, ticket, epoch, F8 ? p.h_scale : (const float *)nullptr,
+                         F8 ? p.w_scale : (const float *)nullptr);
   count_launches(1);
   return e;
 }
@@ -429,7 +457,7 @@ int max_active_clusters() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev] > 0) return cache[dev];
-  auto kfn = lmhead_tc_kernel<CS>;
+  auto kfn = lmhead_tc_kernel<CS, false>;   // the E4M3 form has the same resources
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sm_count() / CS * CS));
@@ -454,7 +482,8 @@ int max_active_clusters() {
 }  // namespace
 
 bool lmhead_tc_supported(const SelectProblem &p) {
-  return p.in_bf16 && (int64_t)p.batch * p.B <= 512 && p.H % kKChunk == 0;
+  return p.in_bf16 && (int64_t)p.batch * p.B <= 512 && p.H % kChunk<false> == 0 &&
+         (!p.fp8w || p.H % kChunk<true> == 0);
 }
 
 int lmhead_tc_grid(const SelectProblem &p) {
@@ -477,10 +506,17 @@ cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned l
                                       ((uint32_t)getpid() << 16)};
   uint32_t e = epochs.fetch_add(1) + 1;
   while (e == 0 || e == 0xFFFFFFFFu) e = epochs.fetch_add(1) + 1;  // never the all-zero / all-one patterns
+  if (p.fp8w) {
+    switch (cluster_size(p)) {
+      case 1: return launch_cs<1, true>(p, part, ticket, e, splits, st);
+      case 2: return launch_cs<2, true>(p, part, ticket, e, splits, st);
+      default: return launch_cs<4, true>(p, part, ticket, e, splits, st);
+    }
+  }
   switch (cluster_size(p)) {
-    case 1: return launch_cs<1>(p, part, ticket, e, splits, st);
-    case 2: return launch_cs<2>(p, part, ticket, e, splits, st);
-    default: return launch_cs<4>(p, part, ticket, e, splits, st);
+    case 1: return launch_cs<1, false>(p, part, ticket, e, splits, st);
+    case 2: return launch_cs<2, false>(p, part, ticket, e, splits, st);
+    default: return launch_cs<4, false>(p, part, ticket, e, splits, st);
   }
 }
 

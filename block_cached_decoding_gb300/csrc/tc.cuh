@@ -190,6 +190,18 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T with E4M3 operands (kind::f8f6f4, K = 32 per instruction: 32
+// bytes of each operand row, the same smem stride per step as the bf16 form).
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every previously issued tcgen05.mma of this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -214,6 +226,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n, ui
          | (1u << 7)            // A format: bf16
          | (1u << 10)           // B format: bf16
          | (b_mn_major << 16)   // B major-ness
+         | ((n >> 3) << 17)     // N >> 3
+         | ((m >> 4) << 24);    // M >> 4
+}
+
+// Instruction descriptor for kind::f8f6f4: D f32, A and B E4M3 (format code 0), both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
+  return (1u << 4)              // D format: f32
+         | (0u << 7)            // A format: E4M3
+         | (0u << 10)           // B format: E4M3
          | ((n >> 3) << 17)     // N >> 3
          | ((m >> 4) << 24);    // M >> 4
 }

@@ -26,7 +26,8 @@ EXPORTS = (
     "fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
     "fdllm_synth_prompt", "fdllm_launch_counter", "fdllm_confidence_select_noalloc",
     "fdllm_selftest_bounded_wait", "fdllm_block_attn_ragged", "fdllm_confidence_select_ragged",
-    "fdllm_kv_splice_ragged",
+    "fdllm_kv_splice_ragged", "fdllm_quantize_fp8_rows", "fdllm_select_fp8w_workspace_size",
+    "fdllm_confidence_select_fp8w",
 )
 
 NOALLOC_SCRATCH_BYTES = 2 << 20
@@ -85,6 +86,12 @@ def lib() -> C.CDLL:
         L.fdllm_confidence_select_ragged.restype = i32
         L.fdllm_kv_splice_ragged.argtypes = [i32] * 4 + [vp, i32, i32] + [vp] * 5
         L.fdllm_kv_splice_ragged.restype = i32
+        L.fdllm_quantize_fp8_rows.argtypes = [i64, i32, i32, vp, vp, vp, vp]
+        L.fdllm_quantize_fp8_rows.restype = i32
+        L.fdllm_select_fp8w_workspace_size.argtypes = [C.POINTER(SelectDesc)]
+        L.fdllm_select_fp8w_workspace_size.restype = sz
+        L.fdllm_confidence_select_fp8w.argtypes = [C.POINTER(SelectDesc)] + [vp] * 10 + [sz, vp]
+        L.fdllm_confidence_select_fp8w.restype = i32
         L.fdllm_status_string.argtypes = [i32]
         L.fdllm_status_string.restype = C.c_char_p
         L.fdllm_last_error.argtypes = []
@@ -173,6 +180,25 @@ def fdllm_block_attn(desc, q, k_cache, v_cache, k_fresh, v_fresh, out, lse=None,
 
 def fdllm_select_workspace_size(desc: SelectDesc) -> int:
     return lib().fdllm_select_workspace_size(C.byref(desc))
+
+
+def fdllm_select_fp8w_workspace_size(desc: SelectDesc) -> int:
+    return lib().fdllm_select_fp8w_workspace_size(C.byref(desc))
+
+
+def fdllm_quantize_fp8_rows(rows, cols, dtype, src, q, scale, stream=None):
+    """Per-row E4M3 codes q [rows, cols] (uint8) and power-of-two scales [rows] (fp32) of src."""
+    _check(lib().fdllm_quantize_fp8_rows(rows, cols, dtype, _ptr(src), _ptr(q), _ptr(scale), _stream(stream)))
+
+
+def fdllm_confidence_select_fp8w(desc, hidden, w_q, w_scale, tokens, unmasked, conf, kappa, argmax, n_masked_left,
+                                 workspace, ws_bytes=None, stream=None):
+    """fdllm_confidence_select with the LM-head weight from the FP8 cache (w_q codes, w_scale per row)."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_confidence_select_fp8w(C.byref(desc), _ptr(hidden), _ptr(w_q), _ptr(w_scale), _ptr(tokens),
+                                              _ptr(unmasked), _ptr(conf), _ptr(kappa), _ptr(argmax),
+                                              _ptr(n_masked_left), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fdllm_confidence_select(desc, hidden, lm_head_w, tokens, unmasked, conf, kappa, argmax, n_masked_left,

@@ -1,6 +1,7 @@
 """Run one hot-path call on a chosen shape a few times (the command ncu profiles).
 
     python -m block_cached_decoding_gb300.profile_case select --vocab 32768 --reps 3
+    python -m block_cached_decoding_gb300.profile_case select --fp8w --reps 3
     python -m block_cached_decoding_gb300.profile_case attn --mode prefix --reps 3
     python -m block_cached_decoding_gb300.profile_case splice --reps 3
 
@@ -32,6 +33,7 @@ def main():
     ap.add_argument("--d", type=int, default=128)
     ap.add_argument("--mode", default="prefix", choices=["dual", "prefix", "none"])
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--fp8w", action="store_true", help="select through the FP8 weight cache")
     ap.add_argument("--time", action="store_true", help="report the mean call time over the reps (CUDA events)")
     a = ap.parse_args()
     wl = configs.LLADA_STEP
@@ -48,12 +50,22 @@ def main():
         tokens = tokens0.clone()
         d = F.select_desc(batch=b, seq_len=n, block_start=s, block_size=B, hidden=a.hidden, vocab=a.vocab,
                           mask_id=a.vocab, threshold=0.9, dtype=code)
-        ws = torch.empty(F.fdllm_select_workspace_size(d), dtype=torch.uint8, device=dev)
         outs = [torch.empty(b, B, dtype=t, device=dev) for t in (torch.uint8, torch.float32, torch.float32, torch.int32)]
         nleft = torch.empty(b, dtype=torch.int32, device=dev)
-        def call():
-            tokens.copy_(tokens0)
-            F.fdllm_confidence_select(d, hid, W, tokens, *outs, nleft, ws)
+        if a.fp8w:
+            wq = torch.empty(a.vocab, a.hidden, dtype=torch.uint8, device=dev)
+            wsc = torch.empty(a.vocab, dtype=torch.float32, device=dev)
+            F.fdllm_quantize_fp8_rows(a.vocab, a.hidden, code, W, wq, wsc)
+            del W
+            ws = torch.empty(F.fdllm_select_fp8w_workspace_size(d), dtype=torch.uint8, device=dev)
+            def call():
+                tokens.copy_(tokens0)
+                F.fdllm_confidence_select_fp8w(d, hid, wq, wsc, tokens, *outs, nleft, ws)
+        else:
+            ws = torch.empty(F.fdllm_select_workspace_size(d), dtype=torch.uint8, device=dev)
+            def call():
+                tokens.copy_(tokens0)
+                F.fdllm_confidence_select(d, hid, W, tokens, *outs, nleft, ws)
     elif a.op == "attn":
         d = F.attn_desc(batch=b, prompt_len=a.prompt, gen_length=a.gen, block_size=B, block_idx=a.block_idx,
                         n_q_heads=a.hq, n_kv_heads=a.hkv, head_dim=a.d, use_cache=0 if a.mode == "none" else 1,

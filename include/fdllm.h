@@ -279,6 +279,44 @@ fdllm_status fdllm_kv_splice_ragged(int32_t batch, int32_t seq_len, int32_t n_kv
                                     void *v_cache, const void *k_src, const void *v_src, fdllm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* FP8 weight cache                                                          */
+/* ------------------------------------------------------------------------ */
+/* The summary proposes FP8 or INT8 storage for cached activations as future
+ * work (section 6, the memory-overhead limitation; section 7, future direction
+ * 3 "KV cache quantization and memory-efficient DualCache") without a scheme.
+ * Here the LM-head weight, the largest per-step read of the path, is stored in
+ * FP8: E4M3 codes (OCP FP8: bias 7, 3 mantissa bits, subnormals, largest finite
+ * value 448) with one power-of-two scale per row.  Row r's scale is 2^k, k the
+ * smallest integer with max|row| <= 448 * 2^k (k = 0 for an all-zero row), and
+ * its codes are x / 2^k rounded to the nearest E4M3 value, ties to even.  Inputs
+ * must be finite. */
+
+/* q[r, :] (uint8 E4M3 codes, device [rows, cols]) and scale[r] (device float
+ * [rows]) for each row of src (device [rows, cols], `dtype`).  Asynchronous on
+ * `stream`; returns FDLLM_EINVAL for a negative shape, a bad dtype or a null
+ * pointer (nothing to do for rows = 0 or cols = 0). */
+fdllm_status fdllm_quantize_fp8_rows(int64_t rows, int32_t cols, int32_t dtype, const void *src, uint8_t *q,
+                                     float *scale, fdllm_stream_t stream);
+
+/* Workspace bytes of fdllm_confidence_select_fp8w (the select workspace plus
+ * the block's hidden rows in E4M3 and their scales); 0 on an invalid or
+ * unsupported descriptor. */
+size_t fdllm_select_fp8w_workspace_size(const fdllm_select_desc *desc);
+
+/* fdllm_confidence_select with the LM-head weight from the FP8 cache: w_q
+ * (device uint8 [V, H]) and w_scale (device float [V]) as written by
+ * fdllm_quantize_fp8_rows.  The block's hidden rows (bf16, desc->dtype =
+ * FDLLM_BF16) are quantised the same way, per row, into the workspace, and
+ * logit l_v = h_scale * w_scale[v] * sum_k qh_k qw_vk (fp32 accumulation); the
+ * reduction, selection and outputs are those of fdllm_confidence_select.
+ * FDLLM_EUNSUPPORTED unless hidden is a multiple of 128 and batch * block_size
+ * <= 512.  Two kernels per call. */
+fdllm_status fdllm_confidence_select_fp8w(const fdllm_select_desc *desc, const void *hidden, const uint8_t *w_q,
+                                          const float *w_scale, int32_t *tokens, uint8_t *unmasked, float *conf,
+                                          float *kappa, int32_t *argmax, int32_t *n_masked_left, void *workspace,
+                                          size_t ws_bytes, fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
 
@@ -303,7 +341,8 @@ fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
  * usable.  Returns FDLLM_EINVAL for a limit outside 1..1000. */
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream);
 
-/* ABI version: 100 * major + minor (101: the per-sequence block calls). */
+/* ABI version: 100 * major + minor (101: the per-sequence block calls; 102: the
+ * FP8 weight cache). */
 int32_t fdllm_version(void);
 
 /* Number of kernels this library has launched in the process so far (all

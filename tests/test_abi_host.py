@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert F.fdllm_version() == 101
+    assert F.fdllm_version() == 102
     for s in range(5):
         assert lib.fdllm_status_string(s).decode().startswith("FDLLM_")
 
@@ -135,3 +135,22 @@ def test_per_sequence_block_calls_validate_on_the_host(lib):
                                               None) == F.EINVAL
     assert lib.fdllm_kv_splice_ragged(2, 64, 4, 64, None, 16, F.BF16, v, v, v, v, None) == F.EINVAL
     assert lib.fdllm_kv_splice_ragged(2, 64, 4, 64, v, 65, F.BF16, v, v, v, v, None) == F.EINVAL
+
+
+def test_fp8_calls_validate_on_the_host(lib):
+    """The FP8 weight-cache calls reject unsupported descriptors and null pointers before any launch."""
+    v = C.c_void_p(16)
+    ok = F.select_desc(batch=1, seq_len=64, block_start=0, block_size=16, hidden=256, vocab=100, mask_id=100)
+    for bad in (dict(hidden=192), dict(dtype=F.F32), dict(batch=40, block_size=16)):
+        kw = dict(batch=1, seq_len=700, block_start=0, block_size=16, hidden=256, vocab=100, mask_id=100)
+        kw.update(bad)
+        d = F.select_desc(**kw)
+        assert F.fdllm_select_fp8w_workspace_size(d) == 0
+        assert lib.fdllm_confidence_select_fp8w(C.byref(d), v, v, v, v, v, v, v, v, v, v, 1 << 30,
+                                                None) == F.EUNSUPPORTED
+    assert lib.fdllm_confidence_select_fp8w(C.byref(ok), v, v, None, v, v, v, v, v, v, v, 1 << 30,
+                                            None) == F.EINVAL
+    assert lib.fdllm_quantize_fp8_rows(4, 64, 7, v, v, v, None) == F.EINVAL
+    assert lib.fdllm_quantize_fp8_rows(-1, 64, F.BF16, v, v, v, None) == F.EINVAL
+    assert lib.fdllm_quantize_fp8_rows(4, 64, F.BF16, None, v, v, None) == F.EINVAL
+    assert lib.fdllm_quantize_fp8_rows(0, 64, F.BF16, None, None, None, None) == F.OK

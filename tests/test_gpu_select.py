@@ -170,3 +170,55 @@ def test_workspace_needs_no_initialisation_and_can_be_shared():
                 for key in ("unmask", "token", "n_left", "tokens"):
                     assert np.array_equal(got[key], fresh[key]), (fill, key, b, B, H, V)
                 assert np.allclose(got["conf"], fresh["conf"], equal_nan=True, rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("path", ["bf16", "f32", "fp8"])
+def test_exact_ties_take_the_lowest_id(path):
+    """Copies of the winning W row at other ids (same 32-column chunk, the next chunk, another
+    CTA's vocabulary range, and a lower id for half the rows) give bitwise-equal logits: the token
+    must be the lowest id among them (reading R3) on every path, and the confidence counts every
+    copy."""
+    dtype = "f32" if path == "f32" else "bf16"
+    V, H, B = 6000, 256, 8
+    sigma = float(np.sqrt(0.02))
+    rng = np.random.default_rng(17)
+    w = synth.lm_head_weight(21, V, H, sigma, dtype).copy()
+    targets = [100 + 650 * i for i in range(B)]            # far apart: the copies never overlap
+    lowest = []
+    for i, t in enumerate(targets):
+        ids = [t + 1, t + 37, t + 420]
+        if i % 2:
+            ids.append(t - 61)
+        for c in ids:
+            w[c] = w[t]
+        lowest.append(min([t] + ids))
+    wf = synth.as_f32(w, dtype)
+    z = rng.standard_normal((1, B, H)).astype(np.float32)
+    h = (z + 6.0 * wf[targets][None]).astype(np.float32)
+    hid = h if dtype == "f32" else synth.f32_to_bf16_bits(h)
+    n, s = 64, 32
+    tokens = np.full((1, n), V, dtype=np.int64)
+    tokens[:, :s] = 3
+    desc = F.select_desc(batch=1, seq_len=n, block_start=s, block_size=B, hidden=H, vocab=V, mask_id=V,
+                         threshold=0.9, dtype=code(dtype))
+    t_dev = torch.from_numpy(tokens.astype(np.int32)).cuda()
+    outs = SelectOutputs(desc, 1, B)
+    if path == "fp8":
+        q = torch.empty(V, H, dtype=torch.uint8, device="cuda")
+        sc = torch.empty(V, dtype=torch.float32, device="cuda")
+        F.fdllm_quantize_fp8_rows(V, H, F.BF16, dev(w, dtype), q, sc)
+        outs.ws = torch.empty(F.fdllm_select_fp8w_workspace_size(desc), dtype=torch.uint8, device="cuda")
+        F.fdllm_confidence_select_fp8w(desc, dev(hid, dtype), q, sc, t_dev, outs.unmasked, outs.conf, outs.kappa,
+                                       outs.argmax, outs.n_left, outs.ws)
+        wc, ws_ = O.quantize_fp8_rows(f64(w, dtype))
+        hq, hs = O.quantize_fp8_rows(f64(hid, dtype)[0])
+        h64, w64 = O.dequantize_fp8_rows(hq, hs)[None], O.dequantize_fp8_rows(wc, ws_)
+    else:
+        outs.run(desc, dev(hid, dtype), dev(w, dtype), t_dev)
+        h64, w64 = f64(hid, dtype), f64(w, dtype)
+    got = outs.host()
+    _, info = O.decode_step(tokens, h64, w64, s=s, block_size=B, mask_id=V, tau=0.9)
+    assert list(info["token"][0]) == lowest
+    assert list(got["token"][0]) == lowest
+    assert np.allclose(got["conf"][0], info["conf"][0], atol=1e-3)
+    assert np.all(info["conf"][0] <= 1.0 / 4 + 1e-9)        # at least four equal maxima per row
