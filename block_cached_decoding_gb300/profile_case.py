@@ -34,6 +34,8 @@ def main():
     ap.add_argument("--mode", default="prefix", choices=["dual", "prefix", "none"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fp8w", action="store_true", help="select through the FP8 weight cache")
+    ap.add_argument("--ragged", action="store_true",
+                    help="per-sequence blocks: sequence i at block i mod (gen / block) (DualCache attention, select)")
     ap.add_argument("--time", action="store_true", help="report the mean call time over the reps (CUDA events)")
     a = ap.parse_args()
     wl = configs.LLADA_STEP
@@ -52,7 +54,13 @@ def main():
                           mask_id=a.vocab, threshold=0.9, dtype=code)
         outs = [torch.empty(b, B, dtype=t, device=dev) for t in (torch.uint8, torch.float32, torch.float32, torch.int32)]
         nleft = torch.empty(b, dtype=torch.int32, device=dev)
-        if a.fp8w:
+        starts = torch.tensor([a.prompt + (i % (a.gen // B)) * B for i in range(b)], dtype=torch.int32, device=dev)
+        if a.ragged:
+            ws = torch.empty(F.fdllm_select_workspace_size(d), dtype=torch.uint8, device=dev)
+            def call():
+                tokens.copy_(tokens0)
+                F.fdllm_confidence_select_ragged(d, starts, hid, W, tokens, *outs, nleft, ws)
+        elif a.fp8w:
             wq = torch.empty(a.vocab, a.hidden, dtype=torch.uint8, device=dev)
             wsc = torch.empty(a.vocab, dtype=torch.float32, device=dev)
             F.fdllm_quantize_fp8_rows(a.vocab, a.hidden, code, W, wq, wsc)
@@ -85,8 +93,12 @@ def main():
         out = torch.empty(b, nq, a.hq, a.d, dtype=torch.bfloat16, device=dev)
         wsb = F.fdllm_attn_workspace_size(d)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        blocks = torch.tensor([i % (a.gen // B) for i in range(b)], dtype=torch.int32, device=dev)
         def call():
-            F.fdllm_block_attn(d, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)
+            if a.ragged:
+                F.fdllm_block_attn_ragged(d, blocks, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)
+            else:
+                F.fdllm_block_attn(d, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)
     else:
         kc = torch.zeros(b, n, a.hkv, a.d, dtype=torch.bfloat16, device=dev)
         vc = torch.zeros_like(kc)
