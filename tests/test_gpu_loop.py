@@ -20,9 +20,10 @@ def _lib():
     ensure_built()
 
 
-def lockstep(wl, tau, strategy="threshold", refresh_interval=None):
-    dec = BlockDecoder(wl, tau=tau, strategy={"threshold": F.SELECT_THRESHOLD, "factor": F.SELECT_FACTOR}[strategy],
-                       refresh_interval=refresh_interval)
+def lockstep(wl, tau, strategy="threshold", refresh_interval=None, topk=1):
+    dec = BlockDecoder(wl, tau=tau, strategy={"threshold": F.SELECT_THRESHOLD, "factor": F.SELECT_FACTOR,
+                                              "topk": F.SELECT_TOPK}[strategy],
+                       refresh_interval=refresh_interval, topk=topk)
     w64 = f64(synth.lm_head_weight(wl.seed, wl.vocab, wl.hidden, wl.sigma_w, wl.dtype), wl.dtype)
     state = {"exempt": 0, "steps": 0, "unmasked": 0}
     caches = {}
@@ -53,7 +54,7 @@ def lockstep(wl, tau, strategy="threshold", refresh_interval=None):
         hid, _, _ = synth.hidden_states(wl.seed, b, g, range(s, s + wl.block_size), wl.hidden, wl.vocab, wl.sigma_w,
                                         wl.dtype, wl.p_plant)
         _, info = O.decode_step(t_before, f64(hid, wl.dtype), w64, s=s, block_size=wl.block_size, mask_id=wl.mask_id,
-                                tau=tau, strategy=strategy)
+                                tau=tau, strategy=strategy, topk=topk)
         got = {"unmask": um, "conf": r.conf.cpu().numpy(), "kappa": r.kappa.cpu().numpy(),
                "token": r.argmax.cpu().numpy()}
         state["exempt"] += compare_select(info, got, tau, strategy)
@@ -104,3 +105,14 @@ def test_refresh_every_two_steps():
 def test_factor_strategy_loop():
     wl = configs.TINY.with_(gen_length=32)
     lockstep(wl, 0.9, strategy="factor")
+
+
+@pytest.mark.parametrize("steps_per_block", [4, 2])
+def test_fixed_count_schedule(steps_per_block):
+    """LLaDA's baseline schedule with T < B steps per block: a fixed B / T tokens per step (top-k),
+    so every block takes exactly T steps and every step unmasks exactly B / T positions."""
+    wl = configs.TINY.with_(gen_length=32)
+    k = wl.block_size // steps_per_block
+    state, steps = lockstep(wl, 0.9, strategy="topk", topk=k)
+    assert steps == [steps_per_block] * (wl.gen_length // wl.block_size)
+    assert state["unmasked"] == k * state["steps"]

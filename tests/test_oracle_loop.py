@@ -70,3 +70,28 @@ def test_std_reading_gives_all_fallback_steps():
     tokens, rec = O.generate(prompt, gen_length=32, block_size=wl.block_size, mask_id=wl.mask_id,
                              tau=0.9, w=w64, hidden_fn=hidden_fn)
     assert all(r["n_unmasked"] == 1 for r in rec) and len(rec) == 32
+
+
+@pytest.mark.parametrize("T", [1, 2, 4, 16])
+def test_fixed_count_schedule_takes_T_steps_per_block(T):
+    """LLaDA's baseline schedule (fixed B / T tokens per step) as top-k selection: every block ends
+    in exactly T steps, each step unmasks B / T positions per sequence, and they are the B / T most
+    confident of the masked ones."""
+    wl = configs.TINY.with_(batch=2)
+    w64, hidden_fn, prompt = _setup(wl)
+    k = wl.block_size // T
+
+    def hook(g, blk, s, tokens, info):
+        for b in range(wl.batch):
+            sel = np.nonzero(info["unmask"][b])[0]
+            assert len(sel) == k
+            rest = [i for i in np.nonzero(info["masked_before"][b])[0] if i not in sel]
+            if rest:                                  # every pick at least as confident as every non-pick
+                assert info["conf"][b, sel].min() >= info["conf"][b, rest].max()
+        return tokens
+
+    tokens, rec = O.generate(prompt, gen_length=wl.gen_length, block_size=wl.block_size, mask_id=wl.mask_id,
+                             tau=0.9, w=w64, hidden_fn=hidden_fn, strategy="topk", topk=k, step_hook=hook)
+    per_block = np.bincount([r["block"] for r in rec], minlength=wl.gen_length // wl.block_size)
+    assert np.all(per_block == T)
+    assert not (tokens == wl.mask_id).any()
