@@ -28,6 +28,8 @@ Readings where the pages are silent (listed again in the design doc):
   per-sequence blocks each sequence is this oracle run alone at its own window.
 * R13 FP8 weight cache: E4M3 codes, one power-of-two scale per row, round to
   nearest even; hidden rows quantised the same way per step.
+* R14 FP8 KV cache: cached K and V rows (sequence, position, KV head) stored by
+  the R13 rule; attention reads the dequantised cache, fresh K/V unchanged.
 """
 from __future__ import annotations
 
@@ -419,3 +421,30 @@ def lm_head_confidence_fp8(h, w_codes, w_scales):
     per row, then both operands are their exact FP8 values times their scales."""
     hq, hs = quantize_fp8_rows(h)
     return lm_head_confidence(dequantize_fp8_rows(hq, hs), dequantize_fp8_rows(w_codes, w_scales))
+
+
+# ---------------------------------------------------------------------------
+# f4: FP8 KV cache -- the summary's own proposal (section 7, future direction 3).
+# Reading R14: cached keys and values are stored per (sequence, position, KV
+# head) row of d values with the R13 rule (E4M3 codes, one power-of-two scale per
+# row); this step's fresh keys and values and the queries stay as they are.  The
+# attention over such a cache is the block attention of the dequantised cache.
+# ---------------------------------------------------------------------------
+
+def quantize_kv_rows(x):
+    """Codes uint8 [b, n, Hkv, d] and scales [b, n, Hkv] of a K or V array [b, n, Hkv, d]."""
+    b, n, h, d = x.shape
+    codes, scales = quantize_fp8_rows(np.asarray(x, dtype=np.float64).reshape(b * n * h, d))
+    return codes.reshape(b, n, h, d), scales.reshape(b, n, h)
+
+
+def dequantize_kv_rows(codes, scales):
+    b, n, h, d = codes.shape
+    return dequantize_fp8_rows(codes.reshape(-1, d), scales.reshape(-1)).reshape(b, n, h, d)
+
+
+def kv_splice_fp8(codes, scales, src, start):
+    """The FP8 cache after writing src [b, len, Hkv, d] at positions [start, start + len): the
+    window's rows are quantised (R13), every other row is unchanged.  Returns new arrays."""
+    qc, qs = quantize_kv_rows(src)
+    return kv_splice(codes, qc, start), kv_splice(scales, qs, start)

@@ -155,3 +155,50 @@ def test_fp8_confidence_scales_multiply_the_logits():
     l1 = O.lm_head_confidence_fp8(h, wc, ws)["logits"]
     l2 = O.lm_head_confidence_fp8(h, wc2, ws2)["logits"]
     assert np.array_equal(l2, l1 * 8.0)
+
+
+def test_kv_rows_quantise_per_position_and_head():
+    """Each (sequence, position, head) row gets its own scale: scaling one row by 2^j changes only
+    that row's scale, and the window splice leaves every other row's codes and scales alone."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((2, 6, 3, 16))
+    c, s = O.quantize_kv_rows(x)
+    assert c.shape == x.shape and s.shape == (2, 6, 3)
+    y = x.copy()
+    y[1, 4, 2] *= 2.0 ** 5
+    c2, s2 = O.quantize_kv_rows(y)
+    assert np.array_equal(c2, c) and s2[1, 4, 2] == s[1, 4, 2] * 32
+    s2[1, 4, 2] = s[1, 4, 2]
+    assert np.array_equal(s2, s)
+    src = rng.standard_normal((2, 2, 3, 16)) * 100
+    nc, ns = O.kv_splice_fp8(c, s, src, 3)
+    keep = np.ones(6, dtype=bool)
+    keep[3:5] = False
+    assert np.array_equal(nc[:, keep], c[:, keep]) and np.array_equal(ns[:, keep], s[:, keep])
+    deq = O.dequantize_kv_rows(nc, ns)[:, 3:5]
+    assert np.all(np.abs(deq - src) <= np.abs(src) * 2.0 ** -4 + ns[:, 3:5, :, None] * 2.0 ** -10)
+
+
+def test_attention_over_an_exact_fp8_cache_is_the_plain_attention():
+    """A cache whose rows are already E4M3 values times powers of two quantises to itself, so the
+    attention over the dequantised cache equals the plain block attention."""
+    rng = np.random.default_rng(10)
+    grid = O.e4m3_decode(FINITE)
+    small = grid[np.abs(grid) <= 4.0]
+    b, n, hkv, d, s, e = 1, 40, 2, 16, 16, 24
+    kc = rng.choice(small, size=(b, n, hkv, d)) * 2.0 ** rng.integers(-3, 3, (b, n, hkv, 1))
+    vc = rng.choice(small, size=(b, n, hkv, d)) * 2.0 ** rng.integers(-3, 3, (b, n, hkv, 1))
+    kc[..., 0] = 448.0 * 2.0 ** -7                  # every row's maximum sets its scale to 2^-7 ...
+    vc[..., 0] = 448.0 * 2.0 ** -7
+    kc[..., 1:] = np.clip(kc[..., 1:], -2.0, 2.0)   # ... and every value is a grid value at that scale
+    vc[..., 1:] = np.clip(vc[..., 1:], -2.0, 2.0)
+    kq, ks = O.quantize_kv_rows(kc)
+    vq, vs = O.quantize_kv_rows(vc)
+    assert np.array_equal(O.dequantize_kv_rows(kq, ks), kc) and np.array_equal(O.dequantize_kv_rows(vq, vs), vc)
+    q = rng.standard_normal((b, e - s, 4, d))
+    kf = rng.standard_normal((b, e - s, hkv, d))
+    vf = rng.standard_normal((b, e - s, hkv, d))
+    a = O.block_attention(q, O.dequantize_kv_rows(kq, ks), O.dequantize_kv_rows(vq, vs), kf, vf, mode="dual", s=s,
+                          e=e, n_q_heads=4, n_kv_heads=hkv)
+    r = O.block_attention(q, kc, vc, kf, vf, mode="dual", s=s, e=e, n_q_heads=4, n_kv_heads=hkv)
+    assert np.array_equal(a[0], r[0]) and np.array_equal(a[1], r[1])
