@@ -113,6 +113,8 @@ fdllm_status resolve_attn(const fdllm_attn_desc *d, AttnProblem &p) {
   p.scale = d->sm_scale > 0.f ? d->sm_scale : (float)(1.0 / sqrt((double)d->head_dim));
   p.in_bf16 = d->dtype == FDLLM_BF16;
   p.out_f32 = d->out_f32;
+  p.f8kv = 0;
+  p.k_scale = p.v_scale = nullptr;
   return FDLLM_OK;
 }
 
@@ -243,7 +245,7 @@ using namespace fdllm;
 
 extern "C" {
 
-int32_t fdllm_version(void) { return 102; }
+int32_t fdllm_version(void) { return 103; }
 
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
   if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");
@@ -303,13 +305,23 @@ size_t fdllm_attn_workspace_size(const fdllm_attn_desc *desc) {
   return attn_workspace(p);
 }
 
+// k_scale / v_scale non-null: the caches are E4M3 codes with per-row scales (the FP8 KV cache)
 static fdllm_status block_attn(const fdllm_attn_desc *desc, const int32_t *blocks, const void *q,
                                const void *k_cache, const void *v_cache, const void *k_fresh,
                                const void *v_fresh, void *out, float *lse, void *workspace, size_t ws_bytes,
-                               fdllm_stream_t stream) {
+                               fdllm_stream_t stream, const float *k_scale = nullptr,
+                               const float *v_scale = nullptr) {
   AttnProblem p;
   fdllm_status st = resolve_attn(desc, p);
   if (st != FDLLM_OK) return st;
+  if (k_scale || v_scale) {
+    if (!k_scale || !v_scale) return fail(FDLLM_EINVAL, "attn fp8kv: k_scale and v_scale are required");
+    if (!desc->use_cache || !attn_tc_supported(p))
+      return fail(FDLLM_EUNSUPPORTED, "attn fp8kv: needs a cache (use_cache = 1) and bf16 queries and fresh K/V");
+    p.f8kv = 1;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+  }
   if (blocks) {
     if (!desc->use_cache || !desc->dual_cache || !attn_tc_supported(p))
       return fail(FDLLM_EUNSUPPORTED, "attn: per-sequence blocks need DualCache and bf16");
@@ -445,6 +457,47 @@ fdllm_status fdllm_confidence_select_fp8w(const fdllm_select_desc *desc, const v
   p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
   p.err = error_word_ptr();
   return cuda_status(run_select(p, L, workspace, (cudaStream_t)stream), "fp8 quantize / lm-head / select launch");
+}
+
+fdllm_status fdllm_block_attn_fp8kv(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
+                                   const uint8_t *k_cache, const float *k_scale, const uint8_t *v_cache,
+                                   const float *v_scale, const void *k_fresh, const void *v_fresh, void *out,
+                                   float *lse, void *workspace, size_t ws_bytes, fdllm_stream_t stream) {
+  if (!k_scale || !v_scale) return fail(FDLLM_EINVAL, "attn fp8kv: k_scale and v_scale are required");
+  return block_attn(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fresh, out, lse, workspace, ws_bytes, stream,
+                    k_scale, v_scale);
+}
+
+fdllm_status fdllm_kv_splice_fp8(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t start, int32_t len, int32_t src_dtype,
+                                 uint8_t *k_cache, float *k_scale, uint8_t *v_cache, float *v_scale,
+                                 const void *k_src, const void *v_src, fdllm_stream_t stream) {
+  if (mode != FDLLM_SPLICE_WINDOW && mode != FDLLM_SPLICE_REFRESH)
+    return fail(FDLLM_EINVAL, "splice fp8: unknown mode %d", mode);
+  if (batch < 1 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1)
+    return fail(FDLLM_EINVAL, "splice fp8: batch, seq_len, n_kv_heads and head_dim must be >= 1");
+  if (src_dtype != FDLLM_BF16 && src_dtype != FDLLM_F32)
+    return fail(FDLLM_EINVAL, "splice fp8: bad source dtype %d", src_dtype);
+  if (start < 0 || len < 0 || (int64_t)start + len > seq_len)
+    return fail(FDLLM_EINVAL, "splice fp8: window [%d, %d) outside [0, %d)", start, start + len, seq_len);
+  if (mode == FDLLM_SPLICE_REFRESH && (start != 0 || len != seq_len))
+    return fail(FDLLM_EINVAL, "splice fp8: REFRESH rewrites the whole cache (start 0, len seq_len)");
+  const void *ptrs[] = {k_cache, k_scale, v_cache, v_scale, k_src, v_src};
+  for (int i = 0; i < 6; ++i)
+    if (!ptrs[i]) return fail(FDLLM_EINVAL, "splice fp8: null pointer");
+  if (len == 0) return FDLLM_OK;
+  // one row per (sequence, position, KV head): source rows b * len * Hkv + i, cache rows
+  // (b * seq_len + start) * Hkv + i
+  const int64_t rpb = (int64_t)len * n_kv_heads, dst = (int64_t)seq_len * n_kv_heads;
+  const int64_t off = (int64_t)start * n_kv_heads;
+  const bool bf16 = src_dtype == FDLLM_BF16;
+  cudaStream_t cs = (cudaStream_t)stream;
+  cudaError_t e = launch_quantize_fp8_batched(k_src, bf16, batch, rpb, head_dim, rpb, k_cache + off * head_dim,
+                                              k_scale + off, dst, cs);
+  if (e == cudaSuccess)
+    e = launch_quantize_fp8_batched(v_src, bf16, batch, rpb, head_dim, rpb, v_cache + off * head_dim,
+                                    v_scale + off, dst, cs);
+  return cuda_status(e, "splice fp8 launch");
 }
 
 fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,

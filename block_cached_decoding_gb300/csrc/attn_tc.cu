@@ -31,9 +31,18 @@
 // into the CTA that owns the row (CTA c owns rows [c R/C, (c+1) R/C)), and each
 // owner combines the C copies of its rows with weights 2^(m_c - M) / L and
 // writes them.
+//
+// FP8 KV cache (F8KV): cached K and V are E4M3 codes with one power-of-two scale
+// per (sequence, position, KV head) row.  A cache tile is loaded as bytes into
+// the V half of its ring stage; warps 2-3 (one thread per key row) turn it into
+// the bf16 tile TMA would have written -- code * scale is exact in bf16 -- and
+// release it to the MMA issuer, so the products and the softmax are unchanged.
+// Fresh K/V tiles are loaded as bf16 directly.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -42,7 +51,7 @@
 namespace fdllm {
 namespace {
 
-constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, idle; 4-11: softmax (two per TMEM lane quadrant)
+constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, FP8 cache conversion (2, 3); 4-11: softmax (two per quadrant)
 constexpr int kTile = 128;       // rows per query tile
 constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
@@ -88,7 +97,9 @@ struct Cfg {
 
 struct Bars {
   uint64_t qfull, kvfull[8], kvempty[8], sfull[2], sempty[2], pfull[2], pvdone, drain;
-  uint32_t tmem_base;  // (the whole struct must fit the 4096 bytes reserved after the P buffers)
+  uint64_t raw[8];     // F8KV: a cache tile's codes have landed (the converters then complete kvfull)
+  uint32_t tmem_base;
+  int32_t cvt_stop;   // F8KV: the converters stop (written before, read between their two barriers)  // (the whole struct must fit the 4096 bytes reserved after the P buffers)
   int32_t abort;
   int32_t issued;     // K/V tiles issued by the producer
   int32_t consumed;   // K/V tiles whose arrival the MMA issuer waited for
@@ -131,7 +142,51 @@ struct Args {
   int32_t *err;
   const int32_t *blocks;   // per-sequence DualCache block indices (null: the plan's window for all)
   int prompt_len, nblocks;
+  const float *k_scale, *v_scale;   // F8KV: scales of the cached rows [b, N, Hkv]
 };
+
+// The two FP8 conversion warps synchronise among themselves.
+__device__ __forceinline__ void convert_bar() { asm volatile("bar.sync 6, 64;" ::: "memory"); }
+
+// 4 E4M3 codes (one 32-bit word) times `sc` as 4 bf16 (two words); exact: an E4M3 value has at most
+// 4 significant bits and `sc` is a power of two.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w, float sc) {
+  uint32_t o[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> (16 * h)), __NV_E4M3);
+    const float2 f = __half22float2(*(const __half2 *)&hr);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+    o[h] = *(const uint32_t *)&b;
+  }
+  return make_uint2(o[0], o[1]);
+}
+
+// Row r of a bf16 K or V tile in the layout the 128-byte-swizzled TMA load writes: 64-column halves
+// of kKeys rows x 128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7).  `codes` holds the row's
+// D / 16 chunks of 16 codes; chunk slot c holds code chunk (c + r) mod (D / 16) (the rotation
+// spreads a warp's shared-memory accesses over the banks).
+template <int D>
+__device__ __forceinline__ void store_bf16_row(unsigned char *tile, int r, const uint4 (&codes)[D / 16], float sc) {
+  constexpr int NC = D / 16;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int cc = (c + r) & (NC - 1);
+    const uint2 a = e4m3x4_to_bf16x4(codes[c].x, sc), b = e4m3x4_to_bf16x4(codes[c].y, sc);
+    const uint2 d = e4m3x4_to_bf16x4(codes[c].z, sc), e = e4m3x4_to_bf16x4(codes[c].w, sc);
+    unsigned char *half = tile + (cc >> 2) * (kKeys * 128) + r * 128;
+    const int j = (cc & 3) * 2;                      // first of the two 16-byte bf16 chunks
+    *(uint4 *)(half + ((j ^ (r & 7)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
+    *(uint4 *)(half + (((j + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void load_code_row(const unsigned char *row, int r, uint4 (&codes)[D / 16]) {
+  constexpr int NC = D / 16;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) codes[c] = *(const uint4 *)(row + ((c + r) & (NC - 1)) * 16);
+}
 
 __device__ __forceinline__ void fail(Bars &br, int32_t *err, int site) {
   record_device_error(err, site);
@@ -147,7 +202,7 @@ __device__ __forceinline__ bool row_target(const Plan &pl, int nq, int nh, int q
 
 static_assert(sizeof(Bars) <= 4096, "Bars must fit its shared-memory reservation");
 
-template <int D, int KVP>
+template <int D, int KVP, bool F8KV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
@@ -179,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (threadIdx.x == 0) {
-    br.abort = 0; br.issued = 0; br.consumed = 0;
+    br.abort = 0; br.issued = 0; br.consumed = 0; br.cvt_stop = 0;
     tc::mbar_init(&br.qfull, 1);
     for (int i = 0; i < NS; ++i) { tc::mbar_init(&br.kvfull[i], 1); tc::mbar_init(&br.kvempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
@@ -189,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(&br.pvdone, 1);
     tc::mbar_init(&br.drain, 1);
+    for (int i = 0; i < NS; ++i) tc::mbar_init(&br.raw[i], 1);
     tc::fence_barrier_init();
   }
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
@@ -248,14 +304,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap *mk = kt.range == 0 ? &mka : (kt.range == 1 ? &mkf : &mkc);
         const CUtensorMap *mv = kt.range == 0 ? &mva : (kt.range == 1 ? &mvf : &mvc);
         unsigned char *ks = kv_s + st * CF::STAGE;
-        tc::mbar_arrive_expect_tx(&br.kvfull[st], (uint32_t)CF::STAGE);
-        for (int dh = 0; dh < CF::DH; ++dh)
+        if (F8KV && kt.range != 1) {
+          // cache tile: K codes then V codes (kKeys rows x D bytes each) into the stage's V half; the
+          // converters write the bf16 tiles and complete kvfull
+          tc::mbar_arrive_expect_tx(&br.raw[st], (uint32_t)(2 * kKeys * D));
 #pragma unroll
-          for (int p = 0; p < KVP; ++p) {   // the tile's 64 key rows: KVP heads x (64 / KVP) keys
-            const int off = dh * CF::KVHALF + p * (kKeys / KVP) * 128;
-            tc::tma_load_4d(ks + off, mk, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
-            tc::tma_load_4d(ks + CF::KV_BYTES + off, mv, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
+          for (int p = 0; p < KVP; ++p) {
+            const int off = CF::KV_BYTES + p * (kKeys / KVP) * D;
+            tc::tma_load_4d(ks + off, mk, &br.raw[st], 0, kvh + p, kt.row0, b, pol_kv);
+            tc::tma_load_4d(ks + off + kKeys * D, mv, &br.raw[st], 0, kvh + p, kt.row0, b, pol_kv);
           }
+        } else {
+          tc::mbar_arrive_expect_tx(&br.kvfull[st], (uint32_t)CF::STAGE);
+          for (int dh = 0; dh < CF::DH; ++dh)
+#pragma unroll
+            for (int p = 0; p < KVP; ++p) {   // the tile's 64 key rows: KVP heads x (64 / KVP) keys
+              const int off = dh * CF::KVHALF + p * (kKeys / KVP) * 128;
+              tc::tma_load_4d(ks + off, mk, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
+              tc::tma_load_4d(ks + CF::KV_BYTES + off, mv, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
+            }
+        }
         atomicExch(&br.issued, i + 1);
       }
     }
@@ -303,6 +371,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::mma_commit(&br.drain);
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
+    }
+  } else if (F8KV && (warp == 2 || warp == 3)) {
+    // FP8 cache tiles to bf16: thread r converts key row r (KV head kvh + r / tk, key r % tk)
+    const int r = threadIdx.x - 64;
+    const int hp = r / pl.tk, local = r - hp * pl.tk;
+    // Every converter thread takes each exit decision from cvt_stop, which is only written before the
+    // first barrier of an iteration and read between its two barriers: no thread can leave while
+    // another waits at a barrier.
+    uint32_t rawpar = 0;                               // bit st: parity of raw[st]'s next phase
+    // this row's K and V scales, loaded one cache tile ahead so that their latency overlaps a conversion
+    // (the key's cache position: prefix rows are absolute, suffix rows relative to f1 unless the maps
+    // cover the whole cache; rows past N were zero-filled and get scale 0)
+    auto next_cache_tile = [&](int j) {
+      while (j < nt && key_tile(pl, a.nq, a.n, k0 + j).range == 1) ++j;
+      return j;
+    };
+    auto load_scales = [&](int j, float &ks_, float &vs_) {
+      ks_ = 0.f;
+      vs_ = 0.f;
+      if (j >= nt) return;
+      const KeyTile t = key_tile(pl, a.nq, a.n, k0 + j);
+      const int pos = (t.range == 2 && !pl.abs_suffix ? pl.f1 : 0) + t.row0 + local;
+      if (pos < a.n) {
+        const int64_t si = ((int64_t)b * a.n + pos) * a.hkv + kvh + hp;
+        ks_ = __ldg(a.k_scale + si);
+        vs_ = __ldg(a.v_scale + si);
+      }
+    };
+    int inext = next_cache_tile(0);
+    float ksn, vsn;
+    load_scales(inext, ksn, vsn);
+    for (int i = inext; i < nt; i = inext) {
+      const float ksc = ksn, vsc = vsn;
+      inext = next_cache_tile(i + 1);
+      load_scales(inext, ksn, vsn);
+      const int st = i % NS;
+      if (!tc::mbar_wait(&br.raw[st], (rawpar >> st) & 1u)) {
+        fail(br, a.err, 220);
+        br.cvt_stop = 1;
+      }
+      rawpar ^= 1u << st;
+      if (r == 0 && br.abort) br.cvt_stop = 1;
+      convert_bar();
+      if (br.cvt_stop) break;
+      unsigned char *ks = kv_s + st * CF::STAGE;
+      uint4 codes[D / 16];
+      load_code_row<D>(ks + CF::KV_BYTES + r * D, r, codes);
+      store_bf16_row<D>(ks, r, codes, ksc);            // K: codes in the V half, bf16 into the K half
+      load_code_row<D>(ks + CF::KV_BYTES + kKeys * D + r * D, r, codes);
+      convert_bar();                                   // every code of this tile has been read ...
+      store_bf16_row<D>(ks + CF::KV_BYTES, r, codes, vsc);   // ... before V overwrites them in place
+      tc::fence_proxy_async_smem();
+      convert_bar();
+      if (r == 0) tc::mbar_arrive(&br.kvfull[st]);
     }
   } else if (warp >= 4) {
     constexpr int DHALF = D / 2;
@@ -521,8 +643,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   if (br.abort && threadIdx.x == 0) {
     // copies issued but never consumed still land in shared memory: wait for them (bounded)
-    for (int i = br.consumed; i < br.issued; ++i)
-      tc::mbar_wait(&br.kvfull[i % NS], (uint32_t)(i / NS) & 1u);
+    for (int i = br.consumed; i < br.issued; ++i) {
+      if (F8KV && key_tile(pl, a.nq, a.n, k0 + i).range != 1) {
+        int uses = 0;                                  // earlier cache tiles in this stage: raw's phase
+        for (int j = i % NS; j < i; j += NS) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
+        tc::mbar_wait(&br.raw[i % NS], (uint32_t)uses & 1u);
+      } else {
+        tc::mbar_wait(&br.kvfull[i % NS], (uint32_t)(i / NS) & 1u);
+      }
+    }
   }
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, CF::TMEM_COLS);
@@ -555,6 +684,21 @@ bool map4(CUtensorMap *m, const void *base, int d, int heads, int rows, int batc
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E4M3 codes [batch, rows, heads, d] (bytes) with the given batch stride (bytes), box {d, 1, box_rows, 1}
+// (whole rows, no swizzle: the converters read them row by row).
+bool map4_codes(CUtensorMap *m, const void *base, int d, int heads, int rows, int batch, int64_t batch_stride,
+                int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)d, (cuuint64_t)heads * d, (cuuint64_t)batch_stride};
+  const cuuint32_t box[4] = {(cuuint32_t)d, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -610,9 +754,9 @@ Plan make_plan(const AttnProblem &p) {
   return pl;
 }
 
-template <int D, int KVP>
+template <int D, int KVP, bool F8KV>
 cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cudaStream_t st) {
-  auto k = attn_tc_kernel<D, KVP>;
+  auto k = attn_tc_kernel<D, KVP, F8KV>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -636,6 +780,18 @@ cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cud
 
 }  // namespace
 
+template <bool F8KV>
+cudaError_t dispatch_kvp(int d, const Plan &pl, const CUtensorMap *maps, const Args &a, cudaStream_t st) {
+  if (d == 128) {
+    if (pl.kvp == 4) return launch_d<128, 4, F8KV>(pl, maps, a, st);
+    if (pl.kvp == 2) return launch_d<128, 2, F8KV>(pl, maps, a, st);
+    return launch_d<128, 1, F8KV>(pl, maps, a, st);
+  }
+  if (pl.kvp == 4) return launch_d<64, 4, F8KV>(pl, maps, a, st);
+  if (pl.kvp == 2) return launch_d<64, 2, F8KV>(pl, maps, a, st);
+  return launch_d<64, 1, F8KV>(pl, maps, a, st);
+}
+
 bool attn_tc_supported(const AttnProblem &p) { return p.in_bf16 && (p.d == 64 || p.d == 128); }
 
 size_t attn_tc_workspace(const AttnProblem &) { return 0; }
@@ -653,14 +809,22 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const bool per_seq = p.blocks != nullptr;
   const int64_t off_c = per_seq ? 0 : (int64_t)pl.f1 * p.hkv * p.d;
   const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
-  if (!map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) ||
-      !map4(&maps[1], p.kc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) ||
-      !map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) ||
-      !map4(&maps[3], kc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk) ||
-      !map4(&maps[4], p.vc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) ||
-      !map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) ||
-      !map4(&maps[6], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk))
-    return cudaErrorInvalidValue;
+  bool ok = map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
+            map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) &&
+            map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk);
+  if (p.f8kv) {   // the cache as E4M3 codes (one byte per element)
+    const uint8_t *kq = (const uint8_t *)p.kc, *vq = (const uint8_t *)p.vc;
+    ok = ok && map4_codes(&maps[1], kq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
+         map4_codes(&maps[3], kq + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk) &&
+         map4_codes(&maps[4], vq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
+         map4_codes(&maps[6], vq + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk);
+  } else {
+    ok = ok && map4(&maps[1], p.kc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
+         map4(&maps[3], kc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk) &&
+         map4(&maps[4], p.vc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
+         map4(&maps[6], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk);
+  }
+  if (!ok) return cudaErrorInvalidValue;
   Args a;
   a.pl = pl;
   a.batch = p.batch; a.n = p.seq_len; a.nq = p.nq; a.hq = p.hq; a.hkv = p.hkv; a.group = group;
@@ -673,14 +837,10 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   a.blocks = p.blocks;
   a.prompt_len = p.prompt_len;
   a.nblocks = p.nblocks;
-  if (p.d == 128) {
-    if (pl.kvp == 4) return launch_d<128, 4>(pl, maps, a, st);
-    if (pl.kvp == 2) return launch_d<128, 2>(pl, maps, a, st);
-    return launch_d<128, 1>(pl, maps, a, st);
-  }
-  if (pl.kvp == 4) return launch_d<64, 4>(pl, maps, a, st);
-  if (pl.kvp == 2) return launch_d<64, 2>(pl, maps, a, st);
-  return launch_d<64, 1>(pl, maps, a, st);
+  a.k_scale = p.k_scale;
+  a.v_scale = p.v_scale;
+  if (p.f8kv) return dispatch_kvp<true>(p.d, pl, maps, a, st);
+  return dispatch_kvp<false>(p.d, pl, maps, a, st);
 }
 
 }  // namespace fdllm

@@ -56,9 +56,13 @@ __device__ __forceinline__ void unpack(const uint4 &u, float (&x)[8], const floa
   x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y); x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
 }
 
+// Rows R = bb * rpb + r (bb < batch): source row bb * src_bstride + r, destination row (codes and
+// scale) bb * dst_bstride + r.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const T *__restrict__ src, int64_t rows, int cols,
-                                                                 uint8_t *__restrict__ q, float *__restrict__ scale) {
+                                                                 uint8_t *__restrict__ q, float *__restrict__ scale,
+                                                                 int64_t rpb, int64_t src_bstride,
+                                                                 int64_t dst_bstride) {
   // launched as a programmatic dependent: the source may come from the previous kernel in the stream
   tc::pdl_wait_primary();
   tc::pdl_launch_dependents();
@@ -67,8 +71,10 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const T *__rest
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // whole 16-byte vectors when every row starts on a 16-byte boundary (and its codes on VE bytes)
   const bool vec = cols % 16 == 0 && ((uintptr_t)src & 15) == 0 && ((uintptr_t)q & 15) == 0;
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const T *row = src + r * cols;
+  for (int64_t R = blockIdx.x; R < rows; R += gridDim.x) {
+    const int64_t bb = R / rpb, rr = R - bb * rpb;
+    const int64_t r = bb * dst_bstride + rr;           // destination row
+    const T *row = src + (bb * src_bstride + rr) * cols;
     uint8_t *qrow = q + r * cols;
     float m = 0.f;
     if (vec) {
@@ -116,6 +122,13 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const T *__rest
 
 cudaError_t launch_quantize_fp8(const void *src, bool src_bf16, int64_t rows, int cols, uint8_t *q, float *scale,
                                 cudaStream_t st) {
+  return launch_quantize_fp8_batched(src, src_bf16, 1, rows, cols, rows, q, scale, rows, st);
+}
+
+cudaError_t launch_quantize_fp8_batched(const void *src, bool src_bf16, int64_t batch, int64_t rpb, int cols,
+                                        int64_t src_bstride, uint8_t *q, float *scale, int64_t dst_bstride,
+                                        cudaStream_t st) {
+  const int64_t rows = batch * rpb;
   if (rows == 0 || cols == 0) return cudaSuccess;
   int64_t grid = rows;
   const int64_t cap = (int64_t)sm_count() * 8;
@@ -132,9 +145,10 @@ cudaError_t launch_quantize_fp8(const void *src, bool src_bf16, int64_t rows, in
   cudaError_t e;
   if (src_bf16)
     e = cudaLaunchKernelEx(&cfg, quantize_rows_kernel<__nv_bfloat16>, (const __nv_bfloat16 *)src, rows, cols, q,
-                           scale);
+                           scale, rpb, src_bstride, dst_bstride);
   else
-    e = cudaLaunchKernelEx(&cfg, quantize_rows_kernel<float>, (const float *)src, rows, cols, q, scale);
+    e = cudaLaunchKernelEx(&cfg, quantize_rows_kernel<float>, (const float *)src, rows, cols, q, scale, rpb,
+                           src_bstride, dst_bstride);
   count_launches(1);
   return e;
 }

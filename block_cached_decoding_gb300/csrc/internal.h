@@ -21,6 +21,9 @@ struct AttnProblem {
   int prompt_len, nblocks;
   float scale;      // softmax scale
   int in_bf16;      // q / k / v storage
+  // FP8 KV cache (f8kv = 1): kc / vc hold E4M3 codes [b, N, Hkv, d] with scales [b, N, Hkv]
+  int f8kv;
+  const float *k_scale, *v_scale;
   int out_f32;
   const void *q, *kc, *vc, *kf, *vf;
   void *out;
@@ -90,6 +93,10 @@ cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned l
 // rounding and scale rule of the FP8 weight cache); programmatic-dependent launch
 cudaError_t launch_quantize_fp8(const void *src, bool src_bf16, int64_t rows, int cols, uint8_t *q, float *scale,
                                 cudaStream_t st);
+// batch groups of rpb rows: source row bb * src_bstride + r -> codes / scale row bb * dst_bstride + r
+cudaError_t launch_quantize_fp8_batched(const void *src, bool src_bf16, int64_t batch, int64_t rpb, int cols,
+                                        int64_t src_bstride, uint8_t *q, float *scale, int64_t dst_bstride,
+                                        cudaStream_t st);
 
 // select.cu: merge partials [b * B, splits] over splits and unmask
 cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st);

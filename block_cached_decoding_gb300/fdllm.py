@@ -27,7 +27,7 @@ EXPORTS = (
     "fdllm_synth_prompt", "fdllm_launch_counter", "fdllm_confidence_select_noalloc",
     "fdllm_selftest_bounded_wait", "fdllm_block_attn_ragged", "fdllm_confidence_select_ragged",
     "fdllm_kv_splice_ragged", "fdllm_quantize_fp8_rows", "fdllm_select_fp8w_workspace_size",
-    "fdllm_confidence_select_fp8w",
+    "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8",
 )
 
 NOALLOC_SCRATCH_BYTES = 2 << 20
@@ -92,6 +92,10 @@ def lib() -> C.CDLL:
         L.fdllm_select_fp8w_workspace_size.restype = sz
         L.fdllm_confidence_select_fp8w.argtypes = [C.POINTER(SelectDesc)] + [vp] * 10 + [sz, vp]
         L.fdllm_confidence_select_fp8w.restype = i32
+        L.fdllm_block_attn_fp8kv.argtypes = [C.POINTER(AttnDesc)] + [vp] * 11 + [sz, vp]
+        L.fdllm_block_attn_fp8kv.restype = i32
+        L.fdllm_kv_splice_fp8.argtypes = [i32] * 8 + [vp] * 7
+        L.fdllm_kv_splice_fp8.restype = i32
         L.fdllm_status_string.argtypes = [i32]
         L.fdllm_status_string.restype = C.c_char_p
         L.fdllm_last_error.argtypes = []
@@ -250,6 +254,24 @@ def fdllm_kv_splice_ragged(batch, seq_len, n_kv_heads, head_dim, start, length, 
     """Window splice with sequence b's window at start[b] (device int32 [batch])."""
     _check(lib().fdllm_kv_splice_ragged(batch, seq_len, n_kv_heads, head_dim, _ptr(start), length, dtype,
                                         _ptr(k_cache), _ptr(v_cache), _ptr(k_src), _ptr(v_src), _stream(stream)))
+
+
+def fdllm_block_attn_fp8kv(desc, block_idx, q, k_cache, k_scale, v_cache, v_scale, k_fresh, v_fresh, out, lse=None,
+                           workspace=None, ws_bytes=None, stream=None):
+    """fdllm_block_attn over an FP8 cache (E4M3 codes + per-row scales); block_idx None or device int32 [batch]."""
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_block_attn_fp8kv(C.byref(desc), _ptr(block_idx), _ptr(q), _ptr(k_cache), _ptr(k_scale),
+                                        _ptr(v_cache), _ptr(v_scale), _ptr(k_fresh), _ptr(v_fresh), _ptr(out),
+                                        _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fdllm_kv_splice_fp8(mode, batch, seq_len, n_kv_heads, head_dim, start, length, src_dtype, k_cache, k_scale,
+                        v_cache, v_scale, k_src, v_src, stream=None):
+    """Quantise src rows into the FP8 cache window [start, start + length)."""
+    _check(lib().fdllm_kv_splice_fp8(mode, batch, seq_len, n_kv_heads, head_dim, start, length, src_dtype,
+                                     _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale), _ptr(k_src),
+                                     _ptr(v_src), _stream(stream)))
 
 
 def fdllm_last_device_error(stream=None) -> tuple[int, int]:

@@ -34,6 +34,7 @@ def main():
     ap.add_argument("--mode", default="prefix", choices=["dual", "prefix", "none"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fp8w", action="store_true", help="select through the FP8 weight cache")
+    ap.add_argument("--fp8kv", action="store_true", help="attention over the FP8 KV cache")
     ap.add_argument("--ragged", action="store_true",
                     help="per-sequence blocks: sequence i at block i mod (gen / block) (DualCache attention, select)")
     ap.add_argument("--time", action="store_true", help="report the mean call time over the reps (CUDA events)")
@@ -94,8 +95,18 @@ def main():
         wsb = F.fdllm_attn_workspace_size(d)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
         blocks = torch.tensor([i % (a.gen // B) for i in range(b)], dtype=torch.int32, device=dev)
+        if a.fp8kv:
+            kq = torch.empty(b, n, a.hkv, a.d, dtype=torch.uint8, device=dev)
+            vq = torch.empty_like(kq)
+            ksc = torch.empty(b, n, a.hkv, dtype=torch.float32, device=dev)
+            vsc = torch.empty_like(ksc)
+            F.fdllm_kv_splice_fp8(F.SPLICE_REFRESH, b, n, a.hkv, a.d, 0, n, code, kq, ksc, vq, vsc, kc, vc)
+            del kc, vc
         def call():
-            if a.ragged:
+            if a.fp8kv:
+                F.fdllm_block_attn_fp8kv(d, blocks if a.ragged else None, q, kq, ksc, vq, vsc, kf, vf, out, None, ws,
+                                         ws_bytes=wsb)
+            elif a.ragged:
                 F.fdllm_block_attn_ragged(d, blocks, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)
             else:
                 F.fdllm_block_attn(d, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)

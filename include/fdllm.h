@@ -316,6 +316,33 @@ fdllm_status fdllm_confidence_select_fp8w(const fdllm_select_desc *desc, const v
                                           float *kappa, int32_t *argmax, int32_t *n_masked_left, void *workspace,
                                           size_t ws_bytes, fdllm_stream_t stream);
 
+/* FP8 KV cache (the summary's future direction 3).  Cached keys and values
+ * are stored per (sequence, position, KV head) row of head_dim values by the
+ * rule above: k_cache / v_cache hold E4M3 codes (device uint8 [b, N, Hkv, d])
+ * and k_scale / v_scale the row scales (device float [b, N, Hkv]).  Queries
+ * and this step's fresh keys and values stay bf16. */
+
+/* fdllm_block_attn (or, with block_idx non-NULL, fdllm_block_attn_ragged) over
+ * an FP8 cache: the result is the attention over the dequantised cache
+ * (code * scale, exact in bf16).  desc->dtype must be FDLLM_BF16 and
+ * desc->use_cache 1 (PrefixCache or DualCache), else FDLLM_EUNSUPPORTED; null
+ * scales give FDLLM_EINVAL.  Cache rows at the fresh positions are read only
+ * where a key tile crosses a range edge, weighted by exactly zero: they must
+ * hold finite values (any codes written by fdllm_kv_splice_fp8 or zeros). */
+fdllm_status fdllm_block_attn_fp8kv(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
+                                   const uint8_t *k_cache, const float *k_scale, const uint8_t *v_cache,
+                                   const float *v_scale, const void *k_fresh, const void *v_fresh, void *out,
+                                   float *lse, void *workspace, size_t ws_bytes, fdllm_stream_t stream);
+
+/* fdllm_kv_splice into an FP8 cache: each source row (b, i, h) of head_dim
+ * values (src [b, len, Hkv, d], `src_dtype` bf16 or fp32) is quantised into
+ * cache row (b, start + i, h) and its scale; every other row is unchanged.
+ * Modes and window checks as for fdllm_kv_splice.  Two kernels per call. */
+fdllm_status fdllm_kv_splice_fp8(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t start, int32_t len, int32_t src_dtype,
+                                 uint8_t *k_cache, float *k_scale, uint8_t *v_cache, float *v_scale,
+                                 const void *k_src, const void *v_src, fdllm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
@@ -342,7 +369,7 @@ fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream);
 
 /* ABI version: 100 * major + minor (101: the per-sequence block calls; 102: the
- * FP8 weight cache). */
+ * FP8 weight cache; 103: the FP8 KV cache). */
 int32_t fdllm_version(void);
 
 /* Number of kernels this library has launched in the process so far (all

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert F.fdllm_version() == 102
+    assert F.fdllm_version() == 103
     for s in range(5):
         assert lib.fdllm_status_string(s).decode().startswith("FDLLM_")
 
@@ -154,3 +154,21 @@ def test_fp8_calls_validate_on_the_host(lib):
     assert lib.fdllm_quantize_fp8_rows(-1, 64, F.BF16, v, v, v, None) == F.EINVAL
     assert lib.fdllm_quantize_fp8_rows(4, 64, F.BF16, None, v, v, None) == F.EINVAL
     assert lib.fdllm_quantize_fp8_rows(0, 64, F.BF16, None, None, None, None) == F.OK
+
+
+def test_fp8kv_calls_validate_on_the_host(lib):
+    """The FP8 KV cache calls reject a cache-free mode, fp32 descriptors and missing scales before any launch."""
+    v = C.c_void_p(16)
+    d = _attn(dtype=F.BF16, head_dim=128)
+    assert lib.fdllm_block_attn_fp8kv(C.byref(d), None, v, v, None, v, v, v, v, v, None, v, 1 << 20,
+                                      None) == F.EINVAL
+    nocache = _attn(dtype=F.BF16, head_dim=128, use_cache=0)
+    assert lib.fdllm_block_attn_fp8kv(C.byref(nocache), None, v, v, v, v, v, v, v, v, None, v, 1 << 20,
+                                      None) == F.EUNSUPPORTED
+    assert lib.fdllm_block_attn_fp8kv(C.byref(_attn()), None, v, v, v, v, v, v, v, v, None, v, 1 << 20,
+                                      None) == F.EUNSUPPORTED
+    assert lib.fdllm_kv_splice_fp8(F.SPLICE_WINDOW, 1, 64, 2, 64, 60, 8, F.BF16, v, v, v, v, v, v, None) == F.EINVAL
+    assert lib.fdllm_kv_splice_fp8(F.SPLICE_REFRESH, 1, 64, 2, 64, 0, 32, F.BF16, v, v, v, v, v, v, None) == F.EINVAL
+    assert lib.fdllm_kv_splice_fp8(F.SPLICE_WINDOW, 1, 64, 2, 64, 0, 8, 5, v, v, v, v, v, v, None) == F.EINVAL
+    assert lib.fdllm_kv_splice_fp8(F.SPLICE_WINDOW, 1, 64, 2, 64, 0, 8, F.BF16, v, None, v, v, v, v,
+                                   None) == F.EINVAL

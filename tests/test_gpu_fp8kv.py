@@ -1,0 +1,131 @@
+"""FP8 KV cache on the GPU: fdllm_kv_splice_fp8 is bit-exact against the oracle's
+quantiser (codes and scales), and fdllm_block_attn_fp8kv matches the oracle's block
+attention over the dequantised cache (relative L2 <= 5e-3, as for the bf16 cache)."""
+import numpy as np
+import pytest
+import torch
+
+from block_cached_decoding_gb300 import fdllm as F
+from block_cached_decoding_gb300 import synth
+from gpu_helpers import assert_attention_close, code, dev, ensure_built, f64
+from oracle import fdllm_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def fp8_cache(b, n, hkv, d):
+    return (torch.zeros(b, n, hkv, d, dtype=torch.uint8, device="cuda"),
+            torch.zeros(b, n, hkv, dtype=torch.float32, device="cuda"))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_refresh_then_window_splice_bit_exact(dtype):
+    b, n, hkv, d, start, ln = 3, 50, 2, 64, 17, 9
+    kc = synth.kv_cache(4, synth.KIND_KCACHE, b, n, hkv, d, 0, dtype)
+    vc = synth.kv_cache(4, synth.KIND_VCACHE, b, n, hkv, d, 0, dtype, sigma=30.0)
+    ks = synth.kv_cache(5, synth.KIND_KCACHE, b, ln, hkv, d, 0, dtype, sigma=0.01)
+    vs = synth.kv_cache(5, synth.KIND_VCACHE, b, ln, hkv, d, 0, dtype)
+    kq, ksc = fp8_cache(b, n, hkv, d)
+    vq, vsc = fp8_cache(b, n, hkv, d)
+    F.fdllm_kv_splice_fp8(F.SPLICE_REFRESH, b, n, hkv, d, 0, n, code(dtype), kq, ksc, vq, vsc, dev(kc, dtype),
+                          dev(vc, dtype))
+    torch.cuda.synchronize()
+    want_kq, want_ks = O.quantize_kv_rows(f64(kc, dtype))
+    want_vq, want_vs = O.quantize_kv_rows(f64(vc, dtype))
+    assert np.array_equal(kq.cpu().numpy(), want_kq) and np.array_equal(ksc.cpu().numpy(), want_ks)
+    assert np.array_equal(vq.cpu().numpy(), want_vq) and np.array_equal(vsc.cpu().numpy(), want_vs)
+    F.fdllm_kv_splice_fp8(F.SPLICE_WINDOW, b, n, hkv, d, start, ln, code(dtype), kq, ksc, vq, vsc, dev(ks, dtype),
+                          dev(vs, dtype))
+    torch.cuda.synchronize()
+    want_kq, want_ks = O.kv_splice_fp8(want_kq, want_ks, f64(ks, dtype), start)
+    want_vq, want_vs = O.kv_splice_fp8(want_vq, want_vs, f64(vs, dtype), start)
+    assert np.array_equal(kq.cpu().numpy(), want_kq) and np.array_equal(ksc.cpu().numpy(), want_ks)
+    assert np.array_equal(vq.cpu().numpy(), want_vq) and np.array_equal(vsc.cpu().numpy(), want_vs)
+
+
+def run_case(*, batch, prompt_len, gen_length, block_size, hq, hkv, d, mode, out_f32=1, block_idx=0, blocks=None,
+             seed=7, step=0):
+    """The cache is drawn in bf16 and written to FP8 by fdllm_kv_splice_fp8 (REFRESH), checked
+    against the oracle's codes; the attention is compared with the oracle's over the dequantised
+    cache.  `blocks` (a list): sequence b at block blocks[b] (DualCache only)."""
+    dtype = "bf16"
+    n = prompt_len + gen_length
+    kc = synth.kv_cache(seed, synth.KIND_KCACHE, batch, n, hkv, d, 0, dtype)
+    vc = synth.kv_cache(seed, synth.KIND_VCACHE, batch, n, hkv, d, 0, dtype)
+    kq, ksc = fp8_cache(batch, n, hkv, d)
+    vq, vsc = fp8_cache(batch, n, hkv, d)
+    F.fdllm_kv_splice_fp8(F.SPLICE_REFRESH, batch, n, hkv, d, 0, n, F.BF16, kq, ksc, vq, vsc, dev(kc, dtype),
+                          dev(vc, dtype))
+    want_kq, want_ks = O.quantize_kv_rows(f64(kc, dtype))
+    want_vq, want_vs = O.quantize_kv_rows(f64(vc, dtype))
+    torch.cuda.synchronize()
+    assert np.array_equal(kq.cpu().numpy(), want_kq) and np.array_equal(vq.cpu().numpy(), want_vq)
+    k64, v64 = O.dequantize_kv_rows(want_kq, want_ks), O.dequantize_kv_rows(want_vq, want_vs)
+    ks_per = blocks if blocks is not None else [block_idx] * batch
+    windows = [O.block_window(prompt_len, block_size, k) for k in ks_per]
+    nq = block_size if mode == "dual" else n - windows[0][0]
+    q = np.empty((batch, nq, hq, d), dtype=np.uint16)
+    kf = np.empty((batch, nq, hkv, d), dtype=np.uint16)
+    vf = np.empty_like(kf)
+    for bi, (s, e) in enumerate(windows):
+        pos = O.query_positions(mode, s, e, n)
+        q[bi] = synth.per_position(seed, synth.KIND_Q, bi + 1, step, pos, hq * d, dtype)[bi].reshape(nq, hq, d)
+        kf[bi] = synth.per_position(seed, synth.KIND_KFRESH, bi + 1, step, pos, hkv * d, dtype)[bi].reshape(nq, hkv, d)
+        vf[bi] = synth.per_position(seed, synth.KIND_VFRESH, bi + 1, step, pos, hkv * d, dtype)[bi].reshape(nq, hkv, d)
+    desc = F.attn_desc(batch=batch, prompt_len=prompt_len, gen_length=gen_length, block_size=block_size,
+                       block_idx=block_idx, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, use_cache=1,
+                       dual_cache=1 if mode == "dual" else 0, dtype=F.BF16, out_f32=out_f32)
+    out = torch.zeros(batch, nq, hq, d, dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    lse = torch.zeros(batch, nq, hq, dtype=torch.float32, device="cuda")
+    wsb = F.fdllm_attn_workspace_size(desc)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    bidx = None if blocks is None else torch.tensor(blocks, dtype=torch.int32, device="cuda")
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    F.fdllm_block_attn_fp8kv(desc, bidx, dev(q, dtype), kq, ksc, vq, vsc, dev(kf, dtype), dev(vf, dtype), out, lse,
+                             ws, ws_bytes=wsb)
+    torch.cuda.synchronize()
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    o_gpu = out.float().cpu().numpy().astype(np.float64)
+    l_gpu = lse.cpu().numpy()
+    worst = 0.0
+    for bi, (s, e) in enumerate(windows):
+        o_ref, lse_ref = O.block_attention(f64(q[bi:bi + 1], dtype), k64[bi:bi + 1], v64[bi:bi + 1],
+                                           f64(kf[bi:bi + 1], dtype), f64(vf[bi:bi + 1], dtype), mode=mode, s=s, e=e,
+                                           n_q_heads=hq, n_kv_heads=hkv)
+        worst = max(worst, assert_attention_close(o_gpu[bi:bi + 1], o_ref))
+        assert np.abs(l_gpu[bi:bi + 1] - lse_ref).max() < 2e-3, bi
+    return worst
+
+
+@pytest.mark.parametrize("mode", ["dual", "prefix"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_modes(mode, d):
+    run_case(batch=2, prompt_len=200, gen_length=96, block_size=32, block_idx=1, hq=4, hkv=4, d=d, mode=mode)
+
+
+def test_gqa_and_bf16_output():
+    run_case(batch=3, prompt_len=45, gen_length=96, block_size=16, block_idx=2, hq=8, hkv=2, d=128, mode="dual",
+             out_f32=0)
+
+
+def test_block_off_the_key_tile():
+    run_case(batch=2, prompt_len=77, gen_length=60, block_size=20, block_idx=1, hq=4, hkv=4, d=128, mode="dual")
+
+
+def test_long_prompt_split_over_the_cluster():
+    run_case(batch=1, prompt_len=1500, gen_length=256, block_size=32, block_idx=3, hq=8, hkv=8, d=128, mode="dual")
+
+
+def test_heads_packed_per_tile():
+    """40 sequences x 8 KV heads at block 16: four KV heads share one 128-row query tile."""
+    run_case(batch=40, prompt_len=100, gen_length=64, block_size=16, block_idx=2, hq=8, hkv=8, d=64, mode="dual")
+
+
+def test_each_sequence_at_its_own_block():
+    run_case(batch=4, prompt_len=70, gen_length=128, block_size=32, hq=4, hkv=4, d=128, mode="dual",
+             blocks=[2, 0, 3, 1])
