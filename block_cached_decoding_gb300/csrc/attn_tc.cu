@@ -181,6 +181,16 @@ __device__ __forceinline__ void store_bf16_row(unsigned char *tile, int r, const
   }
 }
 
+// Scale of key row r (KV head kvh + r / tk, key r % tk) of cache tile t: the key's cache position is
+// absolute for prefix rows, relative to f1 for suffix rows unless the maps cover the whole cache;
+// rows past N were zero-filled and get scale 0.
+__device__ __forceinline__ float cache_scale(const Args &a, const Plan &pl, const KeyTile &t, int b, int kvh, int r,
+                                             const float *scale) {
+  const int hp = r / pl.tk;
+  const int pos = (t.range == 2 && !pl.abs_suffix ? pl.f1 : 0) + t.row0 + (r - hp * pl.tk);
+  return pos < a.n ? __ldg(scale + ((int64_t)b * a.n + pos) * a.hkv + kvh + hp) : 0.f;
+}
+
 template <int D>
 __device__ __forceinline__ void load_code_row(const unsigned char *row, int r, uint4 (&codes)[D / 16]) {
   constexpr int NC = D / 16;
@@ -373,39 +383,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
     }
   } else if (F8KV && (warp == 2 || warp == 3)) {
-    // FP8 cache tiles to bf16: thread r converts key row r (KV head kvh + r / tk, key r % tk)
+    // FP8 cache K tiles to bf16: thread r converts key row r (KV head kvh + r / tk, key r % tk)
     const int r = threadIdx.x - 64;
-    const int hp = r / pl.tk, local = r - hp * pl.tk;
     // Every converter thread takes each exit decision from cvt_stop, which is only written before the
     // first barrier of an iteration and read between its two barriers: no thread can leave while
     // another waits at a barrier.
     uint32_t rawpar = 0;                               // bit st: parity of raw[st]'s next phase
-    // this row's K and V scales, loaded one cache tile ahead so that their latency overlaps a conversion
-    // (the key's cache position: prefix rows are absolute, suffix rows relative to f1 unless the maps
-    // cover the whole cache; rows past N were zero-filled and get scale 0)
+    // this row's K scale, loaded one cache tile ahead so that its latency overlaps a conversion
     auto next_cache_tile = [&](int j) {
       while (j < nt && key_tile(pl, a.nq, a.n, k0 + j).range == 1) ++j;
       return j;
     };
-    auto load_scales = [&](int j, float &ks_, float &vs_) {
-      ks_ = 0.f;
-      vs_ = 0.f;
-      if (j >= nt) return;
-      const KeyTile t = key_tile(pl, a.nq, a.n, k0 + j);
-      const int pos = (t.range == 2 && !pl.abs_suffix ? pl.f1 : 0) + t.row0 + local;
-      if (pos < a.n) {
-        const int64_t si = ((int64_t)b * a.n + pos) * a.hkv + kvh + hp;
-        ks_ = __ldg(a.k_scale + si);
-        vs_ = __ldg(a.v_scale + si);
-      }
+    auto load_scale = [&](int j) -> float {
+      return j < nt ? cache_scale(a, pl, key_tile(pl, a.nq, a.n, k0 + j), b, kvh, r, a.k_scale) : 0.f;
     };
     int inext = next_cache_tile(0);
-    float ksn, vsn;
-    load_scales(inext, ksn, vsn);
+    float ksn = load_scale(inext);
     for (int i = inext; i < nt; i = inext) {
-      const float ksc = ksn, vsc = vsn;
+      const float ksc = ksn;
       inext = next_cache_tile(i + 1);
-      load_scales(inext, ksn, vsn);
+      ksn = load_scale(inext);
       const int st = i % NS;
       if (!tc::mbar_wait(&br.raw[st], (rawpar >> st) & 1u)) {
         fail(br, a.err, 220);
@@ -419,12 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 codes[D / 16];
       load_code_row<D>(ks + CF::KV_BYTES + r * D, r, codes);
       store_bf16_row<D>(ks, r, codes, ksc);            // K: codes in the V half, bf16 into the K half
-      load_code_row<D>(ks + CF::KV_BYTES + kKeys * D + r * D, r, codes);
-      convert_bar();                                   // every code of this tile has been read ...
-      store_bf16_row<D>(ks + CF::KV_BYTES, r, codes, vsc);   // ... before V overwrites them in place
       tc::fence_proxy_async_smem();
       convert_bar();
-      if (r == 0) tc::mbar_arrive(&br.kvfull[st]);
+      if (r == 0) tc::mbar_arrive(&br.kvfull[st]);     // V is converted by the softmax warps
     }
   } else if (warp >= 4) {
     constexpr int DHALF = D / 2;
@@ -438,10 +432,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     // softmax of tile i over this thread's 32 key columns: P_i = 2^((S_i - m_ref) * scale * log2 e)
+    uint32_t vrawpar = 0;                            // F8KV: bit st, parity of raw[st]'s next phase
     auto softmax = [&](int i) -> bool {
       const int j = i & 1;
-      if (!tc::mbar_wait(&br.sfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 218); return false; }
+      // F8KV: the 256 softmax threads also turn a cache tile's V codes into bf16 (thread t: a quarter of
+      // key row t / 4).  S_i is done, so the converters have read this tile's K codes, which the bf16 V
+      // rows overwrite; P_i's release (below) covers these writes too.
+      const bool cvt_v = F8KV && key_tile(pl, a.nq, a.n, k0 + i).range != 1;
+      const int vt = threadIdx.x - 128, vr = vt >> 2, vq = vt & 3;
+      float vsc = 0.f;
+      if (F8KV && cvt_v) vsc = cache_scale(a, pl, key_tile(pl, a.nq, a.n, k0 + i), b, kvh, vr, a.v_scale);
+      if (!tc::mbar_wait(&br.sfull[j], (uint32_t)(i >> 1) & 1u)) {
+        fail(br, a.err, 218);
+        if (F8KV && cvt_v) softmax_bar();              // the others meet this thread there
+        return false;
+      }
       tc::fence_after_sync();
+      if constexpr (F8KV) {
+        if (cvt_v) {
+          constexpr int QC = D / 64;                   // 16-code chunks per quarter row
+          const int st = i % NS;
+          // the codes' arrival, for this thread: complete long ago (the converters waited for it), and
+          // raw[st] cannot move on before this tile's P is released
+          tc::mbar_wait(&br.raw[st], (vrawpar >> st) & 1u);
+          vrawpar ^= 1u << st;
+          unsigned char *vh = kv_s + st * CF::STAGE + CF::KV_BYTES;
+          uint4 cq[QC];
+#pragma unroll
+          for (int c = 0; c < QC; ++c) cq[c] = *(const uint4 *)(vh + kKeys * D + vr * D + (vq * QC + c) * 16);
+          softmax_bar();                               // every V code of the tile has been read
+#pragma unroll
+          for (int c = 0; c < QC; ++c) {
+            const int cc = vq * QC + c;
+            const uint2 x0 = e4m3x4_to_bf16x4(cq[c].x, vsc), x1 = e4m3x4_to_bf16x4(cq[c].y, vsc);
+            const uint2 x2 = e4m3x4_to_bf16x4(cq[c].z, vsc), x3 = e4m3x4_to_bf16x4(cq[c].w, vsc);
+            unsigned char *row = vh + (cc >> 2) * (kKeys * 128) + vr * 128;
+            const int jj = (cc & 3) * 2;
+            *(uint4 *)(row + ((jj ^ (vr & 7)) * 16)) = make_uint4(x0.x, x0.y, x1.x, x1.y);
+            *(uint4 *)(row + (((jj + 1) ^ (vr & 7)) * 16)) = make_uint4(x2.x, x2.y, x3.x, x3.y);
+          }
+        }
+      }
       // this thread's CW score columns: half `half` of its row's head block (the whole tile when
       // KVP == 1; with KVP heads packed, row r's head owns columns [s TK, s TK + TK), s = r / qr)
       constexpr int TK = kKeys / KVP, CW = TK / 2;

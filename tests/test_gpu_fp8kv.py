@@ -129,3 +129,43 @@ def test_heads_packed_per_tile():
 def test_each_sequence_at_its_own_block():
     run_case(batch=4, prompt_len=70, gen_length=128, block_size=32, hq=4, hkv=4, d=128, mode="dual",
              blocks=[2, 0, 3, 1])
+
+
+@pytest.mark.parametrize("k", [0, -9, 5, -111, 111])
+def test_cache_values_convert_exactly(k):
+    """One cache key per head dominates its queries' scores by thousands (its K row is all 256 codes
+    with scale 1, the others zero), so the fp32 output is exactly that key's dequantised V row: every
+    E4M3 code (normal, subnormal, zero, both signs) times the row's scale 2^k must come out exact,
+    for scales from 2^-111 to 2^111 (every value stays a normal float)."""
+    b, prompt, gen, B, h, d = 1, 64, 32, 16, 4, 128
+    n = prompt + gen
+    s = prompt                                           # block 0, DualCache
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F] + [0x01, 0x81], dtype=np.uint8)
+    assert len(codes) == 2 * d
+    kq = np.zeros((b, n, h, d), dtype=np.uint8)
+    vq = np.random.default_rng(3).integers(0, 256, (b, n, h, d)).astype(np.uint8)
+    vq[(vq & 0x7F) == 0x7F] = 0x30                       # no NaN codes
+    dom = [5, 17, 40, 90]                                # the dominant cache position of each head
+    for hh, p in enumerate(dom):
+        kq[0, p, hh] = 0x78                              # 256: the score is 2^15
+        vq[0, p, hh] = codes[(hh % 2) * d:(hh % 2 + 1) * d]
+    # scale 1: the key's raw score q.k is 128 * 256 = 2^15, a power of two, so every product with the
+    # softmax scale is exact and the key's weight is exactly 1; every other key's is 2^-4000 = 0
+    ksc = np.ones((b, n, h), dtype=np.float32)
+    vsc = np.full((b, n, h), 2.0 ** k, dtype=np.float32)
+    desc = F.attn_desc(batch=b, prompt_len=prompt, gen_length=gen, block_size=B, block_idx=0, n_q_heads=h,
+                       n_kv_heads=h, head_dim=d, use_cache=1, dual_cache=1, dtype=F.BF16, out_f32=1)
+    q = torch.ones(b, B, h, d, dtype=torch.bfloat16, device="cuda")
+    kf = torch.zeros(b, B, h, d, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(b, B, h, d, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(F.fdllm_attn_workspace_size(desc), 16), dtype=torch.uint8, device="cuda")
+    t = lambda x: torch.from_numpy(x).cuda()
+    F.fdllm_block_attn_fp8kv(desc, None, q, t(kq), t(ksc), t(vq), t(vsc), kf, kf, out, None, ws,
+                             ws_bytes=F.fdllm_attn_workspace_size(desc))
+    torch.cuda.synchronize()
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    got = out.cpu().numpy()
+    for hh, p in enumerate(dom):
+        want = (O.e4m3_decode(vq[0, p, hh]) * 2.0 ** k).astype(np.float32)
+        for i in range(B):
+            assert np.array_equal(got[0, i, hh], want), (hh, i)          # exact values (+0 == -0)
