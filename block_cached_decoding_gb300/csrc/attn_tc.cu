@@ -318,21 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // cache tile: K codes then V codes (kKeys rows x D bytes each) into the stage's V half; the
           // converters write the bf16 tiles and complete kvfull
           tc::mbar_arrive_expect_tx(&br.raw[st], (uint32_t)(2 * kKeys * D));
-#pragma unroll
-          for (int p = 0; p < KVP; ++p) {
-            const int off = CF::KV_BYTES + p * (kKeys / KVP) * D;
-            tc::tma_load_4d(ks + off, mk, &br.raw[st], 0, kvh + p, kt.row0, b, pol_kv);
-            tc::tma_load_4d(ks + off + kKeys * D, mv, &br.raw[st], 0, kvh + p, kt.row0, b, pol_kv);
-          }
+          // one box: kKeys / KVP keys of each of the KVP heads, head-major
+          tc::tma_load_4d(ks + CF::KV_BYTES, mk, &br.raw[st], 0, kt.row0, kvh, b, pol_kv);
+          tc::tma_load_4d(ks + CF::KV_BYTES + kKeys * D, mv, &br.raw[st], 0, kt.row0, kvh, b, pol_kv);
         } else {
           tc::mbar_arrive_expect_tx(&br.kvfull[st], (uint32_t)CF::STAGE);
-          for (int dh = 0; dh < CF::DH; ++dh)
-#pragma unroll
-            for (int p = 0; p < KVP; ++p) {   // the tile's 64 key rows: KVP heads x (64 / KVP) keys
-              const int off = dh * CF::KVHALF + p * (kKeys / KVP) * 128;
-              tc::tma_load_4d(ks + off, mk, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
-              tc::tma_load_4d(ks + CF::KV_BYTES + off, mv, &br.kvfull[st], dh * 64, kvh + p, kt.row0, b, pol_kv);
-            }
+          for (int dh = 0; dh < CF::DH; ++dh) {   // per 64-column half, the tile's 64 key rows: KVP heads x
+            const int off = dh * CF::KVHALF;        // (64 / KVP) keys, head-major, in one box
+            tc::tma_load_4d(ks + off, mk, &br.kvfull[st], dh * 64, kt.row0, kvh, b, pol_kv);
+            tc::tma_load_4d(ks + CF::KV_BYTES + off, mv, &br.kvfull[st], dh * 64, kt.row0, kvh, b, pol_kv);
+          }
         }
         atomicExch(&br.issued, i + 1);
       }
@@ -718,18 +713,23 @@ bool map4(CUtensorMap *m, const void *base, int d, int heads, int rows, int batc
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// E4M3 codes [batch, rows, heads, d] (bytes) with the given batch stride (bytes), box {d, 1, box_rows, 1}
-// (whole rows, no swizzle: the converters read them row by row).
-bool map4_codes(CUtensorMap *m, const void *base, int d, int heads, int rows, int batch, int64_t batch_stride,
-                int box_rows) {
+// K or V [batch, rows, heads, d] viewed as (d, rows, heads, batch) -- rows and heads swapped -- with box
+// {64, box_rows, kvp, 1}: one load brings box_rows keys of kvp consecutive heads, head-major, which is
+// the tile layout the kernel uses (row p * box_rows + key of head kvh + p).  bf16 with the 128-byte
+// swizzle, or E4M3 codes (codes = true: whole d-byte rows, no swizzle: the converters read them row by
+// row).  batch_stride is in elements.
+bool map4_kv(CUtensorMap *m, const void *base, int d, int heads, int rows, int batch, int64_t batch_stride,
+             int box_rows, int kvp, bool codes) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)batch};
-  const cuuint64_t strides[3] = {(cuuint64_t)d, (cuuint64_t)heads * d, (cuuint64_t)batch_stride};
-  const cuuint32_t box[4] = {(cuuint32_t)d, 1, (cuuint32_t)box_rows, 1};
+  const cuuint64_t es = codes ? 1 : 2;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)heads, (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)heads * d * es, (cuuint64_t)d * es, (cuuint64_t)batch_stride * es};
+  const cuuint32_t box[4] = {codes ? (cuuint32_t)d : 64u, (cuuint32_t)box_rows, (cuuint32_t)kvp, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, codes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            codes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -840,20 +840,21 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const bool per_seq = p.blocks != nullptr;
   const int64_t off_c = per_seq ? 0 : (int64_t)pl.f1 * p.hkv * p.d;
   const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
+  const int kvp = pl.kvp;
   bool ok = map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
-            map4(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk) &&
-            map4(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk);
+            map4_kv(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false) &&
+            map4_kv(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false);
   if (p.f8kv) {   // the cache as E4M3 codes (one byte per element)
     const uint8_t *kq = (const uint8_t *)p.kc, *vq = (const uint8_t *)p.vc;
-    ok = ok && map4_codes(&maps[1], kq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
-         map4_codes(&maps[3], kq + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk) &&
-         map4_codes(&maps[4], vq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
-         map4_codes(&maps[6], vq + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk);
+    ok = ok && map4_kv(&maps[1], kq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk, kvp, true) &&
+         map4_kv(&maps[3], kq + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk, kvp, true) &&
+         map4_kv(&maps[4], vq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk, kvp, true) &&
+         map4_kv(&maps[6], vq + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk, kvp, true);
   } else {
-    ok = ok && map4(&maps[1], p.kc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
-         map4(&maps[3], kc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk) &&
-         map4(&maps[4], p.vc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk) &&
-         map4(&maps[6], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk);
+    ok = ok && map4_kv(&maps[1], p.kc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk, kvp, false) &&
+         map4_kv(&maps[3], kc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk, kvp, false) &&
+         map4_kv(&maps[4], p.vc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk, kvp, false) &&
+         map4_kv(&maps[6], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk, kvp, false);
   }
   if (!ok) return cudaErrorInvalidValue;
   Args a;
