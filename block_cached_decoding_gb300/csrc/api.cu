@@ -191,7 +191,7 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   return FDLLM_OK;
 }
 
-// workspace: [8-byte arrival ticket, 8-byte start ticket] [partials VocabStat
+// workspace: [8-byte arrival ticket, 8-byte start ticket, 8-byte selectors-done count] [partials VocabStat
 // [b * B, splits], 16 bytes each, from byte 256]; the tensor-core kernel serves bf16
 // blocks of up to 512 rows (and runs the select itself), the CUDA-core kernel the
 // rest (followed by select_kernel)
@@ -245,7 +245,7 @@ using namespace fdllm;
 
 extern "C" {
 
-int32_t fdllm_version(void) { return 103; }
+int32_t fdllm_version(void) { return 104; }
 
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
   if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");

@@ -22,7 +22,8 @@
 // the partials [b * B, clusters] and arrives on a 64-bit ticket in the workspace
 // (high half: this call's epoch, low half: count; a ticket left by another call
 // or uninitialised memory is re-armed first, so the workspace needs no
-// zeroing).  The last min(batch, 8) CTAs to arrive wait for the rest, then merge
+// zeroing; the last selector re-arms the tickets for a launch that repeats this
+// one's epoch, as a CUDA graph replay does).  The last min(batch, 8) CTAs to arrive wait for the rest, then merge
 // the partials of their sequences' masked rows and select the unmasked
 // positions (select_impl.cuh); the others exit.  No CTA ever waits for one that
 // cannot be scheduled, so the launch is an ordinary (programmatic dependent) one.
@@ -92,12 +93,14 @@ struct Shared {
 // value read -- one CTA wins, the others see epoch e on their next read, and
 // the word never holds a stale value again during this call -- then every CTA
 // counts itself with one atomic add.
-__device__ int arrive_ticket(unsigned long long *word, uint32_t e) {
+// The CTA whose compare-and-swap re-arms the word also zeroes `done` (if given): no selector counts
+// on it before every CTA, this one included, has arrived.
+__device__ int arrive_ticket(unsigned long long *word, uint32_t e, unsigned long long *done = nullptr) {
   const unsigned long long tag = (unsigned long long)e << 32;
   for (int attempt = 0; attempt < 64; ++attempt) {
     const unsigned long long v = *(volatile unsigned long long *)word;
     if ((uint32_t)(v >> 32) != e) {
-      atomicCAS(word, v, tag);
+      if (atomicCAS(word, v, tag) == v && done != nullptr) atomicExch(done, 0ull);
       continue;
     }
     const unsigned long long old = atomicAdd(word, 1ull);
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // sequence the selector is the last CTA and never waits.
   if (threadIdx.x == 0) {
     __threadfence();                                   // this CTA's partials before its arrival
-    const int a = arrive_ticket(ticket, epoch);
+    const int a = arrive_ticket(ticket, epoch, ticket + 2);
     if (a == 0) record_device_error(err, 106);
     sh.arrival = a;
   }
@@ -375,6 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   select_finish<kThreads>(sp, part, ncl, sel, sc);
   for (int seq = sel + W; seq < batch; seq += W) select_sequence<kThreads>(sp, part, ncl, seq, sc);
+  // The last selector to finish re-arms both tickets to (this epoch, 0): every CTA has arrived and
+  // every selector has seen the full count, so no one reads them again in this launch.  A launch that
+  // repeats this one's parameters (a CUDA graph replay: same epoch) then counts from zero.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ticket + 2, 1ull) + 1 == (unsigned long long)W) {
+      const unsigned long long armed = (unsigned long long)epoch << 32;
+      atomicExch(ticket, armed);
+      atomicExch(ticket + 1, armed);
+      atomicExch(ticket + 2, 0ull);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------

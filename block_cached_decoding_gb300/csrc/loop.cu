@@ -1,0 +1,111 @@
+// Device-driven block loop.
+//
+// One denoising step -- whatever the caller's step function enqueues on the
+// capture stream: the step's inputs, the block attention, the confidence
+// select -- is captured once as the body of a CUDA graph while-loop.  A small
+// control kernel ends each iteration: it counts the step in a device word and
+// keeps the loop running while some sequence still has a masked position in the
+// block (n_masked_left[b] > 0) and fewer than max_steps steps have run.  A
+// launch therefore runs a whole block with no host round trip between steps;
+// the body starts with the loop's condition set, so it runs at least once.
+//
+// The graph: [reset the step counter] -> [while (condition) { body }], body =
+// [captured step] -> [control].
+#include "common.cuh"
+#include "internal.h"
+
+struct fdllm_block_loop {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+namespace fdllm {
+namespace {
+
+__global__ void loop_reset_kernel(int64_t *counter) { *counter = 0; }
+
+__global__ void loop_control_kernel(cudaGraphConditionalHandle cond, const int32_t *__restrict__ n_left,
+                                    int batch, int64_t *counter, int64_t *total, int64_t max_steps) {
+  __shared__ int any;
+  if (threadIdx.x == 0) any = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < batch; b += blockDim.x)
+    if (n_left[b] > 0) any = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int64_t c = *counter + 1;
+    *counter = c;
+    if (total != nullptr) *total += 1;
+    cudaGraphSetConditional(cond, any && c < max_steps ? 1u : 0u);
+  }
+}
+
+}  // namespace
+}  // namespace fdllm
+
+using namespace fdllm;
+
+extern "C" fdllm_status fdllm_block_loop_create(fdllm_block_loop **out, fdllm_step_fn step, void *user,
+                                                const int32_t *n_masked_left, int32_t batch, int32_t max_steps,
+                                                int64_t *step_counter, int64_t *total_steps) {
+  if (!out || !step || !n_masked_left || !step_counter) return FDLLM_EINVAL;
+  if (batch < 1 || max_steps < 1) return FDLLM_EINVAL;
+  *out = nullptr;
+  cudaGraph_t g = nullptr;
+  cudaStream_t cs = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaError_t e = cudaGraphCreate(&g, 0);
+  cudaGraphConditionalHandle cond = 0;
+  cudaGraphNode_t reset = nullptr, wnode = nullptr;
+  cudaGraph_t body = nullptr, captured = nullptr;
+  if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&cond, g, 1, cudaGraphCondAssignDefault);
+  if (e == cudaSuccess) {
+    void *args[] = {&step_counter};
+    cudaKernelNodeParams kp = {};
+    kp.func = (void *)loop_reset_kernel;
+    kp.gridDim = dim3(1);
+    kp.blockDim = dim3(1);
+    kp.kernelParams = args;
+    e = cudaGraphAddKernelNode(&reset, g, nullptr, 0, &kp);
+  }
+  if (e == cudaSuccess) {
+    cudaGraphNodeParams cp = {};
+    cp.type = cudaGraphNodeTypeConditional;
+    cp.conditional.handle = cond;
+    cp.conditional.type = cudaGraphCondTypeWhile;
+    cp.conditional.size = 1;
+    e = cudaGraphAddNode(&wnode, g, &reset, nullptr, 1, &cp);
+    if (e == cudaSuccess) body = cp.conditional.phGraph_out[0];
+  }
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed);
+  if (e == cudaSuccess) {
+    step(user, (fdllm_stream_t)cs);
+    loop_control_kernel<<<1, 256, 0, cs>>>(cond, n_masked_left, batch, step_counter, total_steps,
+                                           (int64_t)max_steps);
+    const cudaError_t le = cudaGetLastError();
+    e = cudaStreamEndCapture(cs, &captured);
+    if (e == cudaSuccess) e = le;
+  }
+  if (cs) cudaStreamDestroy(cs);
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, g, 0);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    (void)cudaGetLastError();
+    return FDLLM_ECUDA;
+  }
+  *out = new fdllm_block_loop{g, exec};
+  return FDLLM_OK;
+}
+
+extern "C" fdllm_status fdllm_block_loop_launch(fdllm_block_loop *loop, fdllm_stream_t stream) {
+  if (!loop) return FDLLM_EINVAL;
+  return cudaGraphLaunch(loop->exec, (cudaStream_t)stream) == cudaSuccess ? FDLLM_OK : FDLLM_ECUDA;
+}
+
+extern "C" void fdllm_block_loop_destroy(fdllm_block_loop *loop) {
+  if (!loop) return;
+  cudaGraphExecDestroy(loop->exec);
+  cudaGraphDestroy(loop->graph);
+  delete loop;
+}

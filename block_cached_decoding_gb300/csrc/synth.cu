@@ -59,11 +59,13 @@ __device__ __forceinline__ uint64_t row_key(uint64_t seed, int kind, int b, int6
                   (uint64_t)pos);
 }
 
-// rows [b, npos, width]: grid (npos, b)
+// rows [b, npos, width]: grid (npos, b); the step is step + *step_add when step_add is given (a device
+// counter, e.g. a graph loop's)
 template <typename T>
-__global__ void rows_kernel(uint64_t seed, int kind, int64_t step, int pos0, int npos, int width,
-                            float sigma, T *out) {
+__global__ void rows_kernel(uint64_t seed, int kind, int64_t step, const int64_t *step_add, int pos0, int npos,
+                            int width, float sigma, T *out) {
   const int p = blockIdx.x, b = blockIdx.y;
+  if (step_add != nullptr) step += *step_add;
   const uint64_t key = row_key(seed, kind, b, step, pos0 + p);
   T *row = out + ((int64_t)b * npos + p) * width;
   for (int i = threadIdx.x; i < width; i += blockDim.x)
@@ -71,9 +73,10 @@ __global__ void rows_kernel(uint64_t seed, int kind, int64_t step, int pos0, int
 }
 
 template <typename T>
-__global__ void hidden_kernel(uint64_t seed, int64_t step, int pos0, int npos, int hidden, int vocab,
-                              uint64_t plant_thr, const T *w, T *out) {
+__global__ void hidden_kernel(uint64_t seed, int64_t step, const int64_t *step_add, int pos0, int npos, int hidden,
+                              int vocab, uint64_t plant_thr, const T *w, T *out) {
   const int p = blockIdx.x, b = blockIdx.y;
+  if (step_add != nullptr) step += *step_add;
   const uint64_t pk = row_key(seed, FDLLM_SYNTH_PLANT, b, step, pos0 + p);
   const bool planted = (splitmix(pk, 0) >> 40) < plant_thr;
   const int64_t target = (int64_t)(((splitmix(pk, 1) >> 32) * (uint64_t)vocab) >> 32);
@@ -143,6 +146,12 @@ extern "C" int32_t fdllm_synth_kv_cache(uint64_t seed, int32_t kind, int32_t bat
 extern "C" int32_t fdllm_synth_rows(uint64_t seed, int32_t kind, int32_t batch, int64_t step,
                                     int32_t pos0, int32_t npos, int32_t width, float sigma,
                                     int32_t dtype, void *out, fdllm_stream_t stream) {
+  return fdllm_synth_rows_at(seed, kind, batch, step, nullptr, pos0, npos, width, sigma, dtype, out, stream);
+}
+
+extern "C" int32_t fdllm_synth_rows_at(uint64_t seed, int32_t kind, int32_t batch, int64_t step,
+                                       const int64_t *step_add, int32_t pos0, int32_t npos, int32_t width,
+                                       float sigma, int32_t dtype, void *out, fdllm_stream_t stream) {
   if (batch < 1 || batch > 65535 || npos < 0 || width < 1 || (npos > 0 && !out) ||
       (dtype != FDLLM_BF16 && dtype != FDLLM_F32))
     return FDLLM_EINVAL;
@@ -150,9 +159,9 @@ extern "C" int32_t fdllm_synth_rows(uint64_t seed, int32_t kind, int32_t batch, 
   dim3 grid(npos, batch);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
-    rows_kernel<<<grid, 128, 0, st>>>(seed, kind, step, pos0, npos, width, sigma, (__nv_bfloat16 *)out);
+    rows_kernel<<<grid, 128, 0, st>>>(seed, kind, step, step_add, pos0, npos, width, sigma, (__nv_bfloat16 *)out);
   else
-    rows_kernel<<<grid, 128, 0, st>>>(seed, kind, step, pos0, npos, width, sigma, (float *)out);
+    rows_kernel<<<grid, 128, 0, st>>>(seed, kind, step, step_add, pos0, npos, width, sigma, (float *)out);
   return finish();
 }
 
@@ -160,6 +169,12 @@ extern "C" int32_t fdllm_synth_hidden(uint64_t seed, int32_t batch, int64_t step
                                       int32_t npos, int32_t hidden, int32_t vocab, double p_plant,
                                       const void *w, int32_t dtype, void *out,
                                       fdllm_stream_t stream) {
+  return fdllm_synth_hidden_at(seed, batch, step, nullptr, pos0, npos, hidden, vocab, p_plant, w, dtype, out, stream);
+}
+
+extern "C" int32_t fdllm_synth_hidden_at(uint64_t seed, int32_t batch, int64_t step, const int64_t *step_add,
+                                         int32_t pos0, int32_t npos, int32_t hidden, int32_t vocab, double p_plant,
+                                         const void *w, int32_t dtype, void *out, fdllm_stream_t stream) {
   if (batch < 1 || batch > 65535 || npos < 0 || hidden < 1 || vocab < 1 || !w ||
       (npos > 0 && !out) || (dtype != FDLLM_BF16 && dtype != FDLLM_F32) || !(p_plant >= 0.0))
     return FDLLM_EINVAL;
@@ -169,10 +184,10 @@ extern "C" int32_t fdllm_synth_hidden(uint64_t seed, int32_t batch, int64_t step
   dim3 grid(npos, batch);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
-    hidden_kernel<<<grid, 128, 0, st>>>(seed, step, pos0, npos, hidden, vocab, thr,
+    hidden_kernel<<<grid, 128, 0, st>>>(seed, step, step_add, pos0, npos, hidden, vocab, thr,
                                         (const __nv_bfloat16 *)w, (__nv_bfloat16 *)out);
   else
-    hidden_kernel<<<grid, 128, 0, st>>>(seed, step, pos0, npos, hidden, vocab, thr, (const float *)w,
+    hidden_kernel<<<grid, 128, 0, st>>>(seed, step, step_add, pos0, npos, hidden, vocab, thr, (const float *)w,
                                         (float *)out);
   return finish();
 }

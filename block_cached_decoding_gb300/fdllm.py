@@ -27,8 +27,12 @@ EXPORTS = (
     "fdllm_synth_prompt", "fdllm_launch_counter", "fdllm_confidence_select_noalloc",
     "fdllm_selftest_bounded_wait", "fdllm_block_attn_ragged", "fdllm_confidence_select_ragged",
     "fdllm_kv_splice_ragged", "fdllm_quantize_fp8_rows", "fdllm_select_fp8w_workspace_size",
-    "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8",
+    "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8", "fdllm_block_loop_create",
+    "fdllm_block_loop_launch", "fdllm_block_loop_destroy", "fdllm_synth_rows_at", "fdllm_synth_hidden_at",
 )
+
+# void step(void *user, fdllm_stream_t stream)
+STEP_FN = C.CFUNCTYPE(None, C.c_void_p, C.c_void_p)
 
 NOALLOC_SCRATCH_BYTES = 2 << 20
 
@@ -114,8 +118,16 @@ def lib() -> C.CDLL:
         L.fdllm_synth_rows.argtypes = [u64, i32, i32, i64, i32, i32, i32, C.c_float, i32, vp, vp]
         L.fdllm_synth_hidden.argtypes = [u64, i32, i64, i32, i32, i32, i32, C.c_double, vp, i32, vp, vp]
         L.fdllm_synth_prompt.argtypes = [u64, i32, i32, i32, vp, vp]
+        L.fdllm_synth_rows_at.argtypes = [u64, i32, i32, i64, vp, i32, i32, i32, C.c_float, i32, vp, vp]
+        L.fdllm_synth_hidden_at.argtypes = [u64, i32, i64, vp, i32, i32, i32, i32, C.c_double, vp, i32, vp, vp]
+        L.fdllm_block_loop_create.argtypes = [C.POINTER(vp), STEP_FN, vp, vp, i32, i32, vp, vp]
+        L.fdllm_block_loop_create.restype = i32
+        L.fdllm_block_loop_launch.argtypes = [vp, vp]
+        L.fdllm_block_loop_launch.restype = i32
+        L.fdllm_block_loop_destroy.argtypes = [vp]
+        L.fdllm_block_loop_destroy.restype = None
         for f in ("fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
-                  "fdllm_synth_prompt"):
+                  "fdllm_synth_prompt", "fdllm_synth_rows_at", "fdllm_synth_hidden_at"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -315,6 +327,59 @@ def fdllm_synth_rows(seed, kind, batch, step, pos0, npos, width, sigma, dtype, o
 def fdllm_synth_hidden(seed, batch, step, pos0, npos, hidden, vocab, p_plant, w, dtype, out, stream=None):
     _check(lib().fdllm_synth_hidden(seed, batch, step, pos0, npos, hidden, vocab, p_plant, _ptr(w), dtype,
                                     _ptr(out), _stream(stream)))
+
+
+def fdllm_synth_rows_at(seed, kind, batch, step, step_add, pos0, npos, width, sigma, dtype, out, stream=None):
+    """fdllm_synth_rows at step + *step_add (step_add: a device int64 tensor, read when the kernel runs)."""
+    _check(lib().fdllm_synth_rows_at(seed, kind, batch, step, _ptr(step_add), pos0, npos, width, sigma, dtype,
+                                     _ptr(out), _stream(stream)))
+
+
+def fdllm_synth_hidden_at(seed, batch, step, step_add, pos0, npos, hidden, vocab, p_plant, w, dtype, out,
+                          stream=None):
+    _check(lib().fdllm_synth_hidden_at(seed, batch, step, _ptr(step_add), pos0, npos, hidden, vocab, p_plant,
+                                       _ptr(w), dtype, _ptr(out), _stream(stream)))
+
+
+class BlockLoop:
+    """fdllm_block_loop: `step(stream)` is captured once as the body of a device-side while-loop that runs
+    until n_masked_left is all zero or max_steps steps have run; `counter` (device int64) counts them per
+    launch, `total` (device int64 or None) across launches."""
+
+    def __init__(self, step, n_masked_left, batch, max_steps, counter, total=None):
+        self._h = None
+        errors = []
+
+        def body(user, stream):
+            try:
+                step(stream)
+            except BaseException as e:           # an exception cannot cross the C frame: keep it
+                errors.append(e)
+
+        self._cb = STEP_FN(body)                 # kept alive with the loop
+        h = C.c_void_p()
+        st = lib().fdllm_block_loop_create(C.byref(h), self._cb, None, _ptr(n_masked_left), batch, max_steps,
+                                           _ptr(counter), _ptr(total))
+        if st == OK:
+            self._h = h
+        if errors:
+            self.close()
+            raise errors[0]
+        _check(st)
+
+    def launch(self, stream=None):
+        _check(lib().fdllm_block_loop_launch(self._h, _stream(stream)))
+
+    def close(self):
+        if self._h:
+            lib().fdllm_block_loop_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def fdllm_synth_prompt(seed, batch, prompt_len, vocab, out, stream=None):

@@ -151,6 +151,70 @@ class BlockDecoder:
         return StepResult(g, k, s, self.epoch(k, 0) if epoch is None else epoch, self.unmasked, self.conf, self.kappa,
                           self.argmax, self.n_left, out)
 
+    def capture_blocks(self, max_steps_per_block: int | None = None):
+        """One device-driven loop (fdllm_block_loop) per block, captured up front: the step -- inputs drawn at
+        the running device step index, the attention and the select -- repeats on the device until the
+        block has no mask.  Returns the loops and the device counters (steps per block, running total)."""
+        wl = self.wl
+        if self.refresh_interval:
+            raise ValueError("graph loops refresh the cache only at block boundaries")
+        cap = max_steps_per_block or wl.block_size
+        nb = wl.gen_length // wl.block_size
+        dev = self.w.device
+        per_block = torch.zeros(nb, dtype=torch.int64, device=dev)
+        total = torch.zeros(1, dtype=torch.int64, device=dev)
+        b, hq, hkv, d, B = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.block_size
+        loops = []
+        for k in range(nb):
+            p0, p1 = self.query_range(k)
+            nq = p1 - p0
+            s = wl.prompt_len + k * B
+            q, out = _packed(self.q, (b, nq, hq, d)), _packed(self.attn_out, (b, nq, hq, d))
+            kf, vf = _packed(self.kf, (b, nq, hkv, d)), _packed(self.vf, (b, nq, hkv, d))
+            adesc, sdesc = self.attn_desc(k), self.select_desc(s)
+
+            def step(stream, p0=p0, s=s, nq=nq, q=q, out=out, kf=kf, vf=vf, adesc=adesc, sdesc=sdesc):
+                F.fdllm_synth_rows_at(wl.seed, F.SYNTH_Q, b, 0, total, p0, nq, hq * d, 1.0, self.code, self.q, stream)
+                F.fdllm_synth_rows_at(wl.seed, F.SYNTH_KFRESH, b, 0, total, p0, nq, hkv * d, 1.0, self.code, self.kf,
+                                      stream)
+                F.fdllm_synth_rows_at(wl.seed, F.SYNTH_VFRESH, b, 0, total, p0, nq, hkv * d, 1.0, self.code, self.vf,
+                                      stream)
+                F.fdllm_synth_hidden_at(wl.seed, b, 0, total, s, B, wl.hidden, wl.vocab, wl.p_plant, self.w,
+                                        self.code, self.hidden, stream)
+                F.fdllm_block_attn(adesc, q, self.kc, self.vc, kf, vf, out, None, self.attn_ws,
+                                   ws_bytes=self.attn_ws_bytes, stream=stream)
+                F.fdllm_confidence_select(sdesc, self.hidden, self.w, self.tokens, self.unmasked, self.conf,
+                                          self.kappa, self.argmax, self.n_left, self.sel_ws, stream=stream)
+
+            loops.append(F.BlockLoop(step, self.n_left, b, cap, per_block[k:k + 1], total))
+        return loops, per_block, total
+
+    def run_graph(self, max_steps_per_block: int | None = None, loops=None):
+        """The same decode as `run` with every block a device-driven loop (`capture_blocks`, or the given
+        capture): the host only launches each block's loop after its cache refresh and reads the step
+        counts once at the end.  Returns (tokens, steps per block)."""
+        wl = self.wl
+        cap = max_steps_per_block or wl.block_size
+        own = loops is None
+        if own:
+            loops = self.capture_blocks(max_steps_per_block)
+        graphs, per_block, total = loops
+        total.zero_()
+        left = torch.zeros(len(graphs), dtype=torch.int32, device=total.device)
+        for k, g in enumerate(graphs):
+            self.refresh(self.epoch(k, 0))
+            g.launch()
+            left[k] = self.n_left.max()             # stream-ordered, no host wait
+        steps = per_block.tolist()                  # one synchronisation for the whole decode
+        left = left.tolist()
+        if own:
+            for g in graphs:
+                g.close()
+        for k, n_left in enumerate(left):
+            if n_left:
+                raise RuntimeError(f"block {k} did not finish within {cap} steps")
+        return self.tokens, steps
+
     def run(self, hook=None, max_steps_per_block: int | None = None):
         """Decode every block left to right; returns (tokens, steps per block)."""
         wl = self.wl

@@ -144,7 +144,7 @@ typedef struct {
   int32_t dtype;        /* fdllm_dtype of hidden and lm_head_w */
 } fdllm_select_desc;
 
-/* Scratch bytes fdllm_confidence_select needs (two 8-byte tickets plus the
+/* Scratch bytes fdllm_confidence_select needs (three 8-byte ticket words plus the
  * per-split softmax partials of up to batch * block_size rows); 0 on an invalid
  * descriptor.  The workspace needs no initialisation and may be reused by
  * consecutive calls, but two calls that may run at the same time (different
@@ -344,6 +344,39 @@ fdllm_status fdllm_kv_splice_fp8(int32_t mode, int32_t batch, int32_t seq_len, i
                                  const void *k_src, const void *v_src, fdllm_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Device-driven block loop                                                  */
+/* ------------------------------------------------------------------------ */
+/* The block loop of Algorithm 1 (summary 3.4.4) repeats denoising steps until
+ * the block has no mask; a host-driven loop reads the masked count back after
+ * every step (the pages' PyTorch form synchronises on it).  This executor runs
+ * the repetition on the device: `step` is called once, with a capture stream,
+ * and must enqueue one whole denoising step on it (the step's inputs, the
+ * attention, fdllm_confidence_select writing n_masked_left, any splice); that
+ * work becomes the body of a CUDA graph while-loop, and a control kernel after
+ * it counts the step in *step_counter (device int64; 0 at the start of each
+ * launch) and, if total_steps is not NULL, in *total_steps (device int64,
+ * never reset: a running step index across launches); captured work may read
+ * either to key per-step inputs.  It repeats
+ * the body while some n_masked_left[b] > 0 (b < batch) and fewer than
+ * max_steps steps have run.  The body always runs at least once.  Pointers and
+ * descriptors are captured by value: each launch re-runs the same calls on the
+ * same buffers.  Capture uses relaxed mode; `step` must not synchronise.
+ * Kernels launched by the graph are not added to fdllm_launch_counter. */
+typedef struct fdllm_block_loop fdllm_block_loop;
+typedef void (*fdllm_step_fn)(void *user, fdllm_stream_t stream);
+
+/* Build and instantiate the loop; FDLLM_EINVAL for null pointers, batch < 1
+ * or max_steps < 1, FDLLM_ECUDA if capture or instantiation fails. */
+fdllm_status fdllm_block_loop_create(fdllm_block_loop **loop, fdllm_step_fn step, void *user,
+                                     const int32_t *n_masked_left, int32_t batch, int32_t max_steps,
+                                     int64_t *step_counter, int64_t *total_steps);
+
+/* Run the loop once on `stream` (asynchronous). */
+fdllm_status fdllm_block_loop_launch(fdllm_block_loop *loop, fdllm_stream_t stream);
+
+void fdllm_block_loop_destroy(fdllm_block_loop *loop);
+
+/* ------------------------------------------------------------------------ */
 /* Status                                                                    */
 /* ------------------------------------------------------------------------ */
 
@@ -369,7 +402,7 @@ fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream);
 
 /* ABI version: 100 * major + minor (101: the per-sequence block calls; 102: the
- * FP8 weight cache; 103: the FP8 KV cache). */
+ * FP8 weight cache; 103: the FP8 KV cache; 104: the device-driven block loop). */
 int32_t fdllm_version(void);
 
 /* Number of kernels this library has launched in the process so far (all

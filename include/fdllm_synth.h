@@ -61,6 +61,16 @@ int32_t fdllm_synth_hidden(uint64_t seed, int32_t batch, int64_t step, int32_t p
                            int32_t hidden, int32_t vocab, double p_plant, const void *w,
                            int32_t dtype, void *out, fdllm_stream_t stream);
 
+/* fdllm_synth_rows / fdllm_synth_hidden with the step taken as step + *step_add, step_add a device
+ * int64 read when the kernel runs (NULL: step alone): per-step inputs inside a captured CUDA graph
+ * whose step counter lives on the device. */
+int32_t fdllm_synth_rows_at(uint64_t seed, int32_t kind, int32_t batch, int64_t step, const int64_t *step_add,
+                            int32_t pos0, int32_t npos, int32_t width, float sigma, int32_t dtype, void *out,
+                            fdllm_stream_t stream);
+int32_t fdllm_synth_hidden_at(uint64_t seed, int32_t batch, int64_t step, const int64_t *step_add, int32_t pos0,
+                              int32_t npos, int32_t hidden, int32_t vocab, double p_plant, const void *w,
+                              int32_t dtype, void *out, fdllm_stream_t stream);
+
 /* Prompt ids out int32 [b, P], uniform over [0, vocab). */
 int32_t fdllm_synth_prompt(uint64_t seed, int32_t batch, int32_t prompt_len, int32_t vocab,
                            int32_t *out, fdllm_stream_t stream);

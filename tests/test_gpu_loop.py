@@ -116,3 +116,32 @@ def test_fixed_count_schedule(steps_per_block):
     state, steps = lockstep(wl, 0.9, strategy="topk", topk=k)
     assert steps == [steps_per_block] * (wl.gen_length // wl.block_size)
     assert state["unmasked"] == k * state["steps"]
+
+
+@pytest.mark.parametrize("name", ["tiny-fp32", "bf16-batch3", "bf16-tau1"])
+def test_device_driven_loop_matches_the_host_loop(name):
+    """Each block as one CUDA-graph while-loop (fdllm_block_loop) gives the host loop's tokens and step
+    counts exactly: the same kernels on the same inputs, with the repetition decided on the device.
+    Replaying the captured select also replays its workspace tickets' epoch."""
+    wl, tau = {
+        "tiny-fp32": (configs.TINY, 0.9),
+        "bf16-batch3": (configs.LLADA_BATCH.with_(batch=3, prompt_len=40, gen_length=64, block_size=16,
+                                                  n_q_heads=4, n_kv_heads=2, head_dim=128, hidden=512, vocab=3000),
+                        0.9),
+        "bf16-tau1": (configs.LLADA_STEP.with_(prompt_len=30, gen_length=32, block_size=16, n_q_heads=4,
+                                               n_kv_heads=4, head_dim=64, hidden=256, vocab=2000, mode="dual"), 1.0),
+    }[name]
+    t_host, s_host = BlockDecoder(wl, tau=tau).run()
+    t_host = t_host.clone()
+    t_dev, s_dev = BlockDecoder(wl, tau=tau).run_graph()
+    assert s_dev == s_host
+    assert torch.equal(t_dev, t_host)
+    if tau >= 1.0:
+        assert s_dev == [wl.block_size] * (wl.gen_length // wl.block_size)
+
+
+def test_device_driven_loop_stops_at_the_step_cap():
+    wl = configs.LLADA_STEP.with_(prompt_len=30, gen_length=32, block_size=16, n_q_heads=4, n_kv_heads=4,
+                                  head_dim=64, hidden=256, vocab=2000, mode="dual")
+    with pytest.raises(RuntimeError, match="did not finish within 15 steps"):
+        BlockDecoder(wl, tau=1.0).run_graph(max_steps_per_block=15)    # tau = 1: 16 steps per block

@@ -143,7 +143,7 @@ def _select_outputs(desc, hid, w, tokens0, ws):
 
 
 def test_workspace_needs_no_initialisation_and_can_be_shared():
-    """The workspace holds two tickets and the softmax partials; whatever it contains on
+    """The workspace holds three ticket words and the softmax partials; whatever it contains on
     entry (all ones, random bytes, another shape's leftovers), the results are the
     same as with a fresh workspace."""
     rng = np.random.default_rng(11)
