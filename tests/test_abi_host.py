@@ -172,3 +172,15 @@ def test_fp8kv_calls_validate_on_the_host(lib):
     assert lib.fdllm_kv_splice_fp8(F.SPLICE_WINDOW, 1, 64, 2, 64, 0, 8, 5, v, v, v, v, v, v, None) == F.EINVAL
     assert lib.fdllm_kv_splice_fp8(F.SPLICE_WINDOW, 1, 64, 2, 64, 0, 8, F.BF16, v, None, v, v, v, v,
                                    None) == F.EINVAL
+
+
+def test_block_loop_validates_on_the_host(lib):
+    """The device-driven loop rejects missing pointers and empty shapes before touching the device."""
+    h = C.c_void_p()
+    v = C.c_void_p(16)
+    cb = F.STEP_FN(lambda user, stream: None)
+    assert lib.fdllm_block_loop_create(C.byref(h), cb, None, None, 1, 4, v, None) == F.EINVAL
+    assert lib.fdllm_block_loop_create(C.byref(h), cb, None, v, 0, 4, v, None) == F.EINVAL
+    assert lib.fdllm_block_loop_create(C.byref(h), cb, None, v, 1, 0, v, None) == F.EINVAL
+    assert lib.fdllm_block_loop_create(C.byref(h), cb, None, v, 1, 4, None, None) == F.EINVAL
+    assert lib.fdllm_block_loop_launch(None, None) == F.EINVAL
