@@ -14,7 +14,7 @@ Every function states the passage of the Fast-dLLM pages it follows.  Pages:
   if_cache_position (dual cache), threshold.
 
 Inputs are the exact stored values (bfloat16 or float32) upcast to float64.
-Readings where the pages are silent (listed again in the design doc):
+Readings where the pages are silent:
 
 * R1 strict ``c > tau`` (the pages write both ">= tau" and "exceeds tau").
 * R2 ranking for the fallback uses kappa = log((1 - c) / c), strictly
