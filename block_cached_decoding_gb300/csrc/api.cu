@@ -500,6 +500,33 @@ fdllm_status fdllm_kv_splice_fp8(int32_t mode, int32_t batch, int32_t seq_len, i
   return cuda_status(e, "splice fp8 launch");
 }
 
+fdllm_status fdllm_kv_splice_fp8_ragged(int32_t batch, int32_t seq_len, int32_t n_kv_heads, int32_t head_dim,
+                                        const int32_t *start, int32_t len, int32_t src_dtype, uint8_t *k_cache,
+                                        float *k_scale, uint8_t *v_cache, float *v_scale, const void *k_src,
+                                        const void *v_src, fdllm_stream_t stream) {
+  if (!start) return fail(FDLLM_EINVAL, "splice fp8: start is null");
+  if (batch < 1 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1)
+    return fail(FDLLM_EINVAL, "splice fp8: batch, seq_len, n_kv_heads and head_dim must be >= 1");
+  if (src_dtype != FDLLM_BF16 && src_dtype != FDLLM_F32)
+    return fail(FDLLM_EINVAL, "splice fp8: bad source dtype %d", src_dtype);
+  if (len < 0 || len > seq_len) return fail(FDLLM_EINVAL, "splice fp8: len %d outside [0, %d]", len, seq_len);
+  const void *ptrs[] = {k_cache, k_scale, v_cache, v_scale, k_src, v_src};
+  for (int i = 0; i < 6; ++i)
+    if (!ptrs[i]) return fail(FDLLM_EINVAL, "splice fp8: null pointer");
+  if (len == 0) return FDLLM_OK;
+  // source rows b * len * Hkv + i; cache rows (b * seq_len + start[b]) * Hkv + i
+  const int64_t rpb = (int64_t)len * n_kv_heads, dst = (int64_t)seq_len * n_kv_heads;
+  const bool bf16 = src_dtype == FDLLM_BF16;
+  cudaStream_t cs = (cudaStream_t)stream;
+  int32_t *err = error_word_ptr();
+  cudaError_t e = launch_quantize_fp8_batched(k_src, bf16, batch, rpb, head_dim, rpb, k_cache, k_scale, dst, cs,
+                                              start, n_kv_heads, seq_len - len, err);
+  if (e == cudaSuccess)
+    e = launch_quantize_fp8_batched(v_src, bf16, batch, rpb, head_dim, rpb, v_cache, v_scale, dst, cs, start,
+                                    n_kv_heads, seq_len - len, err);
+  return cuda_status(e, "splice fp8 launch");
+}
+
 fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
                              int32_t head_dim, int32_t start, int32_t len, int32_t dtype,
                              void *k_cache, void *v_cache, const void *k_src, const void *v_src,

@@ -93,10 +93,13 @@ cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned l
 // rounding and scale rule of the FP8 weight cache); programmatic-dependent launch
 cudaError_t launch_quantize_fp8(const void *src, bool src_bf16, int64_t rows, int cols, uint8_t *q, float *scale,
                                 cudaStream_t st);
-// batch groups of rpb rows: source row bb * src_bstride + r -> codes / scale row bb * dst_bstride + r
+// batch groups of rpb rows: source row bb * src_bstride + r -> codes / scale row bb * dst_bstride + r,
+// plus starts[bb] * row_step with a per-sequence start array (device; a start outside [0, max_start]
+// skips the sequence and records device error 233 in err)
 cudaError_t launch_quantize_fp8_batched(const void *src, bool src_bf16, int64_t batch, int64_t rpb, int cols,
                                         int64_t src_bstride, uint8_t *q, float *scale, int64_t dst_bstride,
-                                        cudaStream_t st);
+                                        cudaStream_t st, const int32_t *starts = nullptr, int64_t row_step = 0,
+                                        int max_start = 0, int32_t *err = nullptr);
 
 // select.cu: merge partials [b * B, splits] over splits and unmask
 cudaError_t launch_select(const SelectProblem &p, const VocabStat *part, int splits, cudaStream_t st);

@@ -29,6 +29,7 @@ EXPORTS = (
     "fdllm_kv_splice_ragged", "fdllm_quantize_fp8_rows", "fdllm_select_fp8w_workspace_size",
     "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8", "fdllm_block_loop_create",
     "fdllm_block_loop_launch", "fdllm_block_loop_destroy", "fdllm_synth_rows_at", "fdllm_synth_hidden_at",
+    "fdllm_kv_splice_fp8_ragged",
 )
 
 # void step(void *user, fdllm_stream_t stream)
@@ -100,6 +101,8 @@ def lib() -> C.CDLL:
         L.fdllm_block_attn_fp8kv.restype = i32
         L.fdllm_kv_splice_fp8.argtypes = [i32] * 8 + [vp] * 7
         L.fdllm_kv_splice_fp8.restype = i32
+        L.fdllm_kv_splice_fp8_ragged.argtypes = [i32] * 4 + [vp, i32, i32] + [vp] * 7
+        L.fdllm_kv_splice_fp8_ragged.restype = i32
         L.fdllm_status_string.argtypes = [i32]
         L.fdllm_status_string.restype = C.c_char_p
         L.fdllm_last_error.argtypes = []
@@ -284,6 +287,14 @@ def fdllm_kv_splice_fp8(mode, batch, seq_len, n_kv_heads, head_dim, start, lengt
     _check(lib().fdllm_kv_splice_fp8(mode, batch, seq_len, n_kv_heads, head_dim, start, length, src_dtype,
                                      _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale), _ptr(k_src),
                                      _ptr(v_src), _stream(stream)))
+
+
+def fdllm_kv_splice_fp8_ragged(batch, seq_len, n_kv_heads, head_dim, start, length, src_dtype, k_cache, k_scale,
+                               v_cache, v_scale, k_src, v_src, stream=None):
+    """Quantise src rows into each sequence's FP8 cache window at start[b] (device int32 [batch])."""
+    _check(lib().fdllm_kv_splice_fp8_ragged(batch, seq_len, n_kv_heads, head_dim, _ptr(start), length, src_dtype,
+                                            _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale), _ptr(k_src),
+                                            _ptr(v_src), _stream(stream)))
 
 
 def fdllm_last_device_error(stream=None) -> tuple[int, int]:

@@ -343,6 +343,14 @@ fdllm_status fdllm_kv_splice_fp8(int32_t mode, int32_t batch, int32_t seq_len, i
                                  uint8_t *k_cache, float *k_scale, uint8_t *v_cache, float *v_scale,
                                  const void *k_src, const void *v_src, fdllm_stream_t stream);
 
+/* The window splice into an FP8 cache with sequence b's window at start[b]
+ * (device int32 [batch], in [0, seq_len - len]; a start outside it skips the
+ * sequence and sets device error site 233, as fdllm_kv_splice_ragged does). */
+fdllm_status fdllm_kv_splice_fp8_ragged(int32_t batch, int32_t seq_len, int32_t n_kv_heads, int32_t head_dim,
+                                        const int32_t *start, int32_t len, int32_t src_dtype, uint8_t *k_cache,
+                                        float *k_scale, uint8_t *v_cache, float *v_scale, const void *k_src,
+                                        const void *v_src, fdllm_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Device-driven block loop                                                  */
 /* ------------------------------------------------------------------------ */

@@ -169,3 +169,28 @@ def test_cache_values_convert_exactly(k):
         want = (O.e4m3_decode(vq[0, p, hh]) * 2.0 ** k).astype(np.float32)
         for i in range(B):
             assert np.array_equal(got[0, i, hh], want), (hh, i)          # exact values (+0 == -0)
+
+
+def test_per_sequence_window_splice_bit_exact():
+    """Each sequence's window at its own start; an out-of-range start skips its sequence (site 233)."""
+    b, n, hkv, d, ln = 4, 60, 2, 128, 12
+    starts = [5, 0, 48, 61]                              # the last is out of range
+    kc = synth.kv_cache(6, synth.KIND_KCACHE, b, n, hkv, d, 0, "bf16")
+    ks = synth.kv_cache(7, synth.KIND_KCACHE, b, ln, hkv, d, 0, "bf16", sigma=3.0)
+    vs = synth.kv_cache(7, synth.KIND_VCACHE, b, ln, hkv, d, 0, "bf16")
+    want_kq, want_ks = O.quantize_kv_rows(f64(kc, "bf16"))
+    kq, ksc = torch.from_numpy(want_kq).cuda(), torch.from_numpy(want_ks.astype(np.float32)).cuda()
+    vq, vsc = kq.clone(), ksc.clone()
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    F.fdllm_kv_splice_fp8_ragged(b, n, hkv, d, torch.tensor(starts, dtype=torch.int32, device="cuda"), ln, F.BF16,
+                                 kq, ksc, vq, vsc, dev(ks, "bf16"), dev(vs, "bf16"))
+    assert F.fdllm_last_device_error() == (F.EINVAL, 233)
+    got_kq, got_ks, got_vq = kq.cpu().numpy(), ksc.cpu().numpy(), vq.cpu().numpy()
+    for i, s in enumerate(starts):
+        if s + ln <= n:
+            wk, wks = O.kv_splice_fp8(want_kq[i:i + 1], want_ks[i:i + 1], f64(ks[i:i + 1], "bf16"), s)
+            wv, _ = O.kv_splice_fp8(want_kq[i:i + 1], want_ks[i:i + 1], f64(vs[i:i + 1], "bf16"), s)
+        else:
+            wk, wks, wv = want_kq[i:i + 1], want_ks[i:i + 1], want_kq[i:i + 1]
+        assert np.array_equal(got_kq[i:i + 1], wk) and np.array_equal(got_ks[i:i + 1], wks)
+        assert np.array_equal(got_vq[i:i + 1], wv)
