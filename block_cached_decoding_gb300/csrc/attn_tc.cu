@@ -32,12 +32,16 @@
 // owner combines the C copies of its rows with weights 2^(m_c - M) / L and
 // writes them.
 //
+// K/V maps view [b, N, Hkv, d] as (d, position, head, b), so one box brings a
+// tile half's keys of all heads packed in the tile, head-major.
+//
 // FP8 KV cache (F8KV): cached K and V are E4M3 codes with one power-of-two scale
 // per (sequence, position, KV head) row.  A cache tile is loaded as bytes into
-// the V half of its ring stage; warps 2-3 (one thread per key row) turn it into
-// the bf16 tile TMA would have written -- code * scale is exact in bf16 -- and
-// release it to the MMA issuer, so the products and the softmax are unchanged.
-// Fresh K/V tiles are loaded as bf16 directly.
+// the V half of its ring stage; warps 2-3 (one thread per key row) turn the K
+// codes into the bf16 K tile TMA would have written -- code * scale is exact in
+// bf16 -- and release it to the MMA issuer; the softmax warps turn the V codes
+// into the bf16 V tile at the start of the tile's softmax.  The products and the
+// softmax arithmetic are unchanged.  Fresh K/V tiles are loaded as bf16 directly.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -51,7 +55,7 @@
 namespace fdllm {
 namespace {
 
-constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, FP8 cache conversion (2, 3); 4-11: softmax (two per quadrant)
+constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, FP8 K conversion (2, 3); 4-11: softmax (two per quadrant)
 constexpr int kTile = 128;       // rows per query tile
 constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
