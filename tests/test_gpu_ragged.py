@@ -350,3 +350,60 @@ def test_generation_with_sequences_at_their_own_blocks():
     assert advanced == batch * (nblk - 1)
     assert exempt <= 6
     assert apart >= 5          # the oracle alone: 11 of 30 steps
+
+
+@pytest.mark.parametrize("fp8kv", [False, True])
+def test_attention_llada_batch16_full_size_sampled(fp8kv):
+    """The DualCache batch-16 LLaDA shape (N = 1024, 32 heads x 128, block 32), sequence b at block b mod 8,
+    inputs drawn on the device; three sequences' outputs checked row by row against the oracle (with the
+    FP8 cache: over the oracle's dequantisation of the same cache)."""
+    b, P, L, B, h, d, seed = 16, 768, 256, 32, 32, 128, 41
+    n = P + L
+    blocks = [i % (L // B) for i in range(b)]
+    kc = torch.empty(b, n, h, d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    F.fdllm_synth_kv_cache(seed, F.SYNTH_KCACHE, b, n, h, d, 0, 1.0, F.BF16, kc)
+    F.fdllm_synth_kv_cache(seed, F.SYNTH_VCACHE, b, n, h, d, 0, 1.0, F.BF16, vc)
+    # fresh rows: each sequence's own block positions (drawn one sequence at a time on the device)
+    q = torch.empty(b, B, h, d, dtype=torch.bfloat16, device="cuda")
+    kf, vf = torch.empty(b, B, h, d, dtype=torch.bfloat16, device="cuda"), torch.empty(b, B, h, d, dtype=torch.bfloat16, device="cuda")
+    for i, k in enumerate(blocks):
+        s = P + k * B
+        tmp = torch.empty(i + 1, B, h * d, dtype=torch.bfloat16, device="cuda")
+        for kind, dst in ((F.SYNTH_Q, q), (F.SYNTH_KFRESH, kf), (F.SYNTH_VFRESH, vf)):
+            F.fdllm_synth_rows(seed, kind, i + 1, 0, s, B, h * d, 1.0, F.BF16, tmp)
+            dst[i] = tmp[i].view(B, h, d)
+    desc = F.attn_desc(batch=b, prompt_len=P, gen_length=L, block_size=B, block_idx=0, n_q_heads=h, n_kv_heads=h,
+                       head_dim=d, use_cache=1, dual_cache=1, dtype=F.BF16, out_f32=1)
+    out = torch.empty(b, B, h, d, dtype=torch.float32, device="cuda")
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    bidx = _ints(blocks)
+    if fp8kv:
+        kq = torch.empty(b, n, h, d, dtype=torch.uint8, device="cuda")
+        vq = torch.empty_like(kq)
+        ks = torch.empty(b, n, h, dtype=torch.float32, device="cuda")
+        vs = torch.empty_like(ks)
+        F.fdllm_kv_splice_fp8(F.SPLICE_REFRESH, b, n, h, d, 0, n, F.BF16, kq, ks, vq, vs, kc, vc)
+        F.fdllm_block_attn_fp8kv(desc, bidx, q, kq, ks, vq, vs, kf, vf, out, None, ws, ws_bytes=0)
+    else:
+        F.fdllm_block_attn_ragged(desc, bidx, q, kc, vc, kf, vf, out, None, ws, ws_bytes=0)
+    torch.cuda.synchronize()
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    got = out.cpu().numpy().astype(np.float64)
+    per = n * h * d
+    for i in (0, 7, 13):
+        s = P + blocks[i] * B
+        kci = synth.scaled_normals(synth.stream_key(seed, synth.KIND_KCACHE, i, 0), per, 1.0, "bf16")
+        vci = synth.scaled_normals(synth.stream_key(seed, synth.KIND_VCACHE, i, 0), per, 1.0, "bf16")
+        k64 = f64(kci, "bf16").reshape(1, n, h, d)
+        v64 = f64(vci, "bf16").reshape(1, n, h, d)
+        if fp8kv:
+            k64 = O.dequantize_kv_rows(*O.quantize_kv_rows(k64))
+            v64 = O.dequantize_kv_rows(*O.quantize_kv_rows(v64))
+        rows = lambda kind, w: np.stack([synth.scaled_normals(synth.stream_key(seed, kind, i, 0, p), w, 1.0, "bf16")
+                                         for p in range(s, s + B)])
+        qi = f64(rows(synth.KIND_Q, h * d), "bf16").reshape(1, B, h, d)
+        kfi = f64(rows(synth.KIND_KFRESH, h * d), "bf16").reshape(1, B, h, d)
+        vfi = f64(rows(synth.KIND_VFRESH, h * d), "bf16").reshape(1, B, h, d)
+        o_ref, _ = O.block_attention(qi, k64, v64, kfi, vfi, mode="dual", s=s, e=s + B, n_q_heads=h, n_kv_heads=h)
+        assert_attention_close(got[i:i + 1], o_ref)
