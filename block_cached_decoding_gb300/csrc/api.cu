@@ -8,6 +8,9 @@
 #include <mutex>
 #include <string>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -47,20 +50,84 @@ fdllm_status cuda_status(cudaError_t e, const char *what) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The clustered LM head multicasts tiles of its operands between the CTAs of a cluster; it is
+// meant for memory of this GPU only, so each operand must be device memory (cudaMalloc, torch)
+// of the current device: host, managed or another device's memory is rejected.
+fdllm_status check_local_device(const void *ptr, const char *what) {
+  int dev = 0;
+  fdllm_status st = cuda_status(cudaGetDevice(&dev), "cudaGetDevice");
+  if (st != FDLLM_OK) return st;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(FDLLM_EINVAL, "select: %s is not CUDA device memory", what);
+  }
+  if (at.type != cudaMemoryTypeDevice || at.device != dev)
+    return fail(FDLLM_EINVAL,
+                "select: with more than 128 block rows, %s must be device memory of the current device "
+                "(memory type %d on device %d; current device %d)",
+                what, (int)at.type, at.device, dev);
+  return FDLLM_OK;
+}
+
+// The LM head's operands (hidden rows or their E4M3 copy, weight) when the clustered kernel runs.
+fdllm_status check_cluster_operands(const SelectProblem &p, bool tc, const void *hidden, const void *w) {
+  if (!tc || !lmhead_tc_clustered(p)) return FDLLM_OK;
+  fdllm_status st = check_local_device(hidden, "hidden");
+  if (st != FDLLM_OK) return st;
+  return check_local_device(w, "lm_head_w");
+}
+
 constexpr int kMaxDevices = 64;
 
-int32_t *error_word_ptr() {
-  static int32_t *ptrs[kMaxDevices] = {nullptr};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(mu);
-  if (!ptrs[dev]) {
+// The calling thread's current CUDA context, or null if it cannot be read.  A device address of a
+// __device__ variable is valid only in the context it was looked up in (a device reset creates a
+// new primary context), so cached addresses are keyed by it.
+void *current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = [] {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = (int32_t *)p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return (PFN_cuCtxGetCurrent_v4000)p;
+    return (PFN_cuCtxGetCurrent_v4000) nullptr;
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return (void *)c;
+}
+
+// Device address of a __device__ symbol on the current device, looked up with
+// cudaGetSymbolAddress the first time it is needed in each (device, context) and cached.
+struct SymbolCache {
+  std::mutex mu;
+  void *ctx[kMaxDevices] = {nullptr};
+  void *ptr[kMaxDevices] = {nullptr};
+
+  cudaError_t get(const void *symbol, void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    // make sure the device's primary context exists (the lookup below would create it too)
+    void *c = current_context();
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptr[dev] || c == nullptr || ctx[dev] != c) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, symbol);
+      if (e != cudaSuccess) return e;
+      ptr[dev] = p;
+      ctx[dev] = current_context();
+    }
+    *out = ptr[dev];
+    return cudaSuccess;
   }
-  return ptrs[dev];
+};
+
+int32_t *error_word_ptr() {
+  static SymbolCache cache;
+  void *p = nullptr;
+  return cache.get((const void *)&g_device_error_word, &p) == cudaSuccess ? (int32_t *)p : nullptr;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -383,6 +450,8 @@ static fdllm_status confidence_select(const fdllm_select_desc *desc, const int32
   const SelectLayout L = select_layout(p);
   if (ws_bytes < L.total)
     return fail(FDLLM_EINVAL, "select: workspace of %zu bytes is smaller than the %zu required", ws_bytes, L.total);
+  st = check_cluster_operands(p, L.tc, hidden, lm_head_w);
+  if (st != FDLLM_OK) return st;
   p.hidden = hidden; p.w = lm_head_w; p.tokens = tokens; p.unmasked = unmasked; p.conf = conf;
   p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
   p.err = error_word_ptr();
@@ -453,6 +522,8 @@ fdllm_status fdllm_confidence_select_fp8w(const fdllm_select_desc *desc, const v
   if (ws_bytes < L.total)
     return fail(FDLLM_EINVAL, "select fp8w: workspace of %zu bytes is smaller than the %zu required", ws_bytes,
                 L.total);
+  st = check_cluster_operands(p, L.tc, workspace, w_q);   // the kernel reads the E4M3 rows from the workspace
+  if (st != FDLLM_OK) return st;
   p.hidden = hidden; p.w = w_q; p.w_scale = w_scale; p.tokens = tokens; p.unmasked = unmasked; p.conf = conf;
   p.kappa = kappa; p.argmax = argmax; p.n_left = n_masked_left; p.ws = workspace; p.ws_bytes = ws_bytes;
   p.err = error_word_ptr();
@@ -586,23 +657,11 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FDLLM_NOALLOC_S
 
 // Device address of g_noalloc_scratch on the current device.  In host code the
 // array's name is only a stand-in for the symbol, so the address is looked up
-// once per device (with that device current) and cached.
+// once per device and context (with that device current) and cached; a new
+// context on the device (after a device reset) gets a fresh lookup.
 fdllm_status noalloc_scratch(void **out) {
-  static void *ptrs[kMaxDevices] = {nullptr};
-  static std::mutex mu;
-  int dev = 0;
-  fdllm_status st = cuda_status(cudaGetDevice(&dev), "noalloc select: cudaGetDevice");
-  if (st != FDLLM_OK) return st;
-  if (dev < 0 || dev >= kMaxDevices) return fail(FDLLM_ECUDA, "noalloc select: device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lk(mu);
-  if (!ptrs[dev]) {
-    void *p = nullptr;
-    st = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_scratch), "noalloc select: cudaGetSymbolAddress");
-    if (st != FDLLM_OK) return st;
-    ptrs[dev] = p;
-  }
-  *out = ptrs[dev];
-  return FDLLM_OK;
+  static SymbolCache cache;
+  return cuda_status(cache.get((const void *)g_noalloc_scratch, out), "noalloc select: cudaGetSymbolAddress");
 }
 
 }  // namespace
@@ -628,6 +687,8 @@ extern "C" fdllm_status fdllm_confidence_select_noalloc(const fdllm_select_desc 
                 "noalloc select: the vocabulary partials need %zu bytes, more than the %u-byte static scratch "
                 "(batch * block_size = %d rows x %d splits); use fdllm_confidence_select with a workspace",
                 L.total, (unsigned)FDLLM_NOALLOC_SCRATCH_BYTES, p.batch * p.B, L.splits);
+  st = check_cluster_operands(p, L.tc, hidden, lm_head_w);
+  if (st != FDLLM_OK) return st;
   void *scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != FDLLM_OK) return st;

@@ -301,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = (warp & 3) * 32 + lane;
   const int half = (warp - 4) >> 2;
   float m_run = kNegInf, l_run = 0.f;
+  // set by the first wait that gives up (fail()); every later wait that polls it returns at once
+  const volatile int32_t *abort_flag = &br.abort;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -313,7 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kvh * a.group + h0 + hs, q0, b, pol_q);
       for (int i = 0; i < nt && !br.abort; ++i) {
         const int st = i % NS;
-        if (!tc::mbar_wait(&br.kvempty[st], ((uint32_t)(i / NS) & 1u) ^ 1u)) { fail(br, a.err, 211); break; }
+        if (!tc::mbar_wait_or_abort(&br.kvempty[st], ((uint32_t)(i / NS) & 1u) ^ 1u, abort_flag)) {
+          if (!*abort_flag) fail(br, a.err, 211);
+          break;
+        }
         const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + i);
         const CUtensorMap *mk = kt.range == 0 ? &mka : (kt.range == 1 ? &mkf : &mkc);
         const CUtensorMap *mv = kt.range == 0 ? &mva : (kt.range == 1 ? &mvf : &mvc);
@@ -341,13 +346,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = tc::idesc_bf16_f32(128, kKeys, 0);
       const uint32_t id_o = tc::idesc_bf16_f32(128, D, 1);
       const uint32_t qa = tc::smem_u32(q_s);
-      bool ok = tc::mbar_wait(&br.qfull, 0);
-      if (!ok) fail(br, a.err, 212);
+      bool ok = tc::mbar_wait_or_abort(&br.qfull, 0, abort_flag);
+      if (!ok && !*abort_flag) fail(br, a.err, 212);
       auto issue_s = [&](int i) -> bool {
         const int st = i % NS, j = i & 1;
-        if (!tc::mbar_wait(&br.kvfull[st], (uint32_t)(i / NS) & 1u)) { fail(br, a.err, 213); return false; }
+        if (!tc::mbar_wait_or_abort(&br.kvfull[st], (uint32_t)(i / NS) & 1u, abort_flag)) {
+          if (!*abort_flag) fail(br, a.err, 213);
+          return false;
+        }
         atomicExch(&br.consumed, i + 1);
-        if (!tc::mbar_wait(&br.sempty[j], ((uint32_t)(i >> 1) & 1u) ^ 1u)) { fail(br, a.err, 214); return false; }
+        if (!tc::mbar_wait_or_abort(&br.sempty[j], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag)) {
+          if (!*abort_flag) fail(br, a.err, 214);
+          return false;
+        }
         tc::fence_after_sync();
         const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
 #pragma unroll
@@ -361,7 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int i) -> bool {
         const int st = i % NS, j = i & 1;
-        if (!tc::mbar_wait(&br.pfull[j], (uint32_t)(i >> 1) & 1u)) { fail(br, a.err, 215); return false; }
+        if (!tc::mbar_wait_or_abort(&br.pfull[j], (uint32_t)(i >> 1) & 1u, abort_flag)) {
+          if (!*abort_flag) fail(br, a.err, 215);
+          return false;
+        }
         tc::fence_after_sync();
         const uint32_t pa = tc::smem_u32(p_s + j * CF::P_BYTES);
         const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
@@ -403,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       inext = next_cache_tile(i + 1);
       ksn = load_scale(inext);
       const int st = i % NS;
-      if (!tc::mbar_wait(&br.raw[st], (rawpar >> st) & 1u)) {
-        fail(br, a.err, 220);
+      if (!tc::mbar_wait_or_abort(&br.raw[st], (rawpar >> st) & 1u, abort_flag)) {
+        if (!*abort_flag) fail(br, a.err, 220);
         br.cvt_stop = 1;
       }
       rawpar ^= 1u << st;
@@ -423,16 +437,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int DHALF = D / 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t oa = tmem + lane_base + CF::O_COL + (uint32_t)(half * DHALF);   // this thread's O columns
+    // Every softmax warp runs every tile and meets every named barrier (the pair's quadrant barrier,
+    // the 256-thread softmax barrier) the same number of times, whatever its waits return: a wait that
+    // gives up only marks this thread's result invalid (ok = false), records the site and raises the
+    // abort flag, after which every wait of the CTA returns at once.  So no warp can be left waiting
+    // at a named barrier for a partner that has left the loop.
     bool ok = true;
     // wait until PV_i has been accumulated into O (phases complete in order, one per tile)
-    auto wait_pv = [&](int i) -> bool {
-      if (!tc::mbar_wait(&br.pvdone, (uint32_t)i & 1u)) { fail(br, a.err, 219); return false; }
+    auto wait_pv = [&](int i) {
+      if (!tc::mbar_wait_or_abort(&br.pvdone, (uint32_t)i & 1u, abort_flag)) {
+        if (!*abort_flag) fail(br, a.err, 219);
+        ok = false;
+      }
       tc::fence_after_sync();
-      return true;
     };
     // softmax of tile i over this thread's 32 key columns: P_i = 2^((S_i - m_ref) * scale * log2 e)
     uint32_t vrawpar = 0;                            // F8KV: bit st, parity of raw[st]'s next phase
-    auto softmax = [&](int i) -> bool {
+    auto softmax = [&](int i) {
       const int j = i & 1;
       // F8KV: the 256 softmax threads also turn a cache tile's V codes into bf16 (thread t: a quarter of
       // key row t / 4).  S_i is done, so the converters have read this tile's K codes, which the bf16 V
@@ -441,10 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int vt = threadIdx.x - 128, vr = vt >> 2, vq = vt & 3;
       float vsc = 0.f;
       if (F8KV && cvt_v) vsc = cache_scale(a, pl, key_tile(pl, a.nq, a.n, k0 + i), b, kvh, vr, a.v_scale);
-      if (!tc::mbar_wait(&br.sfull[j], (uint32_t)(i >> 1) & 1u)) {
-        fail(br, a.err, 218);
-        if (F8KV && cvt_v) softmax_bar();              // the others meet this thread there
-        return false;
+      if (!tc::mbar_wait_or_abort(&br.sfull[j], (uint32_t)(i >> 1) & 1u, abort_flag)) {
+        if (!*abort_flag) fail(br, a.err, 218);
+        ok = false;
       }
       tc::fence_after_sync();
       if constexpr (F8KV) {
@@ -453,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = i % NS;
           // the codes' arrival, for this thread: complete long ago (the converters waited for it), and
           // raw[st] cannot move on before this tile's P is released
-          tc::mbar_wait(&br.raw[st], (vrawpar >> st) & 1u);
+          if (!tc::mbar_wait_or_abort(&br.raw[st], (vrawpar >> st) & 1u, abort_flag)) ok = false;
           vrawpar ^= 1u << st;
           unsigned char *vh = kv_s + st * CF::STAGE + CF::KV_BYTES;
           uint4 cq[QC];
@@ -501,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = need ? fmaxf(m_run, tm) : m_run;
         const float al = tc::ex2_approx((m_run - m_new) * a.scale_log2);   // 0 on a row's first tile
         if (i > 0) {
-          if (!wait_pv(i - 1)) return false;       // O holds PV_0 .. PV_{i-1}
+          wait_pv(i - 1);                          // O holds PV_0 .. PV_{i-1}
 #pragma unroll
           for (int c0 = 0; c0 < DHALF; c0 += 32) {
             uint32_t o[32];
@@ -544,10 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mbar_arrive(&br.pfull[j]);
         tc::mbar_arrive(&br.sempty[j]);
       }
-      return true;
     };
-    for (int i = 0; i < nt && ok; ++i) ok = softmax(i);
-    if (ok && nt > 0) ok = wait_pv(nt - 1);        // O is complete
+    for (int i = 0; i < nt; ++i) softmax(i);
+    if (nt > 0) wait_pv(nt - 1);                   // O is complete
     if (!ok) l_run = 0.f;
     br.lhalf[half][r] = l_run;
     softmax_bar();

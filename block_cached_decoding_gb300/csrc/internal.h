@@ -85,6 +85,10 @@ cudaError_t launch_lmhead_simt(const SelectProblem &p, VocabStat *part, int spli
 // [b * B, splits] and runs the merge + select itself; `ticket` is 8 bytes of
 // workspace.  lmhead_tc_grid gives the number of vocabulary splits (clusters).
 bool lmhead_tc_supported(const SelectProblem &p);
+// true when the kernel runs in thread-block clusters (more than 128 block rows): its operand tiles
+// are then multicast between the CTAs of a cluster, and the operands must be device memory of the
+// current device
+bool lmhead_tc_clustered(const SelectProblem &p);
 int lmhead_tc_grid(const SelectProblem &p);
 cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int splits,
                              cudaStream_t st);

@@ -29,8 +29,13 @@
 // cannot be scheduled, so the launch is an ordinary (programmatic dependent) one.
 //
 // Every mbarrier wait is bounded; a wait that gives up records a site code in
-// the device error word, the CTA stops issuing work, waits (bounded) for the
-// copies and MMAs it already issued, frees its TMEM and exits.
+// the device error word and sets the abort flag in every CTA of the cluster.
+// Producers and MMA issuers stop at their next stage, every wait that polls the
+// flag returns, each CTA waits (bounded) for its own MMAs, and after a cluster
+// barrier each CTA settles the copies and MMA commits addressed to it from the
+// stage counts every CTA published (settle_after_abort), so that no transfer
+// of a peer reaches a CTA that has left; then a second cluster barrier, TMEM
+// freed, exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <unistd.h>
@@ -124,9 +129,81 @@ __device__ bool wait_ticket(const unsigned long long *word, uint32_t e, int coun
   }
 }
 
-__device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site) {
+// A wait of this CTA gave up: record the site and stop the whole cluster.  The flag is set in
+// every CTA of the cluster (distributed shared memory when CS > 1 and the launch has CS-CTA
+// clusters), so every producer and MMA issuer stops at its next stage and every wait that polls the
+// flag returns; the settlement after the first cluster barrier then accounts for the transfers that
+// were already in flight.
+template <int CS>
+__device__ __forceinline__ void set_abort(Shared &sh, int32_t *err, int site, bool cluster) {
   record_device_error(err, site);
-  atomicExch(&sh.abort, 1);
+  if (CS > 1 && cluster) {
+    for (uint32_t r = 0; r < (uint32_t)CS; ++r) tc::st_cluster_u32(tc::cluster_map(&sh.abort, r), 1u);
+  } else {
+    atomicExch(&sh.abort, 1);
+  }
+}
+
+// Bytes of one stage that cluster CTA r loads into every CTA: its W boxes u = r, r + CS, ... < nu.
+template <int CS>
+__device__ __forceinline__ uint32_t share_bytes(int r, int nu) {
+  return r < nu ? (uint32_t)((nu - r + CS - 1) / CS) * (uint32_t)(kUnit * kRowBytes) : 0u;
+}
+
+// After an abort, with every producer and MMA issuer of the cluster stopped (first cluster barrier
+// passed), wait until every copy and every MMA commit addressed to this CTA has landed, so that no
+// transfer reaches it after it exits.  issued[r] / consumed[r] are the stage counts of cluster CTA
+// r (copies issued by its producer; stages whose MMAs its issuer committed).  A peer issues stage
+// i only after its empty barrier saw every CTA's commit for stage i - STAGES, so the copies still
+// unaccounted for here are those of stages [consumed[c], max issued), one use per ring slot.  Each
+// such full barrier is completed exactly: bytes that a peer never sent are completed by hand
+// (complete_tx), and a stage this CTA never armed is armed for the bytes the peers did send.  The
+// commits are settled the same way on the empty barriers: arrivals of CTAs that never committed a
+// stage are made by this CTA itself, and the phase then completes when the real ones have landed.
+template <int CS>
+__device__ void settle_after_abort(Shared &sh, int c, int u0, int u1, int kchunks, int32_t *err) {
+  using C = Cfg;
+  int iss[CS], con[CS];
+  int hi_iss = 0, hi_con = 0;
+#pragma unroll
+  for (int r = 0; r < CS; ++r) {
+    if (CS > 1) {
+      iss[r] = (int)tc::ld_cluster_u32(tc::cluster_map(&sh.issued, (uint32_t)r));
+      con[r] = (int)tc::ld_cluster_u32(tc::cluster_map(&sh.consumed, (uint32_t)r));
+    } else {
+      iss[r] = sh.issued;
+      con[r] = sh.consumed;
+    }
+    hi_iss = max(hi_iss, iss[r]);
+    hi_con = max(hi_con, con[r]);
+  }
+  // copies into this CTA
+  for (int it = con[c]; it < hi_iss; ++it) {
+    const int st = it % C::STAGES;
+    const int t = it / kchunks;
+    const int nu = min(C::UNITS, u1 - (u0 + t * C::UNITS));
+    uint32_t sent = iss[c] > it ? (uint32_t)C::A_BYTES : 0u;   // this CTA's own hidden tile
+#pragma unroll
+    for (int r = 0; r < CS; ++r)
+      if (iss[r] > it) sent += share_bytes<CS>(r, nu);
+    if (iss[c] > it) {
+      const uint32_t armed = (uint32_t)C::A_BYTES + (uint32_t)nu * (uint32_t)(kUnit * kRowBytes);
+      if (armed > sent) tc::mbar_complete_tx(&sh.full[st], armed - sent);
+    } else {
+      tc::mbar_arrive_expect_tx(&sh.full[st], sent);
+    }
+    if (!tc::mbar_wait(&sh.full[st], (uint32_t)(it / C::STAGES) & 1u)) record_device_error(err, 112);
+  }
+  // MMA commits into this CTA's empty barriers (its producer waited for those of stages below
+  // issued[c] - STAGES)
+  for (int it = max(0, iss[c] - C::STAGES); it < hi_con; ++it) {
+    const int st = it % C::STAGES;
+    int n = 0;
+#pragma unroll
+    for (int r = 0; r < CS; ++r) n += con[r] > it;
+    if (n < CS) tc::mbar_arrive_count(&sh.empty[st], (uint32_t)(CS - n));
+    if (!tc::mbar_wait(&sh.empty[st], (uint32_t)(it / C::STAGES) & 1u)) record_device_error(err, 113);
+  }
 }
 
 // F8: E4M3 operands (the hidden rows quantised per row in the workspace, the FP8 weight cache) with
@@ -222,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool shape_ok = CS == 1 || tc::cluster_nctarank() == (uint32_t)CS;
   if (!shape_ok && threadIdx.x == 0) record_device_error(err, 111);
   const bool run = shape_ok && active != 0 && ntiles > 0;
+  const volatile int32_t *abort_flag = &sh.abort;       // set in every CTA of the cluster on a failure
 
   if (run) {
     if (warp == 0) {
@@ -230,14 +308,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_w = tc::policy_evict_first();
         const uint64_t pol_h = tc::policy_evict_last();
         int it = 0;
-        for (int t = 0; t < ntiles && !sh.abort; ++t) {
+        bool go = true;
+        for (int t = 0; t < ntiles && go; ++t) {
           const int tu0 = u0 + t * C::UNITS;
           const int nu = min(C::UNITS, u1 - tu0);
           const uint32_t bytes = (uint32_t)(kABox * kRowBytes + nu * kUnit * kRowBytes);
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int st = it % C::STAGES;
             const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-            if (!tc::mbar_wait(&sh.empty[st], ph ^ 1u)) { set_abort(sh, err, 101); break; }
+            if (*abort_flag || !tc::mbar_wait_or_abort(&sh.empty[st], ph ^ 1u, abort_flag)) {
+              if (!*abort_flag) set_abort<CS>(sh, err, 101, shape_ok);
+              go = false;
+              break;
+            }
             unsigned char *a = tiles + st * C::STAGE;
             unsigned char *w = a + C::A_BYTES;
             tc::mbar_arrive_expect_tx(&sh.full[st], bytes);
@@ -253,12 +336,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicExch(&sh.issued, it + 1);
           }
         }
-        if (CS > 1 && !sh.abort) {
+        if (CS > 1 && go) {
           // every CTA of the cluster has released every stage: no commit of theirs is still on its
-          // way to this CTA's barriers when it leaves
+          // way to this CTA's barriers when it leaves (after an abort the settlement does this)
           for (int i = 0; i < C::STAGES; ++i, ++it)
-            if (!tc::mbar_wait(&sh.empty[it % C::STAGES], ((uint32_t)(it / C::STAGES) & 1u) ^ 1u)) {
-              set_abort(sh, err, 110);
+            if (!tc::mbar_wait_or_abort(&sh.empty[it % C::STAGES], ((uint32_t)(it / C::STAGES) & 1u) ^ 1u,
+                                        abort_flag)) {
+              if (!*abort_flag) set_abort<CS>(sh, err, 110, shape_ok);
               break;
             }
         }
@@ -267,19 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- MMA issuer ----------------
       if (lane == 0) {
         int it = 0;
-        for (int t = 0; t < ntiles && !sh.abort; ++t) {
+        for (int t = 0; t < ntiles && !*abort_flag; ++t) {
           const int tu0 = u0 + t * C::UNITS;
           const int nu = min(C::UNITS, u1 - tu0);
           const uint32_t idesc =
               F8 ? tc::idesc_e4m3_f32(128, (uint32_t)(nu * kUnit)) : tc::idesc_bf16_f32(128, (uint32_t)(nu * kUnit));
           const int j = t & 1;
-          if (!tc::mbar_wait(&sh.acce[j], ((uint32_t)(t >> 1) & 1u) ^ 1u)) { set_abort(sh, err, 102); break; }
+          if (!tc::mbar_wait_or_abort(&sh.acce[j], ((uint32_t)(t >> 1) & 1u) ^ 1u, abort_flag)) {
+            if (!*abort_flag) set_abort<CS>(sh, err, 102, shape_ok);
+            break;
+          }
           tc::fence_after_sync();
           bool ok = true;
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int st = it % C::STAGES;
             const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-            if (!tc::mbar_wait(&sh.full[st], ph)) { set_abort(sh, err, 103); ok = false; break; }
+            if (*abort_flag || !tc::mbar_wait_or_abort(&sh.full[st], ph, abort_flag)) {
+              if (!*abort_flag) set_abort<CS>(sh, err, 103, shape_ok);
+              ok = false;
+              break;
+            }
             tc::fence_after_sync();
             const uint32_t a = tc::smem_u32(tiles + st * C::STAGE);
             const uint32_t w = a + C::A_BYTES;
@@ -316,7 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ncol = min(C::UNITS, u1 - tu0) * kUnit;
         const int v0 = tu0 * kUnit;
         const int j = t & 1;
-        if (!tc::mbar_wait(&sh.accf[j], (uint32_t)(t >> 1) & 1u)) { set_abort(sh, err, 105); ok = false; break; }
+        if (!tc::mbar_wait_or_abort(&sh.accf[j], (uint32_t)(t >> 1) & 1u, abort_flag)) {
+          if (lane == 0 && !*abort_flag) set_abort<CS>(sh, err, 105, shape_ok);
+          ok = false;
+          break;
+        }
         tc::fence_after_sync();
         if (any) {
           // 32 columns at a time, reduced without branches and merged into the row's statistics (every
@@ -348,11 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (sh.abort && threadIdx.x == 0) {
-    // copies issued but never consumed still land in this CTA's shared memory: wait for them
-    for (int it = sh.consumed; it < sh.issued; ++it)
-      tc::mbar_wait(&sh.full[it % C::STAGES], (uint32_t)(it / C::STAGES) & 1u);
-  }
+  // This CTA has stopped issuing copies and MMAs, and its MMAs are complete.  After the first cluster
+  // barrier every CTA of the cluster has stopped too, and an abort anywhere is visible everywhere, so
+  // either no CTA or every CTA settles.
+  if (CS > 1 && shape_ok) tc::cluster_sync();
+  if (*abort_flag && run && threadIdx.x == 0) settle_after_abort<CS>(sh, c, u0, u1, kchunks, err);
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
   if (CS > 1 && shape_ok) tc::cluster_sync();          // no CTA leaves while a peer may still address it
@@ -500,6 +595,8 @@ bool lmhead_tc_supported(const SelectProblem &p) {
   return p.in_bf16 && (int64_t)p.batch * p.B <= 512 && p.H % kChunk<false> == 0 &&
          (!p.fp8w || p.H % kChunk<true> == 0);
 }
+
+bool lmhead_tc_clustered(const SelectProblem &p) { return cluster_size(p) > 1; }
 
 int lmhead_tc_grid(const SelectProblem &p) {
   // vocabulary splits = clusters: as many as can be resident at once (one CTA per SM), at least one

@@ -5,9 +5,12 @@ Tolerances (decoding method: bf16 inputs, fp32 accumulation):
   * attention output: relative L2 error <= 5e-3 per (sequence, head);
   * confidence: absolute error <= 1e-3; kappa: |d kappa| <= 1e-3 * max(1, |kappa|) + 1e-3;
   * argmax token: bit-exact unless the oracle's top-2 logit gap is < 1e-2;
-  * unmask decision: bit-exact unless |c - tau| < 2e-3 at that position, or the step
-    fell back to one position and the two candidates' kappas are within the kappa
-    tolerance (a near tie).
+  * unmask decision: per sequence, the oracle's set, or a set the selection rule gives
+    when only exempt comparisons go the other way: a position with |c - tau| < 2e-3
+    (threshold), a factor comparison (n + 1)(1 - c_(n)) within (n + 1) 2e-3 of f, or a
+    ranking / fallback choice between positions whose kappas are within the kappa
+    tolerance (a near tie).  A wrong decision anywhere else fails, whatever its
+    neighbours are.
 """
 from __future__ import annotations
 
@@ -94,11 +97,74 @@ def kappa_tol(k):
     return 1e-3 * max(1.0, abs(k)) + 1e-3
 
 
+def _eps(k):
+    """1 - c from the log-odds kappa = log((1 - c) / c)."""
+    return 1.0 / (1.0 + math.exp(-k)) if k > -700 else 0.0
+
+
+def _rank_prefix_ok(kap, masked_idx, sel_idx):
+    """`sel_idx` is a most-confident prefix of the masked positions up to near ties of kappa: no
+    selected position is less confident than an unselected one by more than the kappa tolerance."""
+    rest = [i for i in masked_idx if i not in set(sel_idx)]
+    if not sel_idx or not rest:
+        return True
+    worst_in = max(kap[i] for i in sel_idx)
+    best_out = min(kap[i] for i in rest)
+    return worst_in <= best_out + kappa_tol(best_out)
+
+
+def threshold_selection_ok(conf, kap, masked_idx, sel_idx, tau):
+    """Can the threshold rule with the progress guarantee (unmask every masked c > tau; if none,
+    the single most confident) give `sel_idx`, when only positions with |c - tau| < TAU_EXEMPT may
+    fall on either side of tau and the fallback may pick any position tied with the least kappa?
+
+    Positions above the band must be selected and positions below it must not, so the selection is
+    either {above} plus some of the band, or -- only if nothing lies above the band -- a single
+    fallback pick among the near-tied most confident positions (or a single band position)."""
+    above = {i for i in masked_idx if conf[i] - tau >= TAU_EXEMPT}
+    band = {i for i in masked_idx if abs(conf[i] - tau) < TAU_EXEMPT}
+    sel = set(sel_idx)
+    if not masked_idx:
+        return not sel
+    if sel and above <= sel and sel <= above | band:
+        return True
+    if not above and len(sel) == 1:
+        (j,) = sel
+        kmin = min(kap[i] for i in masked_idx)
+        return kap[j] <= kmin + kappa_tol(kmin)
+    return False
+
+
+def factor_selection_ok(kap, masked_idx, sel_idx, factor):
+    """Can the factor rule (largest n with (n + 1)(1 - c_(n)) < f over the confidence order, at least
+    one) give `sel_idx`?  The selection must be a most-confident prefix (near ties of kappa aside), and
+    every n between its size and the oracle's count must have (n + 1)(1 - c_(n)) within
+    (n + 1) * TAU_EXEMPT of f: only such comparisons may fall on either side of f."""
+    if not masked_idx:
+        return not sel_idx
+    order = sorted(masked_idx, key=lambda i: (kap[i], i))
+    vals = [(n + 1) * _eps(kap[order[n - 1]]) for n in range(1, len(order) + 1)]
+    n_ref = max([n for n in range(1, len(order) + 1) if vals[n - 1] < factor] + [1])
+    n_got = len(sel_idx)
+    if n_got < 1 or not _rank_prefix_ok(kap, masked_idx, sel_idx):
+        return False
+    lo, hi = sorted((n_got, n_ref))
+    # n = 1 is never compared (at least one position is unmasked), so the band starts at n = 2
+    return all(abs(vals[n - 1] - factor) < (n + 1) * TAU_EXEMPT for n in range(max(lo + 1, 2), hi + 1))
+
+
 def compare_select(ref: dict, got: dict, tau: float, strategy="threshold", factor: float = 1.0):
     """Compare one step's GPU outputs with the oracle's `decode_step` info.
 
-    Returns the number of exempted positions; raises AssertionError on a mismatch
-    outside the tolerance bands."""
+    Per masked position: confidence within CONF_ATOL, kappa within kappa_tol, argmax token equal
+    unless the oracle's top-2 logit gap is below GAP_EXEMPT.  Per sequence, the unmask set must
+    equal the oracle's, or be one the selection rule can produce when only the comparisons the
+    contract exempts (|c - tau| < TAU_EXEMPT; a factor comparison within the same band; kappa near
+    ties in a ranking or fallback) go the other way (threshold_selection_ok, factor_selection_ok,
+    _rank_prefix_ok for top-k).
+
+    Returns the number of exempted positions (token differences plus unmask differences); raises
+    AssertionError on a mismatch outside the tolerance bands."""
     masked = ref["masked_before"]
     b, B = masked.shape
     exempt = 0
@@ -116,30 +182,19 @@ def compare_select(ref: dict, got: dict, tau: float, strategy="threshold", facto
         sel_g, sel_r = got["unmask"][bi], ref["unmask"][bi]
         if np.array_equal(sel_g, sel_r):
             continue
-        diff = np.nonzero(sel_g != sel_r)[0]
-        near_tau = [i for i in diff if abs(ref["conf"][bi, i] - tau) < TAU_EXEMPT]
-        if strategy == "threshold" and len(near_tau) == len(diff):
-            exempt += len(diff)
-            continue
-        # a fallback (or rank-based) pick between near-tied candidates
-        if sel_g.sum() == sel_r.sum():
-            kg = sorted(ref["kappa"][bi, np.nonzero(sel_g)[0]])
-            kr = sorted(ref["kappa"][bi, np.nonzero(sel_r)[0]])
-            if all(abs(x - y) <= kappa_tol(y) for x, y in zip(kg, kr)):
-                exempt += len(diff)
-                continue
+        midx = [int(i) for i in np.nonzero(masked[bi])[0]]
+        gidx = [int(i) for i in np.nonzero(sel_g)[0]]
+        assert set(gidx) <= set(midx), f"sequence {bi}: unmasked a position that was not masked"
+        conf, kap = ref["conf"][bi], ref["kappa"][bi]
         if strategy == "threshold":
-            # near-threshold flips change whether the step falls back; accept when the only
-            # disagreement is explained by positions within the tau band
-            if any(abs(ref["conf"][bi, i] - tau) < TAU_EXEMPT for i in np.nonzero(masked[bi])[0]):
-                exempt += len(diff)
-                continue
-        if strategy == "factor":
-            # the rule compares (n + 1) (1 - c_(n)) with f; a value within the confidence
-            # tolerance of f may fall on either side
-            eps = np.sort(1.0 - ref["conf"][bi, np.nonzero(masked[bi])[0]])
-            if any(abs((n + 2) * e - factor) < (n + 2) * TAU_EXEMPT for n, e in enumerate(eps)):
-                exempt += len(diff)
-                continue
-        raise AssertionError(f"sequence {bi}: unmask {np.nonzero(sel_g)[0]} vs oracle {np.nonzero(sel_r)[0]}")
+            ok = threshold_selection_ok(conf, kap, midx, gidx, tau)
+        elif strategy == "factor":
+            ok = factor_selection_ok(kap, midx, gidx, factor)
+        elif strategy == "topk":
+            ok = len(gidx) == int(sel_r.sum()) and _rank_prefix_ok(kap, midx, gidx)
+        else:
+            raise ValueError(strategy)
+        if not ok:
+            raise AssertionError(f"sequence {bi}: unmask {gidx} vs oracle {list(np.nonzero(sel_r)[0])}")
+        exempt += int(np.count_nonzero(sel_g != sel_r))
     return exempt

@@ -49,7 +49,7 @@ def one_step(*, batch, prompt_len, gen_length, block_size, block_idx, H, V, dtyp
     outs = SelectOutputs(desc, batch, block_size)
     outs.run(desc, dev(hid, dtype), w_dev, t_dev)
     got = outs.host()
-    compare_select(info, got, tau, strategy)
+    compare_select(info, got, tau, strategy, factor)
     t_got = t_dev.cpu().numpy()
     # tokens: only this step's unmasked positions changed, to the GPU's argmax
     changed = t_got != tokens

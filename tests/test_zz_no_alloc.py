@@ -81,6 +81,16 @@ def test_matches_the_workspace_entry_point_on_two_steps(dtype, batch, B, H, V):
             assert np.array_equal(a["n_left"], b["n_left"])
         assert b["unmasked"].sum() >= 1
     assert (t_new.cpu().numpy()[:, s:s + B] != V).sum() >= 2      # both steps unmasked something
+    # no device memory is taken by further calls (a stray cudaMalloc inside the library would not
+    # show in torch's allocator statistics, but it does in the device's free memory)
+    t_new.copy_(torch.from_numpy(tokens0).cuda())
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        F.fdllm_confidence_select_noalloc(desc, h_dev, w_dev, t_new, new["unmasked"], new["conf"], new["kappa"],
+                                          new["argmax"], new["n_left"])
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_rejects_requests_beyond_the_static_scratch():
