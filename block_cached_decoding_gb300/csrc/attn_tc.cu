@@ -8,29 +8,32 @@
 //
 // One CTA = (sequence, KV head, 128-row query tile, split of the key tiles);
 // all query heads sharing the KV head are packed into the 128 rows when
-// nq <= 128.  Within the CTA the key tiles are pipelined:
-//   warp 0     TMA: the query tile once, then K and V tiles into a ring
-//   warp 1     TMEM owner, MMA issuer: S_i = Q K_i^T (M=128, N=64 keys,
-//              K=d) into one of two TMEM score buffers, then PV_i = P_i V_i
-//              (N=d, K=64 keys, V read MN-major) into one of two TMEM
-//              buffers; S_{i+1} is issued before PV_i; the K/V ring holds
-//              4 tiles (d = 128) so loads run ahead of the MMAs
-//   warps 4-11 two threads per query row (warps w and w + 4 share a TMEM lane
-//              quadrant and split the key and output columns; they exchange
-//              the half-row maxima through shared memory under a barrier of
-//              the two warps only), online softmax in base 2 with a lazy
-//              reference max: P_i = 2^(S_i - m_ref) is written as bf16 (128-byte
-//              swizzle) into one of two P buffers and the tensor core
-//              accumulates O += P_i V_i in TMEM.  m_ref moves only when a row's
-//              max exceeds it by more than 2^8; then that row of O (and l) is
-//              rescaled in TMEM once the previous PV product has landed.
-//              Tile i+1's softmax runs while the tensor core computes PV_i.
-// Splits of one unit form a thread block cluster (<= 8) and merge through
-// distributed shared memory with stores only, between two cluster barriers:
-// every CTA writes each of its O rows, unnormalised, with the row's (max, l)
-// into the CTA that owns the row (CTA c owns rows [c R/C, (c+1) R/C)), and each
-// owner combines the C copies of its rows with weights 2^(m_c - M) / L and
-// writes them.
+// nq <= 128.  Both operands that are reused across a tile's MMAs live in tensor
+// memory, so the tensor core reads only K and V from shared memory:
+//   TMEM   Q (128 rows x d bf16, written once), S0 / S1 (64 fp32 score columns
+//          each), P0 / P1 (the probabilities as bf16 pairs), O0 / O1 (d fp32
+//          columns each)
+//   warp 0     TMA: the query tile once (into the last ring stage), then K and
+//              V tiles into a 6-stage ring (d = 128; 8 stages at d = 64)
+//   warp 1     TMEM owner, MMA issuer: S_i = Q K_i^T (M=128, N=64 keys, K=d,
+//              A from TMEM) and O_g += P_i V_i (N=d, K=64 keys, P from TMEM, V
+//              read MN-major), each issued as soon as its inputs are ready
+//   warps 2-3  FP8 KV cache only: cache K tiles from E4M3 codes to bf16
+//   warps 4-7  softmax group 0: the even key tiles; warps 8-11 group 1: the odd
+//              ones.  One thread per query row holds the tile's whole score row:
+//              row max, lazy reference max (it moves only when a row's max
+//              exceeds it by more than 2^8, and then O_g's row and l are
+//              rescaled in TMEM after the group's previous PV product has
+//              landed), P = 2^((S - m_ref) * scale * log2 e) stored as bf16 to
+//              TMEM.  Each group keeps its own (m, l, O_g); while one group
+//              computes its softmax the tensor core works on the other's tile.
+// At the end the two groups' rows are combined in the CTA.  Splits of one unit
+// form a thread block cluster (<= 8) and merge through distributed shared
+// memory: every CTA stages its rows, unnormalised, with the row's (max, sum) in
+// its own shared memory, grouped by the CTA that owns each row (CTA c owns rows
+// [c R/C, (c+1) R/C)), then sends each group to its owner with one bulk copy
+// whose bytes complete on the owner's mbarrier; each owner combines the C copies
+// of its rows with weights 2^(m_c - M) / L and writes them.
 //
 // K/V maps view [b, N, Hkv, d] as (d, position, head, b), so one box brings a
 // tile half's keys of all heads packed in the tile, head-major.
@@ -39,10 +42,10 @@
 // per (sequence, position, KV head) row.  A cache tile is loaded as bytes into
 // the V half of its ring stage; warps 2-3 (one thread per key row) turn the K
 // codes into the bf16 K tile TMA would have written -- code * scale is exact in
-// bf16 -- and release it to the MMA issuer; the softmax warps turn the V codes
-// into the bf16 V tile at the start of the tile's softmax.  The products and the
-// softmax arithmetic are unchanged.  Fresh K/V tiles are loaded as bf16 directly.
-#include <cooperative_groups.h>
+// bf16 -- and release it to the MMA issuer; the softmax group of the tile turns
+// the V codes into the bf16 V tile after the tile's scores are done.  The
+// products and the softmax arithmetic are unchanged.  Fresh K/V tiles are loaded
+// as bf16 directly.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -55,7 +58,7 @@
 namespace fdllm {
 namespace {
 
-constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, FP8 K conversion (2, 3); 4-11: softmax (two per quadrant)
+constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, FP8 K conversion (2, 3); 4-11: two softmax groups
 constexpr int kTile = 128;       // rows per query tile
 constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
@@ -79,42 +82,51 @@ struct Plan {
 template <int D>
 struct Cfg {
   static constexpr int DH = D / 64;                   // 64-column halves of a row
-  static constexpr int Q_BYTES = kTile * D * 2;       // 128 query rows x d bf16
   static constexpr int QHALF = kTile * 128;           // 128 rows x 64 bf16
   static constexpr int KV_BYTES = kKeys * D * 2;      // 64 key rows x d bf16
   static constexpr int KVHALF = kKeys * 128;          // 64 rows x 64 bf16
-  static constexpr int P_BYTES = kTile * kKeys * 2;   // 128 rows x 64 keys bf16 (one swizzle atom column)
   static constexpr int STAGE = 2 * KV_BYTES;          // K + V
-  static constexpr int NS = D == 128 ? 4 : 8;         // K/V ring stages
-  // cluster merge: the O rows an owner receives, C * ceil(128 / C) <= 136 of them, fp32 with a row
-  // pitch of D + 4 floats (a column written by 8 consecutive rows falls in 8 different banks), then
-  // each received row's (max, l), then its combination weight
+  static constexpr int NS = D == 128 ? 7 : 8;         // K/V ring stages
+  static_assert(kTile * D * 2 <= STAGE, "the query tile is staged in one ring stage");
+  // split merge: rows of D fp32 values, then the row's max (log2 units) and sum, then the row's
+  // weight; the pitch keeps every row 16-byte aligned.  A send area (every row of the CTA, grouped by
+  // owner) and a receive area (C copies of the rows this CTA owns), C * ceil(128 / C) <= 136 rows each.
+  static constexpr int RP = D + 4;
   static constexpr int MERGE_ROWS = 136;
-  static constexpr int DP = D + 4;
-  static constexpr int MERGE_BYTES = MERGE_ROWS * DP * 4 + MERGE_ROWS * 8 + MERGE_ROWS * 4;
+  static constexpr int MERGE_BYTES = 2 * MERGE_ROWS * RP * 4;
   static constexpr int RING = NS * STAGE > MERGE_BYTES ? NS * STAGE : MERGE_BYTES;
-  static constexpr int SMEM = Q_BYTES + RING + 2 * P_BYTES + 1024 + 4096;   // + alignment + Bars
-  static constexpr uint32_t S_COL = 0;                // TMEM: S0, S1 (64 columns each), then O (D columns)
-  static constexpr uint32_t O_COL = 2 * kKeys;
-  static constexpr uint32_t TMEM_COLS = 256;
+  // after the pipeline the ring also holds the output tile (one 128-row block of 128 bytes per 64 bf16 or
+  // 32 fp32 columns, 128-byte swizzle) and, at its end, the two groups' (max, sum) per row
+  static constexpr int OUT_BYTES = kTile * D * 4;
+  static constexpr int ML_OFF = RING - 2 * kTile * 8;
+  static_assert(MERGE_BYTES <= ML_OFF && OUT_BYTES <= ML_OFF, "ring areas after the pipeline");
+  static constexpr int SMEM = RING + 1024 + 512;    // + alignment + Bars
+  // TMEM columns
+  static constexpr uint32_t Q_COL = 0;               // D / 2 columns of bf16 pairs
+  static constexpr uint32_t S_COL = D / 2;           // S0, S1: 64 fp32 columns each
+  static constexpr uint32_t P_COL = D / 2 + 128;     // P0, P1: 32 columns (64 bf16) each
+  static constexpr uint32_t O_COL = D / 2 + 192;     // O0, O1: D fp32 columns each
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(O_COL + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
 struct Bars {
-  uint64_t qfull, kvfull[8], kvempty[8], sfull[2], sempty[2], pfull[2], pvdone, drain;
-  uint64_t raw[8];     // F8KV: a cache tile's codes have landed (the converters then complete kvfull)
+  uint64_t qfull, qtmem, kvfull[8], kvempty[8], raw[8], sfull[2], sempty[2], pfull[2], pvdone[2], drain, mrg;
   uint32_t tmem_base;
-  int32_t cvt_stop;   // F8KV: the converters stop (written before, read between their two barriers)  // (the whole struct must fit the 4096 bytes reserved after the P buffers)
+  int32_t cvt_stop;   // F8KV: the converters stop (written before, read between their two barriers)
   int32_t abort;
   int32_t issued;     // K/V tiles issued by the producer
-  int32_t consumed;   // K/V tiles whose arrival the MMA issuer waited for
-  float rowmax[2][2][kTile];  // [tile parity][column half][row] half-row maxima
-  float lhalf[2][kTile];      // [column half][row] partial softmax denominators
+  int32_t consumed_g[2];   // per group: key tiles whose arrival its MMA issuer waited for
 };
 
 // The 256 softmax threads (warps 4-11) synchronise among themselves.
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The two softmax warps of TMEM lane quadrant q (warps 4 + q and 8 + q) synchronise as a pair.
 __device__ __forceinline__ void quadrant_bar(int q) { asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory"); }
+// The two FP8 conversion warps synchronise among themselves.
+__device__ __forceinline__ void convert_bar() { asm volatile("bar.sync 6, 64;" ::: "memory"); }
+// The four warps of softmax group g.
+__device__ __forceinline__ void group_bar(int g) { asm volatile("bar.sync %0, 128;" ::"r"(7 + g) : "memory"); }
 
 struct KeyTile {
   int range;   // 0 prefix cache, 1 fresh, 2 suffix cache
@@ -148,9 +160,6 @@ struct Args {
   int prompt_len, nblocks;
   const float *k_scale, *v_scale;   // F8KV: scales of the cached rows [b, N, Hkv]
 };
-
-// The two FP8 conversion warps synchronise among themselves.
-__device__ __forceinline__ void convert_bar() { asm volatile("bar.sync 6, 64;" ::: "memory"); }
 
 // 4 E4M3 codes (one 32-bit word) times `sc` as 4 bf16 (two words); exact: an E4M3 value has at most
 // 4 significant bits and `sc` is a power of two.
@@ -214,21 +223,54 @@ __device__ __forceinline__ bool row_target(const Plan &pl, int nq, int nh, int q
   return hs < nh && qi < nq;
 }
 
-static_assert(sizeof(Bars) <= 4096, "Bars must fit its shared-memory reservation");
+// D / 2 values as bf16 (8 per 16-byte chunk) or fp32 (4 per chunk) at `dst`.
+template <int N>
+__device__ __forceinline__ void store_row_part(void *dst, bool f32, const float (&v)[N], float inv) {
+  if (f32) {
+    float4 *o = (float4 *)dst;
+#pragma unroll
+    for (int c = 0; c < N / 4; ++c) o[c] = make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
+  } else {
+    uint4 *o = (uint4 *)dst;
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * c + 2 * e] * inv, v[8 * c + 2 * e + 1] * inv);
+        w[e] = *(uint32_t *)&h2;
+      }
+      o[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+static_assert(sizeof(Bars) <= 512, "Bars must fit its shared-memory reservation");
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
 
 template <int D, int KVP, bool F8KV>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
                    const __grid_constant__ CUtensorMap mva, const __grid_constant__ CUtensorMap mvf,
-                   const __grid_constant__ CUtensorMap mvc, const Args a) {
+                   const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mo, const Args a) {
   using CF = Cfg<D>;
   constexpr int NS = CF::NS;
+  constexpr int TK = kKeys / KVP;                      // keys of one KV head in a key tile
   extern __shared__ unsigned char smem_raw[];
-  unsigned char *q_s = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char *kv_s = q_s + CF::Q_BYTES;              // NS stages of (K tile, V tile)
-  unsigned char *p_s = kv_s + CF::RING;                 // 2 P buffers
-  Bars &br = *(Bars *)(p_s + 2 * CF::P_BYTES);
+  unsigned char *kv_s = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);   // NS stages
+  unsigned char *q_s = kv_s + (NS - 1) * CF::STAGE;    // the query tile, until it is in TMEM
+  Bars &br = *(Bars *)(kv_s + CF::RING);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Plan pl = a.pl;   // per-sequence blocks fill in this CTA's ranges after the dependency wait
 
@@ -236,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit = blockIdx.x / pl.nsplit;
   const int nkvg = a.hkv / KVP;                        // KV head groups
   const int qt = unit % pl.nqt;
-  const int kvh = ((unit / pl.nqt) % nkvg) * KVP;        // first KV head of this tile
+  const int kvh = ((unit / pl.nqt) % nkvg) * KVP;      // first KV head of this tile
   const int b = unit / (pl.nqt * nkvg);
   int h0, nh, q0;
   if (KVP > 1) {
@@ -246,30 +288,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     h0 = qt / pl.qtiles_per_head; nh = 1; q0 = (qt % pl.qtiles_per_head) * kTile;
   }
+  const int C = pl.nsplit;                             // CTAs of this unit's cluster
+  const int rpc = (kTile + C - 1) / C;                 // rows owned per CTA in the split merge
+  const uint32_t seg_bytes = (uint32_t)(rpc * CF::RP * 4);   // one owner's rows, as sent
 
   if (threadIdx.x == 0) {
-    br.abort = 0; br.issued = 0; br.consumed = 0; br.cvt_stop = 0;
+    br.abort = 0; br.issued = 0; br.consumed_g[0] = 0; br.consumed_g[1] = 0; br.cvt_stop = 0;
     tc::mbar_init(&br.qfull, 1);
-    for (int i = 0; i < NS; ++i) { tc::mbar_init(&br.kvfull[i], 1); tc::mbar_init(&br.kvempty[i], 1); }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&br.sfull[i], 1);
-      tc::mbar_init(&br.sempty[i], 8);
-      tc::mbar_init(&br.pfull[i], 8);
+    tc::mbar_init(&br.qtmem, 4);
+    for (int i = 0; i < NS; ++i) {
+      tc::mbar_init(&br.kvfull[i], 1);
+      tc::mbar_init(&br.kvempty[i], 1);
+      tc::mbar_init(&br.raw[i], 1);
     }
-    tc::mbar_init(&br.pvdone, 1);
-    tc::mbar_init(&br.drain, 1);
-    for (int i = 0; i < NS; ++i) tc::mbar_init(&br.raw[i], 1);
+    for (int g = 0; g < 2; ++g) {
+      tc::mbar_init(&br.sfull[g], 1);
+      tc::mbar_init(&br.sempty[g], 4);
+      tc::mbar_init(&br.pfull[g], 4);
+      tc::mbar_init(&br.pvdone[g], 1);
+    }
+    tc::mbar_init(&br.drain, F8KV ? 1 : 2);          // one arrival per MMA issuer
+    tc::mbar_init(&br.mrg, 1);
     tc::fence_barrier_init();
+    // the merge barrier expects the other C - 1 CTAs' rows of this one
+    if (C > 1) tc::mbar_arrive_expect_tx(&br.mrg, (uint32_t)(C - 1) * seg_bytes);
+    for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc, &mo}) tc::prefetch_tensormap(m);
   }
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
-  if (threadIdx.x == 0) {
-    for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc}) tc::prefetch_tensormap(m);
-  }
-  if (KVP > 1) {
-    // each row writes only its own head's block of a P tile: the rest stays zero
-    for (int i = threadIdx.x; i < 2 * CF::P_BYTES / 16; i += kThreads) ((uint4 *)p_s)[i] = make_uint4(0u, 0u, 0u, 0u);
-    tc::fence_proxy_async_smem();
-  }
   // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
   // stream, which may produce q, the caches or the fresh K/V (or still read the output).
   tc::pdl_wait_primary();
@@ -296,16 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int k0 = (int)((int64_t)pl.kt * split / pl.nsplit);
   const int nt = (int)((int64_t)pl.kt * (split + 1) / pl.nsplit) - k0;
-
-  // thread of the softmax warps: its query row, column half and running state (reference max, l)
-  const int r = (warp & 3) * 32 + lane;
-  const int half = (warp - 4) >> 2;
-  float m_run = kNegInf, l_run = 0.f;
   // set by the first wait that gives up (fail()); every later wait that polls it returns at once
   const volatile int32_t *abort_flag = &br.abort;
 
+  // thread of the softmax groups: its query row, group and running state
+  const int g = (warp - 4) >> 2;                       // softmax group (warps >= 4)
+  const int r = (warp & 3) * 32 + lane;
+  float m_run = kNegInf, l_run = 0.f;
+  bool ok = true;
+
   if (warp == 0) {
     if (lane == 0) {
+      // ---------------- TMA producer ----------------
       const uint64_t pol_q = tc::policy_evict_last();
       const uint64_t pol_kv = tc::policy_evict_first();
       tc::mbar_arrive_expect_tx(&br.qfull, (uint32_t)(pl.qr * 128 * CF::DH * nh));
@@ -313,8 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int dh = 0; dh < CF::DH; ++dh)
           tc::tma_load_4d(q_s + dh * CF::QHALF + hs * pl.qr * 128, &mq, &br.qfull, dh * 64,
                           kvh * a.group + h0 + hs, q0, b, pol_q);
-      for (int i = 0; i < nt && !br.abort; ++i) {
+      for (int i = 0; i < nt && !*abort_flag; ++i) {
         const int st = i % NS;
+        // the last stage holds the query tile until group 0 has copied it into TMEM
+        if (i == NS - 1 && !tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag)) {
+          if (!*abort_flag) fail(br, a.err, 210);
+          break;
+        }
         if (!tc::mbar_wait_or_abort(&br.kvempty[st], ((uint32_t)(i / NS) & 1u) ^ 1u, abort_flag)) {
           if (!*abort_flag) fail(br, a.err, 211);
           break;
@@ -341,56 +393,117 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicExch(&br.issued, i + 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (!F8KV && (warp == 1 || warp == 2)) {
     if (lane == 0) {
+      // ---------------- MMA issuers, one per softmax group ----------------
+      // Warp 1 serves group 0 (the even key tiles), warp 2 group 1 (the odd ones).  Each issues its
+      // group's S_j = Q K_j^T as soon as the tile has landed and the group has read S_{j-2} from its
+      // score buffer, and O_g += P_i V_i as soon as the group has stored P_i, whichever is ready first
+      // (a PV first when both are), so the two groups' products never wait on each other's issue.
+      const int gg = warp - 1;
       const uint32_t id_s = tc::idesc_bf16_f32(128, kKeys, 0);
       const uint32_t id_o = tc::idesc_bf16_f32(128, D, 1);
-      const uint32_t qa = tc::smem_u32(q_s);
-      bool ok = tc::mbar_wait_or_abort(&br.qfull, 0, abort_flag);
-      if (!ok && !*abort_flag) fail(br, a.err, 212);
-      auto issue_s = [&](int i) -> bool {
-        const int st = i % NS, j = i & 1;
-        if (!tc::mbar_wait_or_abort(&br.kvfull[st], (uint32_t)(i / NS) & 1u, abort_flag)) {
-          if (!*abort_flag) fail(br, a.err, 213);
-          return false;
-        }
-        atomicExch(&br.consumed, i + 1);
-        if (!tc::mbar_wait_or_abort(&br.sempty[j], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag)) {
-          if (!*abort_flag) fail(br, a.err, 214);
-          return false;
-        }
-        tc::fence_after_sync();
-        const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
+      bool run = tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag);    // Q is in TMEM
+      if (!run && !*abort_flag) fail(br, a.err, 212);
+      int js = gg, jp = gg;                             // next S, next PV of this group
+      uint64_t t0 = tc::globaltimer();
+      for (uint32_t spin = 0; run && jp < nt; ++spin) {
+        if (jp < js && tc::mbar_test_wait(&br.pfull[gg], (uint32_t)(jp >> 1) & 1u)) {
+          const int st = jp % NS;
+          tc::fence_after_sync();
+          const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t kin = (uint32_t)((ks % 4) * 32);
-          tc::mma_bf16(tmem + CF::S_COL + (uint32_t)(j * kKeys), tc::sw128_desc(qa + (ks / 4) * CF::QHALF + kin),
-                       tc::sw128_desc(ka + (ks / 4) * CF::KVHALF + kin), id_s, ks != 0);
+          for (int ks = 0; ks < kKeys / 16; ++ks)
+            tc::mma_bf16_ts(tmem + CF::O_COL + (uint32_t)(gg * D), tmem + CF::P_COL + (uint32_t)(gg * 32 + ks * 8),
+                            tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::KVHALF), id_o, (jp >= 2) || ks != 0);
+          tc::mma_commit(&br.pvdone[gg]);
+          tc::mma_commit(&br.kvempty[st]);
+          jp += 2;
+          t0 = tc::globaltimer();
+          continue;
         }
-        tc::mma_commit(&br.sfull[j]);
-        return true;
-      };
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % NS, j = i & 1;
-        if (!tc::mbar_wait_or_abort(&br.pfull[j], (uint32_t)(i >> 1) & 1u, abort_flag)) {
-          if (!*abort_flag) fail(br, a.err, 215);
-          return false;
-        }
-        tc::fence_after_sync();
-        const uint32_t pa = tc::smem_u32(p_s + j * CF::P_BYTES);
-        const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
+        if (js < nt && tc::mbar_test_wait(&br.kvfull[js % NS], (uint32_t)(js / NS) & 1u) &&
+            tc::mbar_test_wait(&br.sempty[gg], ((uint32_t)(js >> 1) & 1u) ^ 1u)) {
+          const int st = js % NS;
+          tc::fence_after_sync();
+          const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
 #pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks)
-          tc::mma_bf16(tmem + CF::O_COL, tc::sw128_desc(pa + (uint32_t)(ks * 32)),
-                       tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::KVHALF), id_o, (i | ks) != 0);
-        tc::mma_commit(&br.pvdone);
-        tc::mma_commit(&br.kvempty[st]);
-        return true;
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc::mma_bf16_ts(tmem + CF::S_COL + (uint32_t)(gg * kKeys), tmem + CF::Q_COL + (uint32_t)(ks * 8),
+                            tc::sw128_desc(ka + (ks / 4) * CF::KVHALF + (uint32_t)((ks % 4) * 32)), id_s, ks != 0);
+          tc::mma_commit(&br.sfull[gg]);
+          js += 2;
+          atomicExch(&br.consumed_g[gg], js >> 1);
+          t0 = tc::globaltimer();
+          continue;
+        }
+        if ((spin & 63u) == 0) {
+          if (*abort_flag) break;
+          if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
+            fail(br, a.err, jp < js ? 215 : 213);
+            break;
+          }
+        }
+      }
+      tc::mma_commit(&br.drain);                        // both issuers arrive: count 2
+      if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
+    }
+  } else if (F8KV && warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer (FP8 cache: one thread for both groups) ----------------
+      // S_j and PV_i are issued in whatever order their inputs become ready (a PV first when both
+      // are): S_j needs its K/V tile and the group's score buffer (released when the group has read
+      // S_{j-2}); PV_i needs the group's P_i.  The thread sleeps in mbarrier try_wait (with a short
+      // time hint) on the input it expects next, rather than spinning on the issue slots the softmax
+      // warps of its sub-partition need.
+      const uint32_t id_s = tc::idesc_bf16_f32(128, kKeys, 0);
+      const uint32_t id_o = tc::idesc_bf16_f32(128, D, 1);
+      bool run = tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag);    // Q is in TMEM
+      if (!run && !*abort_flag) fail(br, a.err, 212);
+      int js = 0, jp = 0;                               // next S, next PV
+      uint64_t t0 = tc::globaltimer();
+      auto s_ready = [&]() {
+        return tc::mbar_test_wait(&br.kvfull[js % NS], (uint32_t)(js / NS) & 1u) &&
+               tc::mbar_test_wait(&br.sempty[js & 1], ((uint32_t)(js >> 1) & 1u) ^ 1u);
       };
-      if (ok && nt > 0) ok = issue_s(0);
-      for (int i = 0; i < nt && ok; ++i) {
-        if (i + 1 < nt && !issue_s(i + 1)) break;
-        if (!issue_pv(i)) break;
+      for (uint32_t spin = 0; run && jp < nt; ++spin) {
+        if (jp < js && tc::mbar_try_wait_hint(&br.pfull[jp & 1], (uint32_t)(jp >> 1) & 1u, js < nt ? 200u : 2000u)) {
+          const int st = jp % NS, gg = jp & 1;
+          tc::fence_after_sync();
+          const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks)
+            tc::mma_bf16_ts(tmem + CF::O_COL + (uint32_t)(gg * D), tmem + CF::P_COL + (uint32_t)(gg * 32 + ks * 8),
+                            tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::KVHALF), id_o, (jp >= 2) || ks != 0);
+          tc::mma_commit(&br.pvdone[gg]);
+          tc::mma_commit(&br.kvempty[st]);
+          ++jp;
+          t0 = tc::globaltimer();
+          continue;
+        }
+        if (js < nt && (s_ready() || (jp >= js && tc::mbar_try_wait_hint(&br.kvfull[js % NS],
+                                                                          (uint32_t)(js / NS) & 1u, 2000u) &&
+                                       s_ready()))) {
+          const int st = js % NS, gg = js & 1;
+          tc::fence_after_sync();
+          const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            tc::mma_bf16_ts(tmem + CF::S_COL + (uint32_t)(gg * kKeys), tmem + CF::Q_COL + (uint32_t)(ks * 8),
+                            tc::sw128_desc(ka + (ks / 4) * CF::KVHALF + (uint32_t)((ks % 4) * 32)), id_s, ks != 0);
+          tc::mma_commit(&br.sfull[gg]);
+          atomicExch(&br.consumed_g[js & 1], (js >> 1) + 1);
+          ++js;
+          t0 = tc::globaltimer();
+          continue;
+        }
+        if ((spin & 15u) == 0) {
+          if (*abort_flag) break;
+          if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
+            fail(br, a.err, jp < js ? 215 : 213);
+            break;
+          }
+        }
       }
       tc::mma_commit(&br.drain);
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
@@ -408,12 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return j;
     };
     auto load_scale = [&](int j) -> float {
-      return j < nt ? cache_scale(a, pl, key_tile(pl, a.nq, a.n, k0 + j), b, kvh, r, a.k_scale) : 0.f;
+      if (j >= nt) return 0.f;
+      const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + j);
+      return (r % pl.tk) < kt.nvalid ? cache_scale(a, pl, kt, b, kvh, r, a.k_scale) : 0.f;
     };
     int inext = next_cache_tile(0);
     float ksn = load_scale(inext);
     for (int i = inext; i < nt; i = inext) {
       const float ksc = ksn;
+      const bool valid = (r % pl.tk) < key_tile(pl, a.nq, a.n, k0 + i).nvalid;
       inext = next_cache_tile(i + 1);
       ksn = load_scale(inext);
       const int st = i % NS;
@@ -428,281 +544,385 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char *ks = kv_s + st * CF::STAGE;
       uint4 codes[D / 16];
       load_code_row<D>(ks + CF::KV_BYTES + r * D, r, codes);
+      if (!valid) {                                    // a row outside the sequence's key range: zeros
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) codes[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
       store_bf16_row<D>(ks, r, codes, ksc);            // K: codes in the V half, bf16 into the K half
       tc::fence_proxy_async_smem();
       convert_bar();
-      if (r == 0) tc::mbar_arrive(&br.kvfull[st]);     // V is converted by the softmax warps
+      if (r == 0) tc::mbar_arrive(&br.kvfull[st]);     // V is converted by the tile's softmax group
     }
   } else if (warp >= 4) {
-    constexpr int DHALF = D / 2;
+    // Every softmax warp runs every tile of its group and meets every named barrier the same number of
+    // times, whatever its waits return: a wait that gives up only marks this thread's result invalid
+    // (ok = false), records the site and raises the abort flag, after which every wait of the CTA
+    // returns at once.  So no warp can be left waiting at a named barrier for a partner that has left.
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t oa = tmem + lane_base + CF::O_COL + (uint32_t)(half * DHALF);   // this thread's O columns
-    // Every softmax warp runs every tile and meets every named barrier (the pair's quadrant barrier,
-    // the 256-thread softmax barrier) the same number of times, whatever its waits return: a wait that
-    // gives up only marks this thread's result invalid (ok = false), records the site and raises the
-    // abort flag, after which every wait of the CTA returns at once.  So no warp can be left waiting
-    // at a named barrier for a partner that has left the loop.
-    bool ok = true;
-    // wait until PV_i has been accumulated into O (phases complete in order, one per tile)
-    auto wait_pv = [&](int i) {
-      if (!tc::mbar_wait_or_abort(&br.pvdone, (uint32_t)i & 1u, abort_flag)) {
-        if (!*abort_flag) fail(br, a.err, 219);
+    const int gt = threadIdx.x - 128 - 128 * g;        // thread index within the group
+    const int slot = KVP > 1 ? r / pl.qr : 0;         // KVP > 1: this row's head slot (uniform per warp)
+    const uint32_t s_col = tmem + lane_base + CF::S_COL + (uint32_t)(g * kKeys + slot * TK);
+    const uint32_t p_col = tmem + lane_base + CF::P_COL + (uint32_t)(g * 32);
+    const uint32_t o_col = tmem + lane_base + CF::O_COL + (uint32_t)(g * D);
+    if (g == 0) {
+      // the query tile into TMEM: row r as D / 2 columns of bf16 pairs (rows of absent head slots: zeros)
+      if (!tc::mbar_wait_or_abort(&br.qfull, 0, abort_flag)) {
+        if (!*abort_flag) fail(br, a.err, 216);
         ok = false;
       }
-      tc::fence_after_sync();
+      const bool qvalid = pl.qtiles_per_head != 0 || r < nh * pl.qr;
+#pragma unroll
+      for (int dh = 0; dh < CF::DH; ++dh) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = qvalid ? *(const uint4 *)(q_s + dh * CF::QHALF + r * 128 + ((c ^ (r & 7)) * 16))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+        }
+        tc::tmem_st_32x32b_x32(tmem + lane_base + CF::Q_COL + (uint32_t)(dh * 32), w);
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&br.qtmem);
+    }
+    if (KVP > 1) {
+      // each row writes only its head's block of P: the rest of its P row stays zero
+      uint32_t z[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) z[e] = 0u;
+      tc::tmem_st_32x32b_x32(p_col, z);
+      tc::tmem_st_wait();
+    }
+    const float sl2 = a.scale_log2;
+    // F8KV: phase parity of raw[st] for tile i (the cache tiles loaded into its stage before it)
+    auto raw_phase = [&](int i) -> uint32_t {
+      int uses = 0;
+      for (int j = i % NS; j < i; j += NS) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
+      return (uint32_t)uses & 1u;
     };
-    // softmax of tile i over this thread's 32 key columns: P_i = 2^((S_i - m_ref) * scale * log2 e)
-    uint32_t vrawpar = 0;                            // F8KV: bit st, parity of raw[st]'s next phase
-    auto softmax = [&](int i) {
-      const int j = i & 1;
-      // F8KV: the 256 softmax threads also turn a cache tile's V codes into bf16 (thread t: a quarter of
-      // key row t / 4).  S_i is done, so the converters have read this tile's K codes, which the bf16 V
-      // rows overwrite; P_i's release (below) covers these writes too.
-      const bool cvt_v = F8KV && key_tile(pl, a.nq, a.n, k0 + i).range != 1;
-      const int vt = threadIdx.x - 128, vr = vt >> 2, vq = vt & 3;
-      float vsc = 0.f;
-      if (F8KV && cvt_v) vsc = cache_scale(a, pl, key_tile(pl, a.nq, a.n, k0 + i), b, kvh, vr, a.v_scale);
-      if (!tc::mbar_wait_or_abort(&br.sfull[j], (uint32_t)(i >> 1) & 1u, abort_flag)) {
+    int u = 0;                                         // this group's tile count
+    for (int i = g; i < nt; i += 2, ++u) {
+      const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + i);
+      const int nv = kt.nvalid;
+      const int st = i % NS;
+      if (!tc::mbar_wait_or_abort(&br.sfull[g], (uint32_t)u & 1u, abort_flag)) {
         if (!*abort_flag) fail(br, a.err, 218);
         ok = false;
       }
       tc::fence_after_sync();
-      if constexpr (F8KV) {
-        if (cvt_v) {
-          constexpr int QC = D / 64;                   // 16-code chunks per quarter row
-          const int st = i % NS;
-          // the codes' arrival, for this thread: complete long ago (the converters waited for it), and
-          // raw[st] cannot move on before this tile's P is released
-          if (!tc::mbar_wait_or_abort(&br.raw[st], (vrawpar >> st) & 1u, abort_flag)) ok = false;
-          vrawpar ^= 1u << st;
-          unsigned char *vh = kv_s + st * CF::STAGE + CF::KV_BYTES;
-          uint4 cq[QC];
+      // The tile's V (its K codes were consumed before S_i): FP8 codes into bf16 (cache tiles), or zeros
+      // over rows outside the sequence's key range (per-sequence blocks read window rows at the edge of
+      // the prefix; they must not reach the product even as 0 * inf).  Thread gt handles half (vh) of
+      // key row vr.
+      const bool cvt = F8KV && kt.range != 1;
+      const bool zero_rows = !cvt && a.blocks != nullptr && kt.range == 0 && nv < pl.tk;
+      if (cvt || zero_rows) {
+        const int vr = gt >> 1, vh = gt & 1;
+        const bool rvalid = (vr % pl.tk) < nv;
+        unsigned char *vt = kv_s + st * CF::STAGE + CF::KV_BYTES;
+        constexpr int HB = D / 2;                      // bf16 values (and codes) per half row
+        uint32_t w[HB / 2];
+        if constexpr (F8KV) {
+          if (cvt) {
+            // the codes' arrival, for this thread: complete long ago (the converters waited for it, and
+            // the tile's scores are done), and raw[st] cannot move on before this tile's P is released
+            if (!tc::mbar_wait_or_abort(&br.raw[st], raw_phase(i), abort_flag)) ok = false;
+            const float vsc = rvalid ? cache_scale(a, pl, kt, b, kvh, vr, a.v_scale) : 0.f;
+            uint4 cq[HB / 16];
 #pragma unroll
-          for (int c = 0; c < QC; ++c) cq[c] = *(const uint4 *)(vh + kKeys * D + vr * D + (vq * QC + c) * 16);
-          softmax_bar();                               // every V code of the tile has been read
+            for (int c = 0; c < HB / 16; ++c)
+              cq[c] = *(const uint4 *)(vt + kKeys * D + vr * D + vh * HB + c * 16);
+            group_bar(g);                              // every V code of the tile has been read
 #pragma unroll
-          for (int c = 0; c < QC; ++c) {
-            const int cc = vq * QC + c;
-            const uint2 x0 = e4m3x4_to_bf16x4(cq[c].x, vsc), x1 = e4m3x4_to_bf16x4(cq[c].y, vsc);
-            const uint2 x2 = e4m3x4_to_bf16x4(cq[c].z, vsc), x3 = e4m3x4_to_bf16x4(cq[c].w, vsc);
-            unsigned char *row = vh + (cc >> 2) * (kKeys * 128) + vr * 128;
-            const int jj = (cc & 3) * 2;
-            *(uint4 *)(row + ((jj ^ (vr & 7)) * 16)) = make_uint4(x0.x, x0.y, x1.x, x1.y);
-            *(uint4 *)(row + (((jj + 1) ^ (vr & 7)) * 16)) = make_uint4(x2.x, x2.y, x3.x, x3.y);
+            for (int c = 0; c < HB / 16; ++c) {
+              const uint2 x0 = e4m3x4_to_bf16x4(cq[c].x, vsc), x1 = e4m3x4_to_bf16x4(cq[c].y, vsc);
+              const uint2 x2 = e4m3x4_to_bf16x4(cq[c].z, vsc), x3 = e4m3x4_to_bf16x4(cq[c].w, vsc);
+              w[8 * c] = x0.x; w[8 * c + 1] = x0.y; w[8 * c + 2] = x1.x; w[8 * c + 3] = x1.y;
+              w[8 * c + 4] = x2.x; w[8 * c + 5] = x2.y; w[8 * c + 6] = x3.x; w[8 * c + 7] = x3.y;
+            }
           }
         }
+        if (!rvalid || !cvt) {
+#pragma unroll
+          for (int e = 0; e < HB / 2; ++e) w[e] = 0u;
+        }
+        if (cvt || !rvalid) {
+          // half vh of row vr in the 128-byte swizzle layout: d = 128: the whole 128-byte row of d-half
+          // vh; d = 64: chunks [4 vh, 4 vh + 4) of the single 128-byte row
+          unsigned char *row = vt + (D == 128 ? vh * CF::KVHALF : 0) + vr * 128;
+#pragma unroll
+          for (int c = 0; c < HB / 8; ++c) {
+            const int j = (D == 128 ? 0 : 4 * vh) + c;
+            *(uint4 *)(row + ((j ^ (vr & 7)) * 16)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          }
+        }
+        tc::fence_proxy_async_smem();
       }
-      // this thread's CW score columns: half `half` of its row's head block (the whole tile when
-      // KVP == 1; with KVP heads packed, row r's head owns columns [s TK, s TK + TK), s = r / qr)
-      constexpr int TK = kKeys / KVP, CW = TK / 2;
-      const int c0 = (KVP > 1 ? r / pl.qr : 0) * TK + half * CW;
-      const int nv = key_tile(pl, a.nq, a.n, k0 + i).nvalid - half * CW;   // valid columns of this thread
-      uint32_t x[CW];
-      const uint32_t sa = tmem + lane_base + CF::S_COL + (uint32_t)(j * kKeys + c0);
-      if constexpr (CW == 32) tc::tmem_ld_32x32b_x32(sa, x);
-      else if constexpr (CW == 16) tc::tmem_ld_32x32b_x16(sa, x);
-      else tc::tmem_ld_32x32b_x8(sa, x);
-      tc::tmem_ld_wait();
-      float mx[CW / 2];                              // half-row max as a tree
+      float x[TK];
+      {
+        uint32_t xr[TK];
+        if constexpr (TK == 64) {
+          tc::tmem_ld_32x32b_x32(s_col, *(uint32_t(*)[32])&xr[0]);
+          tc::tmem_ld_32x32b_x32(s_col + 32, *(uint32_t(*)[32])&xr[32]);
+        } else if constexpr (TK == 32) {
+          tc::tmem_ld_32x32b_x32(s_col, xr);
+        } else {
+          tc::tmem_ld_32x32b_x16(s_col, xr);
+        }
+        tc::tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < CW / 2; ++e)
-        mx[e] = fmaxf(e < nv ? __uint_as_float(x[e]) : kNegInf,
-                      e + CW / 2 < nv ? __uint_as_float(x[e + CW / 2]) : kNegInf);
+        for (int e = 0; e < TK; ++e) x[e] = e < nv ? __uint_as_float(xr[e]) : kNegInf;
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&br.sempty[g]);  // S_g may be overwritten by this group's next S
+      // row max over the valid keys, lazy reference max
+      float mx[TK / 2];
 #pragma unroll
-      for (int w = CW / 4; w >= 1; w >>= 1)
+      for (int e = 0; e < TK / 2; ++e) mx[e] = fmaxf(x[e], x[e + TK / 2]);
 #pragma unroll
-        for (int e = 0; e < w; ++e) mx[e] = fmaxf(mx[e], mx[e + w]);
-      br.rowmax[j][half][r] = mx[0];
-      quadrant_bar(warp & 3);                        // the other half of these 32 rows
-      float tm = fmaxf(br.rowmax[j][0][r], br.rowmax[j][1][r]);
-      // move the reference max only when the row max outgrows it by more than 2^8
-      const bool need = m_run == kNegInf || (tm - m_run) * a.scale_log2 > 8.f;
+      for (int w2 = TK / 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+        for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
+      const float tm = mx[0];
+      // the group's previous PV product has read P_g and finished updating O_g
+      if (u > 0 && !tc::mbar_wait_or_abort(&br.pvdone[g], (uint32_t)(u - 1) & 1u, abort_flag)) {
+        if (!*abort_flag) fail(br, a.err, 219);
+        ok = false;
+      }
+      tc::fence_after_sync();
+      const bool need = m_run == kNegInf || (tm - m_run) * sl2 > 8.f;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? fmaxf(m_run, tm) : m_run;
-        const float al = tc::ex2_approx((m_run - m_new) * a.scale_log2);   // 0 on a row's first tile
-        if (i > 0) {
-          wait_pv(i - 1);                          // O holds PV_0 .. PV_{i-1}
+        const float al = tc::ex2_approx((m_run - m_new) * sl2);   // 0 on a row's first tile
+        if (u > 0) {
 #pragma unroll
-          for (int c0 = 0; c0 < DHALF; c0 += 32) {
+          for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
-            tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, o);
+            tc::tmem_ld_32x32b_x32(o_col + (uint32_t)c0, o);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
-            tc::tmem_st_32x32b_x32(oa + (uint32_t)c0, o);
+            tc::tmem_st_32x32b_x32(o_col + (uint32_t)c0, o);
           }
-          tc::tmem_st_wait();
         }
         l_run *= al;
         m_run = m_new;
       }
-      const float ms = m_run * a.scale_log2;
-      // CW keys = chunks c0 / 8 .. c0 / 8 + CW / 8 - 1 of this row's 128 bytes in the 128-byte swizzle
-      // layout (with KVP heads packed, the row's other chunks hold zeros from the prologue)
-      unsigned char *rowp = p_s + j * CF::P_BYTES + r * 128;
-      float lt[4] = {0.f, 0.f, 0.f, 0.f};           // four independent partial sums
+      const float ms = m_run * sl2;
+      uint32_t pw[TK / 2];
+      float lt[4] = {0.f, 0.f, 0.f, 0.f};             // four independent partial sums
 #pragma unroll
-      for (int cc = 0; cc < CW / 8; ++cc) {
-        const int ch = c0 / 8 + cc;
-        uint32_t pk[4];
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const int e = cc * 8 + e2 * 2;
-          const float p0 = (e < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e]), a.scale_log2, -ms)) : 0.f;
-          const float p1 = (e + 1 < nv) ? tc::ex2_approx(fmaf(__uint_as_float(x[e + 1]), a.scale_log2, -ms)) : 0.f;
-          lt[cc & 3] += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pk[e2] = *(uint32_t *)&h2;
-        }
-        *(uint4 *)(rowp + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int e = 0; e < TK / 2; ++e) {
+        const float p0 = 2 * e < nv ? tc::ex2_approx(fmaf(x[2 * e], sl2, -ms)) : 0.f;
+        const float p1 = 2 * e + 1 < nv ? tc::ex2_approx(fmaf(x[2 * e + 1], sl2, -ms)) : 0.f;
+        lt[e & 3] += p0 + p1;
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        pw[e] = *(uint32_t *)&h2;
       }
       l_run += (lt[0] + lt[1]) + (lt[2] + lt[3]);
-      tc::fence_proxy_async_smem();
+      if constexpr (TK == 64) tc::tmem_st_32x32b_x32(p_col, *(const uint32_t(*)[32])&pw[0]);
+      else if constexpr (TK == 32) tc::tmem_st_32x32b_x16(p_col + (uint32_t)(slot * (TK / 2)), pw);
+      else tc::tmem_st_32x32b_x8(p_col + (uint32_t)(slot * (TK / 2)), pw);
+      tc::tmem_st_wait();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        tc::mbar_arrive(&br.pfull[j]);
-        tc::mbar_arrive(&br.sempty[j]);
-      }
-    };
-    for (int i = 0; i < nt; ++i) softmax(i);
-    if (nt > 0) wait_pv(nt - 1);                   // O is complete
-    if (!ok) l_run = 0.f;
-    br.lhalf[half][r] = l_run;
-    softmax_bar();
-    l_run = ok ? br.lhalf[0][r] + br.lhalf[1][r] : 0.f;
-    if (pl.nsplit == 1 && ok && l_run > 0.f) {
-      int hs, qi;
-      const bool valid = row_target(pl, a.nq, nh, q0, r, hs, qi);
-      const int h = kvh * a.group + h0 + hs;
-      const float inv = 1.f / l_run;
-      const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D + half * DHALF;
-#pragma unroll
-      for (int c0 = 0; c0 < DHALF; c0 += 32) {
-        uint32_t x[32];
-        tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
-        tc::tmem_ld_wait();
-        if (!valid) continue;
-        if (a.out_f32) {
-          float4 *dst = (float4 *)((float *)a.out + obase + c0);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(__uint_as_float(x[4 * q4]) * inv, __uint_as_float(x[4 * q4 + 1]) * inv,
-                                  __uint_as_float(x[4 * q4 + 2]) * inv, __uint_as_float(x[4 * q4 + 3]) * inv);
+      if (lane == 0) tc::mbar_arrive(&br.pfull[g]);
+    }
+    // O_g is complete once the group's last PV product has landed
+    if (u > 0 && !tc::mbar_wait_or_abort(&br.pvdone[g], (uint32_t)(u - 1) & 1u, abort_flag)) {
+      if (!*abort_flag) fail(br, a.err, 219);
+      ok = false;
+    }
+    tc::fence_after_sync();
+  }
+
+  // ---- every role is done: all copies consumed, all MMAs complete ----
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      // copies issued but never consumed still land in shared memory: wait for them (bounded)
+      for (int i = 0; i < br.issued; ++i) {
+        if ((i >> 1) < br.consumed_g[i & 1]) continue;
+        if (F8KV && key_tile(pl, a.nq, a.n, k0 + i).range != 1) {
+          int uses = 0;                                // earlier cache tiles in this stage: raw's phase
+          for (int j = i % NS; j < i; j += NS) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
+          tc::mbar_wait(&br.raw[i % NS], (uint32_t)uses & 1u);
         } else {
-          uint4 *dst = (uint4 *)((__nv_bfloat16 *)a.out + obase + c0);
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(x[8 * q8 + 2 * e]) * inv,
-                                                        __uint_as_float(x[8 * q8 + 2 * e + 1]) * inv);
-              w[e] = *(uint32_t *)&h2;
-            }
-            dst[q8] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          tc::mbar_wait(&br.kvfull[i % NS], (uint32_t)(i / NS) & 1u);
         }
       }
-      if (valid && half == 0 && a.lse) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = m_run * a.scale + __logf(l_run);
+    }
+    __syncthreads();
+  }
+
+  // ---- combine the two groups' rows: row r's final (M, L) and D values ----
+  // The ring is idle now.  It holds: the two groups' (max, sum) per row at ML_OFF; with one split, the
+  // output tile (blocks of 128 rows x 128 bytes: 64 bf16 or 32 fp32 columns each, 128-byte swizzle,
+  // the layout a tile load of the output map would write), stored by TMA; with a cluster, the send
+  // and receive areas of the split merge.
+  float *send = (float *)kv_s;
+  float *recv = send + CF::MERGE_ROWS * CF::RP;
+  float2 *ml = (float2 *)(kv_s + CF::ML_OFF);           // [group][row]
+  const int out_f32 = a.out_f32;
+  const int cw = out_f32 ? 32 : 64;                     // columns per 128-byte output block
+  if (warp >= 4) {
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    ml[g * kTile + r] = make_float2(m_run, ok ? l_run : 0.f);
+    quadrant_bar(q);
+    const float2 ml0 = ml[r], ml1 = ml[kTile + r];
+    const float M = fmaxf(ml0.y > 0.f ? ml0.x : kNegInf, ml1.y > 0.f ? ml1.x : kNegInf);
+    const float w0 = ml0.y > 0.f ? tc::ex2_approx((ml0.x - M) * a.scale_log2) : 0.f;
+    const float w1 = ml1.y > 0.f ? tc::ex2_approx((ml1.x - M) * a.scale_log2) : 0.f;
+    const float L = w0 * ml0.y + w1 * ml1.y;
+    constexpr int DHALF = D / 2;                       // this thread's columns [g D/2, (g + 1) D/2)
+    float v[DHALF];
+#pragma unroll
+    for (int c0 = 0; c0 < DHALF; c0 += 32) {
+      uint32_t o0[32], o1[32];
+      tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::O_COL + (uint32_t)(g * DHALF + c0), o0);
+      tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::O_COL + (uint32_t)(D + g * DHALF + c0), o1);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        v[c0 + e] = (w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f) + (w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f);
+    }
+    if (C == 1) {
+      // normalised row part into the output tile: 16-byte chunk j of row r of a block at (j ^ (r & 7))
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      unsigned char *ot = kv_s;
+      if (!out_f32) {
+#pragma unroll
+        for (int c = 0; c < DHALF / 8; ++c) {          // 8 bf16 per chunk
+          const int col = g * DHALF + 8 * c;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * c + 2 * e] * inv, v[8 * c + 2 * e + 1] * inv);
+            w[e] = *(uint32_t *)&h2;
+          }
+          const int blk = col / 64, j = (col % 64) / 8;
+          *(uint4 *)(ot + blk * CF::QHALF + r * 128 + ((j ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < DHALF / 4; ++c) {          // 4 fp32 per chunk
+          const int col = g * DHALF + 4 * c;
+          const int blk = col / 32, j = (col % 32) / 4;
+          *(float4 *)(ot + blk * CF::QHALF + r * 128 + ((j ^ (r & 7)) * 16)) =
+              make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
+        }
+      }
+      int hs, qi;
+      if (g == 0 && a.lse && L > 0.f && row_target(pl, a.nq, nh, q0, r, hs, qi))
+        a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = M * a.scale + __logf(L);
+      tc::fence_proxy_async_smem();                    // the TMA stores read the tile
+      softmax_bar();
+      if (threadIdx.x == 128) {
+        // one box per head slot and column block; rows past nq lie outside the map and are not written
+        for (int hs2 = 0; hs2 < nh; ++hs2)
+          for (int blk = 0; blk < D / cw; ++blk)
+            tc::tma_store_4d(&mo, ot + blk * CF::QHALF + hs2 * pl.qr * 128, blk * cw, kvh * a.group + h0 + hs2, q0, b);
+        tc::bulk_commit_group();
+        tc::bulk_wait_all();
+      }
+    } else {
+      // stage the row (unnormalised, relative to M) in the send area: row r, grouped by owner
+      float *row = send + (size_t)r * CF::RP;
+#pragma unroll
+      for (int c = 0; c < DHALF / 4; ++c)
+        *(float4 *)(row + g * DHALF + 4 * c) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      if (g == 0) *(float2 *)(row + D) = make_float2(L > 0.f ? M * a.scale_log2 : kNegInf, L);
+      tc::fence_proxy_async_smem();                    // the bulk copies read these rows
     }
   }
 
-  if (pl.nsplit > 1) {
-    // ---- merge the splits of this unit through the cluster's shared memory, stores only ----
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    const int C = pl.nsplit;
-    const int crank = (int)cluster.block_rank();
-    constexpr int CH = D / 4;                        // float4 chunks per row
-    constexpr int DP = CF::DP;
-    const int rpc = (kTile + C - 1) / C;             // rows owned per CTA
-    // receive area in the K/V ring: [C][rpc] O rows (unnormalised), then [C][rpc] (max * log2 e, l)
-    float *orecv = (float *)kv_s;
-    float2 *mlrecv = (float2 *)(kv_s + (size_t)CF::MERGE_ROWS * DP * 4);
-    tc::fence_before_sync();
-    cluster.sync();                                  // every CTA's MMAs and copies are done: rings are free
+  if (C > 1) {
+    // ---- split merge through the cluster ----
+    const int crank = (int)tc::cluster_ctarank();
+    tc::cluster_arrive();                              // this CTA's ring is free and its rows are staged
+    tc::cluster_wait();                                // so is every peer's
+    if (threadIdx.x == 128) {
+      for (int c = 0; c < C; ++c) {
+        if (c == crank) continue;
+        tc::bulk_copy_to_cluster(tc::cluster_map(recv + (size_t)crank * rpc * CF::RP, (uint32_t)c),
+                                 send + (size_t)c * rpc * CF::RP, seg_bytes, tc::cluster_map(&br.mrg, (uint32_t)c));
+      }
+    }
     if (warp >= 4) {
-      // this thread's half row, as accumulated, and the row's (max, l) go to the CTA that owns the row
-      const int owner = r / rpc;
-      const int slot = crank * rpc + (r - owner * rpc);
-      float *orow = orecv + (size_t)slot * DP + half * (D / 2);
-      float4 *dst = (float4 *)(owner == crank ? orow : cluster.map_shared_rank(orow, owner));
-      if (half == 0) {
-        const float2 mine = l_run > 0.f ? make_float2(m_run * a.scale_log2, l_run) : make_float2(kNegInf, 0.f);
-        *(owner == crank ? mlrecv + slot : cluster.map_shared_rank(mlrecv + slot, owner)) = mine;
+      if (!tc::mbar_wait_or_abort(&br.mrg, 0, abort_flag)) {   // the peers' copies of this CTA's rows
+        if (!*abort_flag) fail(br, a.err, 221);
       }
-      const uint32_t oa = tmem + ((uint32_t)((warp & 3) * 32) << 16) + CF::O_COL + (uint32_t)(half * (D / 2));
+    }
+    tc::cluster_arrive();                              // every copy into this CTA has landed
+    if (warp >= 4) {
+      // owner: rows [r0, r1) of the tile.  Item = (local row, 32-column chunk); source c of local row lr
+      // is the receive area, or for this CTA's own rows the send area.  out = sum_c O_c w_c with
+      // w_c = 2^(m_c - M) / L, M = max_c m_c, L = sum_c l_c 2^(m_c - M).  The loads of an item are
+      // independent of one another, so they are all in flight at once.
+      const int st = threadIdx.x - 128;
+      const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);
+      const uint32_t send_a = tc::smem_u32(send), recv_a = tc::smem_u32(recv);
+      auto src_addr = [&](int c, int lr) -> uint32_t {
+        return (c == crank ? send_a + (uint32_t)((crank * rpc + lr) * CF::RP * 4)
+                           : recv_a + (uint32_t)((c * rpc + lr) * CF::RP * 4));
+      };
+      constexpr int NCH = D / 32;
+      for (int it = st; it < (r1 - r0) * NCH; it += 256) {
+        const int lr = it / NCH, ch = it % NCH;
+        int hs, qi;
+        if (!row_target(pl, a.nq, nh, q0, r0 + lr, hs, qi)) continue;
+        float2 mlc[kMaxCluster];
+        float M = kNegInf;
 #pragma unroll
-      for (int c0 = 0; c0 < D / 2; c0 += 32) {
-        uint32_t x[32];
-        tc::tmem_ld_32x32b_x32(oa + (uint32_t)c0, x);
-        tc::tmem_ld_wait();
+        for (int c = 0; c < kMaxCluster; ++c)
+          if (c < C) {
+            mlc[c] = lds_f2(src_addr(c, lr) + D * 4);
+            M = fmaxf(M, mlc[c].x);
+          }
+        float L = 0.f, wc[kMaxCluster];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4)
-          dst[c0 / 4 + q4] = make_float4(__uint_as_float(x[4 * q4]), __uint_as_float(x[4 * q4 + 1]),
-                                         __uint_as_float(x[4 * q4 + 2]), __uint_as_float(x[4 * q4 + 3]));
+        for (int c = 0; c < kMaxCluster; ++c)
+          if (c < C) {
+            wc[c] = mlc[c].y > 0.f ? tc::ex2_approx(mlc[c].x - M) : 0.f;
+            L += wc[c] * mlc[c].y;
+          }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+          if (c < C && wc[c] > 0.f) {
+            const uint32_t base = src_addr(c, lr) + (uint32_t)(ch * 32 * 4);
+            float4 x[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = lds_f4(base + 16 * k);
+            const float w = wc[c] * inv;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              acc[4 * k] = fmaf(x[k].x, w, acc[4 * k]); acc[4 * k + 1] = fmaf(x[k].y, w, acc[4 * k + 1]);
+              acc[4 * k + 2] = fmaf(x[k].z, w, acc[4 * k + 2]); acc[4 * k + 3] = fmaf(x[k].w, w, acc[4 * k + 3]);
+            }
+          }
+        const int h = kvh * a.group + h0 + hs;
+        const int64_t off = (((int64_t)b * a.nq + qi) * a.hq + h) * D + ch * 32;
+        void *dst = out_f32 ? (void *)((float *)a.out + off) : (void *)((__nv_bfloat16 *)a.out + off);
+        store_row_part<32>(dst, out_f32 != 0, acc, 1.f);
+        if (ch == 0 && a.lse && L > 0.f) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
       }
     }
-    cluster.sync();                                  // every row is in its owner
-    // owner: out = sum_c O_c w_c with w_c = 2^(m_c - M) / L, M = max_c m_c, L = sum_c l_c 2^(m_c - M)
-    const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);
-    float *wrecv = (float *)(mlrecv + CF::MERGE_ROWS);   // [C][rpc] weights, 0 for an empty or aborted split
-    for (int lr = threadIdx.x; lr < r1 - r0; lr += kThreads) {
-      float M = kNegInf, L = 0.f;
-      for (int c = 0; c < C; ++c) M = fmaxf(M, mlrecv[c * rpc + lr].x);
-      for (int c = 0; c < C; ++c) {
-        const float2 ml = mlrecv[c * rpc + lr];
-        if (ml.y > 0.f) L += ml.y * exp2f(ml.x - M);
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      for (int c = 0; c < C; ++c) {
-        const float2 ml = mlrecv[c * rpc + lr];
-        wrecv[c * rpc + lr] = ml.y > 0.f ? exp2f(ml.x - M) * inv : 0.f;
-      }
-      int hs, qi;
-      if (a.lse && L > 0.f && row_target(pl, a.nq, nh, q0, r0 + lr, hs, qi))
-        a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = (M + log2f(L)) * 0.6931471805599453f;
-    }
-    __syncthreads();
-    for (int u = threadIdx.x; u < (r1 - r0) * CH; u += kThreads) {
-      const int lr = u / CH, ch = u % CH;
-      int hs, qi;
-      if (!row_target(pl, a.nq, nh, q0, r0 + lr, hs, qi)) continue;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < C; ++c) {
-        const float w = wrecv[c * rpc + lr];
-        if (w == 0.f) continue;                      // its rows may hold anything
-        const float4 v = *(const float4 *)(orecv + (size_t)(c * rpc + lr) * DP + ch * 4);
-        acc.x = fmaf(v.x, w, acc.x); acc.y = fmaf(v.y, w, acc.y);
-        acc.z = fmaf(v.z, w, acc.z); acc.w = fmaf(v.w, w, acc.w);
-      }
-      const int64_t off = (((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs) * D + ch * 4;
-      if (a.out_f32) {
-        *(float4 *)((float *)a.out + off) = acc;
-      } else {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
-        *(uint2 *)((__nv_bfloat16 *)a.out + off) = make_uint2(*(uint32_t *)&lo, *(uint32_t *)&hi);
-      }
-    }
+    tc::cluster_wait();                                // every copy out of this CTA has landed too
   }
 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (br.abort && threadIdx.x == 0) {
-    // copies issued but never consumed still land in shared memory: wait for them (bounded)
-    for (int i = br.consumed; i < br.issued; ++i) {
-      if (F8KV && key_tile(pl, a.nq, a.n, k0 + i).range != 1) {
-        int uses = 0;                                  // earlier cache tiles in this stage: raw's phase
-        for (int j = i % NS; j < i; j += NS) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
-        tc::mbar_wait(&br.raw[i % NS], (uint32_t)uses & 1u);
-      } else {
-        tc::mbar_wait(&br.kvfull[i % NS], (uint32_t)(i / NS) & 1u);
-      }
-    }
-  }
-  __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, CF::TMEM_COLS);
 }
 
@@ -732,6 +952,20 @@ bool map4(CUtensorMap *m, const void *base, int d, int heads, int rows, int batc
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same view of an fp32 tensor, box {32, 1, box_rows, 1} (128-byte rows in the swizzled layout).
+bool map4_f32(CUtensorMap *m, const void *base, int d, int heads, int rows, int batch, int64_t batch_stride,
+              int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4, (cuuint64_t)batch_stride * 4};
+  const cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -827,7 +1061,7 @@ cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cud
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a);
+  e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], a);
   count_launches(1);
   return e;
 }
@@ -856,7 +1090,7 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t cstride = (int64_t)p.seq_len * p.hkv * p.d;  // cache batch stride
   const int64_t fstride = (int64_t)p.nq * p.hkv * p.d;       // fresh batch stride
   const int64_t qstride = (int64_t)p.nq * p.hq * p.d;
-  CUtensorMap maps[7];
+  CUtensorMap maps[8];
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
   // per-sequence blocks: prefix and suffix tiles are read through maps of the whole cache; rows of a
   // sequence's own window that fall in a boundary tile are read and weighted by exactly zero
@@ -864,7 +1098,10 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t off_c = per_seq ? 0 : (int64_t)pl.f1 * p.hkv * p.d;
   const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
   const int kvp = pl.kvp;
-  bool ok = map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
+  // the output [b, nq, Hq, d] like the queries: bf16 boxes of 64 columns, or fp32 boxes of 32
+  bool ok = (p.out_f32 ? map4_f32(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, pl.qr)
+                       : map4(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, pl.qr)) &&
+            map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
             map4_kv(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false) &&
             map4_kv(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false);
   if (p.f8kv) {   // the cache as E4M3 codes (one byte per element)
