@@ -88,18 +88,21 @@ struct Cfg {
   static constexpr int STAGE = 2 * KV_BYTES;          // K + V
   static constexpr int NS = D == 128 ? 7 : 8;         // K/V ring stages
   static_assert(kTile * D * 2 <= STAGE, "the query tile is staged in one ring stage");
-  // split merge: rows of D fp32 values, then the row's max (log2 units) and sum, then the row's
-  // weight; the pitch keeps every row 16-byte aligned.  A send area (every row of the CTA, grouped by
-  // owner) and a receive area (C copies of the rows this CTA owns), C * ceil(128 / C) <= 136 rows each.
-  static constexpr int RP = D + 4;
+  // split merge: a row sent to its owner is D fp32 values normalised by the row's sum, then the row's
+  // max (log2 units) and sum, padded to a multiple of 16 bytes.  A send area (the rows this CTA
+  // does not own, grouped by owner) and a receive area (the C - 1 copies of the rows it owns),
+  // C * ceil(128 / C) <= 136 rows each, then the output tile.
+  static constexpr int SRP = D * 4 + 16;
   static constexpr int MERGE_ROWS = 136;
-  static constexpr int MERGE_BYTES = 2 * MERGE_ROWS * RP * 4;
-  static constexpr int RING = NS * STAGE > MERGE_BYTES ? NS * STAGE : MERGE_BYTES;
+  static constexpr int MERGE_BYTES = 2 * MERGE_ROWS * SRP;
+  static constexpr int RING = NS * STAGE;
   // after the pipeline the ring also holds the output tile (one 128-row block of 128 bytes per 64 bf16 or
-  // 32 fp32 columns, 128-byte swizzle) and, at its end, the two groups' (max, sum) per row
+  // 32 fp32 columns, 128-byte swizzle; with a cluster, after the merge areas) and, at its end, the two
+  // groups' (max, sum) per row
   static constexpr int OUT_BYTES = kTile * D * 4;
+  static constexpr int OUT_OFF = (MERGE_BYTES + 1023) / 1024 * 1024;
   static constexpr int ML_OFF = RING - 2 * kTile * 8;
-  static_assert(MERGE_BYTES <= ML_OFF && OUT_BYTES <= ML_OFF, "ring areas after the pipeline");
+  static_assert(OUT_OFF + OUT_BYTES <= ML_OFF, "ring areas after the pipeline");
   static constexpr int SMEM = RING + 1024 + 512;    // + alignment + Bars
   // TMEM columns
   static constexpr uint32_t Q_COL = 0;               // D / 2 columns of bf16 pairs
@@ -247,6 +250,15 @@ __device__ __forceinline__ void store_row_part(void *dst, bool f32, const float 
 
 static_assert(sizeof(Bars) <= 512, "Bars must fit its shared-memory reservation");
 
+// Rows of one TMA store box of the output (its map's box height): a head slot's qr rows, or, with a
+// cluster, the rows a CTA owns when they fall inside one slot; 0 when a CTA's rows do not fall on such
+// boundaries (multiples of 8 rows), and its threads then store their rows directly.
+__host__ __device__ __forceinline__ int out_box_rows(const Plan &pl) {
+  const int C = pl.nsplit, rpc = (kTile + C - 1) / C;
+  const int br = C == 1 ? pl.qr : (rpc % pl.qr == 0 ? pl.qr : (pl.qr % rpc == 0 ? rpc : 0));
+  return br % 8 == 0 ? br : 0;
+}
+
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -290,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int C = pl.nsplit;                             // CTAs of this unit's cluster
   const int rpc = (kTile + C - 1) / C;                 // rows owned per CTA in the split merge
-  const uint32_t seg_bytes = (uint32_t)(rpc * CF::RP * 4);   // one owner's rows, as sent
+  const uint32_t seg_bytes = (uint32_t)(rpc * CF::SRP);   // one owner's rows, as sent
 
   if (threadIdx.x == 0) {
     br.abort = 0; br.issued = 0; br.consumed_g[0] = 0; br.consumed_g[1] = 0; br.cvt_stop = 0;
@@ -761,27 +773,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- combine the two groups' rows: row r's final (M, L) and D values ----
-  // The ring is idle now.  It holds: the two groups' (max, sum) per row at ML_OFF; with one split, the
-  // output tile (blocks of 128 rows x 128 bytes: 64 bf16 or 32 fp32 columns each, 128-byte swizzle,
-  // the layout a tile load of the output map would write), stored by TMA; with a cluster, the send
-  // and receive areas of the split merge.
-  float *send = (float *)kv_s;
-  float *recv = send + CF::MERGE_ROWS * CF::RP;
+  // The ring is idle now.  It holds: the two groups' (max, sum) per row at ML_OFF; the output tile
+  // (blocks of 128 rows x 128 bytes: 64 bf16 or 32 fp32 columns each, 128-byte swizzle, the layout a tile
+  // load of the output map would write), written by TMA; with a cluster, before it, the send and
+  // receive areas of the split merge.
+  unsigned char *send = kv_s;
+  unsigned char *recv = kv_s + CF::MERGE_ROWS * CF::SRP;
+  unsigned char *ot = kv_s + (C == 1 ? 0 : CF::OUT_OFF);
   float2 *ml = (float2 *)(kv_s + CF::ML_OFF);           // [group][row]
   const int out_f32 = a.out_f32;
   const int cw = out_f32 ? 32 : 64;                     // columns per 128-byte output block
+  const int crank = C > 1 ? (int)tc::cluster_ctarank() : 0;
+  const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);   // the rows this CTA writes
+  // rows per TMA store box: a head slot (qr rows), or the owned rows when they lie in one slot; 0 when
+  // the owned rows do not fall on slot boundaries (the owners then store their rows directly)
+  const int br_rows = out_box_rows(pl);
+  constexpr int DHALF = D / 2;                         // a softmax thread's columns [g D/2, (g + 1) D/2)
+  float v[DHALF];
+  float Mrow = kNegInf, Lrow = 0.f;                    // the CTA's row: max (raw score units), sum
   if (warp >= 4) {
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     ml[g * kTile + r] = make_float2(m_run, ok ? l_run : 0.f);
     quadrant_bar(q);
     const float2 ml0 = ml[r], ml1 = ml[kTile + r];
-    const float M = fmaxf(ml0.y > 0.f ? ml0.x : kNegInf, ml1.y > 0.f ? ml1.x : kNegInf);
-    const float w0 = ml0.y > 0.f ? tc::ex2_approx((ml0.x - M) * a.scale_log2) : 0.f;
-    const float w1 = ml1.y > 0.f ? tc::ex2_approx((ml1.x - M) * a.scale_log2) : 0.f;
-    const float L = w0 * ml0.y + w1 * ml1.y;
-    constexpr int DHALF = D / 2;                       // this thread's columns [g D/2, (g + 1) D/2)
-    float v[DHALF];
+    Mrow = fmaxf(ml0.y > 0.f ? ml0.x : kNegInf, ml1.y > 0.f ? ml1.x : kNegInf);
+    const float w0 = ml0.y > 0.f ? tc::ex2_approx((ml0.x - Mrow) * a.scale_log2) : 0.f;
+    const float w1 = ml1.y > 0.f ? tc::ex2_approx((ml1.x - Mrow) * a.scale_log2) : 0.f;
+    Lrow = w0 * ml0.y + w1 * ml1.y;
 #pragma unroll
     for (int c0 = 0; c0 < DHALF; c0 += 32) {
       uint32_t o0[32], o1[32];
@@ -792,10 +811,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 32; ++e)
         v[c0 + e] = (w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f) + (w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f);
     }
-    if (C == 1) {
+    if (C > 1 && r / rpc != crank) {
+      // a row another CTA owns: normalised half row (g) and, from group 0, (max, sum) to the send area
+      unsigned char *row = send + (size_t)r * CF::SRP;
+      const float inv = Lrow > 0.f ? 1.f / Lrow : 0.f;
+#pragma unroll
+      for (int c = 0; c < DHALF / 4; ++c)
+        *(float4 *)(row + g * DHALF * 4 + 16 * c) =
+            make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
+      if (g == 0) *(float2 *)(row + D * 4) = make_float2(Lrow > 0.f ? Mrow * a.scale_log2 : kNegInf, Lrow);
+      tc::fence_proxy_async_smem();                    // the bulk copies read these rows
+    }
+  }
+
+  if (C > 1) {
+    // ---- split merge through the cluster: the rows go to their owners ----
+    // The cluster barriers only say "reached here": a peer's ring is idle once it arrives (its loads
+    // landed and its products completed before that, as it observed), and its staged rows are read by
+    // its own bulk copies after the softmax barrier below.  Neither publishes memory, so the arrivals
+    // are relaxed.
+    tc::cluster_arrive_relaxed();                      // this CTA's ring is free
+    if (warp >= 4) softmax_bar();                      // its staged rows are complete
+    tc::cluster_wait();                                // every peer's ring is free
+    if (threadIdx.x == 128) {
+      for (int c = 0; c < C; ++c) {
+        if (c == crank) continue;
+        tc::bulk_copy_to_cluster(tc::cluster_map(recv + (size_t)crank * rpc * CF::SRP, (uint32_t)c),
+                                 send + (size_t)c * rpc * CF::SRP, seg_bytes, tc::cluster_map(&br.mrg, (uint32_t)c));
+      }
+    }
+    if (warp >= 4 && r / rpc == crank) {
+      // an owned row: combine this CTA's part (registers, relative to Mrow) with the peers' normalised
+      // copies; weight of source s: L_s 2^(m_s - M), M = max_s m_s (log2 units)
+      if (!tc::mbar_wait_or_abort(&br.mrg, 0, abort_flag)) {   // the peers' copies of this CTA's rows
+        if (!*abort_flag) fail(br, a.err, 221);
+      }
+      const float mown = Lrow > 0.f ? Mrow * a.scale_log2 : kNegInf;
+      float M = mown;
+      for (int c = 0; c < C; ++c) {
+        if (c == crank) continue;
+        const float2 mlc = lds_f2(tc::smem_u32(recv + (size_t)(c * rpc + r - r0) * CF::SRP + D * 4));
+        if (mlc.y > 0.f) M = fmaxf(M, mlc.x);
+      }
+      const float wown = Lrow > 0.f ? tc::ex2_approx(mown - M) : 0.f;
+      float W = wown * Lrow;
+#pragma unroll
+      for (int e = 0; e < DHALF; ++e) v[e] = wown > 0.f ? v[e] * wown : 0.f;
+      for (int c = 0; c < C; ++c) {
+        if (c == crank) continue;
+        const uint32_t rowa = tc::smem_u32(recv + (size_t)(c * rpc + r - r0) * CF::SRP);
+        const float2 mlc = lds_f2(rowa + D * 4);
+        if (!(mlc.y > 0.f)) continue;                  // an empty split: its values may be anything
+        const float wc = mlc.y * tc::ex2_approx(mlc.x - M);
+        W += wc;
+#pragma unroll
+        for (int cc = 0; cc < DHALF / 4; ++cc) {
+          const float4 x = lds_f4(rowa + (uint32_t)(g * DHALF * 4 + 16 * cc));
+          v[4 * cc] = fmaf(x.x, wc, v[4 * cc]); v[4 * cc + 1] = fmaf(x.y, wc, v[4 * cc + 1]);
+          v[4 * cc + 2] = fmaf(x.z, wc, v[4 * cc + 2]); v[4 * cc + 3] = fmaf(x.w, wc, v[4 * cc + 3]);
+        }
+      }
+      // v is now relative to M with sum W (log2 units): as if this CTA had seen every key
+      Mrow = M / a.scale_log2;
+      Lrow = W;
+    }
+    tc::cluster_arrive_relaxed();                      // every copy into this CTA has landed
+  }
+
+  // ---- output: this CTA's rows [r0, r1) ----
+  if (warp >= 4 && r >= r0 && r < r1) {
+    const float inv = Lrow > 0.f ? 1.f / Lrow : 0.f;
+    int hs, qi;
+    const bool valid = row_target(pl, a.nq, nh, q0, r, hs, qi);
+    const int h = kvh * a.group + h0 + hs;
+    if (valid && g == 0 && a.lse && Lrow > 0.f)
+      a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = Mrow * a.scale + __logf(Lrow);
+    if (br_rows > 0) {
       // normalised row part into the output tile: 16-byte chunk j of row r of a block at (j ^ (r & 7))
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      unsigned char *ot = kv_s;
       if (!out_f32) {
 #pragma unroll
         for (int c = 0; c < DHALF / 8; ++c) {          // 8 bf16 per chunk
@@ -818,107 +910,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
         }
       }
-      int hs, qi;
-      if (g == 0 && a.lse && L > 0.f && row_target(pl, a.nq, nh, q0, r, hs, qi))
-        a.lse[((int64_t)b * a.nq + qi) * a.hq + kvh * a.group + h0 + hs] = M * a.scale + __logf(L);
       tc::fence_proxy_async_smem();                    // the TMA stores read the tile
-      softmax_bar();
-      if (threadIdx.x == 128) {
-        // one box per head slot and column block; rows past nq lie outside the map and are not written
-        for (int hs2 = 0; hs2 < nh; ++hs2)
-          for (int blk = 0; blk < D / cw; ++blk)
-            tc::tma_store_4d(&mo, ot + blk * CF::QHALF + hs2 * pl.qr * 128, blk * cw, kvh * a.group + h0 + hs2, q0, b);
-        tc::bulk_commit_group();
-        tc::bulk_wait_all();
-      }
-    } else {
-      // stage the row (unnormalised, relative to M) in the send area: row r, grouped by owner
-      float *row = send + (size_t)r * CF::RP;
-#pragma unroll
-      for (int c = 0; c < DHALF / 4; ++c)
-        *(float4 *)(row + g * DHALF + 4 * c) = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      if (g == 0) *(float2 *)(row + D) = make_float2(L > 0.f ? M * a.scale_log2 : kNegInf, L);
-      tc::fence_proxy_async_smem();                    // the bulk copies read these rows
+    } else if (valid && Lrow > 0.f) {
+      const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D + g * DHALF;
+      void *dst = out_f32 ? (void *)((float *)a.out + obase) : (void *)((__nv_bfloat16 *)a.out + obase);
+      store_row_part<DHALF>(dst, out_f32 != 0, v, inv);
     }
   }
-
-  if (C > 1) {
-    // ---- split merge through the cluster ----
-    const int crank = (int)tc::cluster_ctarank();
-    tc::cluster_arrive();                              // this CTA's ring is free and its rows are staged
-    tc::cluster_wait();                                // so is every peer's
+  if (warp >= 4 && br_rows > 0) {
+    softmax_bar();
     if (threadIdx.x == 128) {
-      for (int c = 0; c < C; ++c) {
-        if (c == crank) continue;
-        tc::bulk_copy_to_cluster(tc::cluster_map(recv + (size_t)crank * rpc * CF::RP, (uint32_t)c),
-                                 send + (size_t)c * rpc * CF::RP, seg_bytes, tc::cluster_map(&br.mrg, (uint32_t)c));
-      }
-    }
-    if (warp >= 4) {
-      if (!tc::mbar_wait_or_abort(&br.mrg, 0, abort_flag)) {   // the peers' copies of this CTA's rows
-        if (!*abort_flag) fail(br, a.err, 221);
-      }
-    }
-    tc::cluster_arrive();                              // every copy into this CTA has landed
-    if (warp >= 4) {
-      // owner: rows [r0, r1) of the tile.  Item = (local row, 32-column chunk); source c of local row lr
-      // is the receive area, or for this CTA's own rows the send area.  out = sum_c O_c w_c with
-      // w_c = 2^(m_c - M) / L, M = max_c m_c, L = sum_c l_c 2^(m_c - M).  The loads of an item are
-      // independent of one another, so they are all in flight at once.
-      const int st = threadIdx.x - 128;
-      const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);
-      const uint32_t send_a = tc::smem_u32(send), recv_a = tc::smem_u32(recv);
-      auto src_addr = [&](int c, int lr) -> uint32_t {
-        return (c == crank ? send_a + (uint32_t)((crank * rpc + lr) * CF::RP * 4)
-                           : recv_a + (uint32_t)((c * rpc + lr) * CF::RP * 4));
-      };
-      constexpr int NCH = D / 32;
-      for (int it = st; it < (r1 - r0) * NCH; it += 256) {
-        const int lr = it / NCH, ch = it % NCH;
+      // one box per br_rows rows of a head slot and column block; rows past nq lie outside the map
+      for (int rb = r0; rb < r1; rb += br_rows) {
         int hs, qi;
-        if (!row_target(pl, a.nq, nh, q0, r0 + lr, hs, qi)) continue;
-        float2 mlc[kMaxCluster];
-        float M = kNegInf;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-          if (c < C) {
-            mlc[c] = lds_f2(src_addr(c, lr) + D * 4);
-            M = fmaxf(M, mlc[c].x);
-          }
-        float L = 0.f, wc[kMaxCluster];
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-          if (c < C) {
-            wc[c] = mlc[c].y > 0.f ? tc::ex2_approx(mlc[c].x - M) : 0.f;
-            L += wc[c] * mlc[c].y;
-          }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        float acc[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-#pragma unroll
-        for (int c = 0; c < kMaxCluster; ++c)
-          if (c < C && wc[c] > 0.f) {
-            const uint32_t base = src_addr(c, lr) + (uint32_t)(ch * 32 * 4);
-            float4 x[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) x[k] = lds_f4(base + 16 * k);
-            const float w = wc[c] * inv;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              acc[4 * k] = fmaf(x[k].x, w, acc[4 * k]); acc[4 * k + 1] = fmaf(x[k].y, w, acc[4 * k + 1]);
-              acc[4 * k + 2] = fmaf(x[k].z, w, acc[4 * k + 2]); acc[4 * k + 3] = fmaf(x[k].w, w, acc[4 * k + 3]);
-            }
-          }
-        const int h = kvh * a.group + h0 + hs;
-        const int64_t off = (((int64_t)b * a.nq + qi) * a.hq + h) * D + ch * 32;
-        void *dst = out_f32 ? (void *)((float *)a.out + off) : (void *)((__nv_bfloat16 *)a.out + off);
-        store_row_part<32>(dst, out_f32 != 0, acc, 1.f);
-        if (ch == 0 && a.lse && L > 0.f) a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = (M + log2f(L)) * 0.6931471805599453f;
+        row_target(pl, a.nq, nh, q0, rb, hs, qi);
+        if (hs >= nh) continue;
+        for (int blk = 0; blk < D / cw; ++blk)
+          tc::tma_store_4d(&mo, ot + blk * CF::QHALF + rb * 128, blk * cw, kvh * a.group + h0 + hs, qi, b);
       }
+      tc::bulk_commit_group();
+      tc::bulk_wait_all();
     }
-    tc::cluster_wait();                                // every copy out of this CTA has landed too
   }
+  if (C > 1) tc::cluster_wait();                      // every copy out of this CTA has landed too
 
   tc::fence_before_sync();
   __syncthreads();
@@ -1099,8 +1113,9 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
   const int kvp = pl.kvp;
   // the output [b, nq, Hq, d] like the queries: bf16 boxes of 64 columns, or fp32 boxes of 32
-  bool ok = (p.out_f32 ? map4_f32(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, pl.qr)
-                       : map4(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, pl.qr)) &&
+  const int obr = out_box_rows(pl) > 0 ? out_box_rows(pl) : pl.qr;
+  bool ok = (p.out_f32 ? map4_f32(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, obr)
+                       : map4(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, obr)) &&
             map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
             map4_kv(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false) &&
             map4_kv(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false);
