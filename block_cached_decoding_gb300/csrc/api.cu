@@ -182,6 +182,9 @@ fdllm_status resolve_attn(const fdllm_attn_desc *d, AttnProblem &p) {
   p.out_f32 = d->out_f32;
   p.f8kv = 0;
   p.k_scale = p.v_scale = nullptr;
+  p.update = 0;
+  p.win = d->block_size;
+  p.kc_w = p.vc_w = nullptr;
   return FDLLM_OK;
 }
 
@@ -312,7 +315,7 @@ using namespace fdllm;
 
 extern "C" {
 
-int32_t fdllm_version(void) { return 104; }
+int32_t fdllm_version(void) { return 105; }
 
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
   if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");
@@ -377,10 +380,17 @@ static fdllm_status block_attn(const fdllm_attn_desc *desc, const int32_t *block
                                const void *k_cache, const void *v_cache, const void *k_fresh,
                                const void *v_fresh, void *out, float *lse, void *workspace, size_t ws_bytes,
                                fdllm_stream_t stream, const float *k_scale = nullptr,
-                               const float *v_scale = nullptr) {
+                               const float *v_scale = nullptr, bool update = false) {
   AttnProblem p;
   fdllm_status st = resolve_attn(desc, p);
   if (st != FDLLM_OK) return st;
+  if (update) {
+    if (!desc->use_cache)
+      return fail(FDLLM_EUNSUPPORTED, "attn update: the window update needs a cache (use_cache = 1)");
+    p.update = 1;
+    p.kc_w = const_cast<void *>(k_cache);
+    p.vc_w = const_cast<void *>(v_cache);
+  }
   if (k_scale || v_scale) {
     if (!k_scale || !v_scale) return fail(FDLLM_EINVAL, "attn fp8kv: k_scale and v_scale are required");
     if (!desc->use_cache || !attn_tc_supported(p))
@@ -408,6 +418,21 @@ static fdllm_status block_attn(const fdllm_attn_desc *desc, const int32_t *block
   p.out = out; p.lse = lse; p.ws = workspace; p.ws_bytes = ws_bytes;
   p.err = error_word_ptr();
   cudaStream_t cs = (cudaStream_t)stream;
+  if (p.update && !attn_tc_fuses_update(p)) {
+    // the kernel cannot store this window itself: the attention, then the splice kernel (the block's
+    // fresh rows are the whole fresh tensor only under DualCache)
+    if (blocks || !desc->dual_cache)
+      return fail(FDLLM_EUNSUPPORTED,
+                  "attn update: the window (block_size %d) must fill whole key tiles for per-sequence blocks or "
+                  "PrefixCache", desc->block_size);
+    p.update = 0;
+    st = cuda_status(attn_tc_supported(p) ? launch_attn_tc(p, cs) : launch_attn_simt(p, cs), "attn launch");
+    if (st != FDLLM_OK) return st;
+    const int64_t row_bytes = (int64_t)p.hkv * p.d * (p.in_bf16 ? 2 : 4);
+    return cuda_status(launch_splice(p.batch, p.seq_len, row_bytes, p.fresh0, p.win, p.kc_w, p.vc_w, k_fresh,
+                                     v_fresh, cs),
+                       "attn update: splice launch");
+  }
   return cuda_status(attn_tc_supported(p) ? launch_attn_tc(p, cs) : launch_attn_simt(p, cs), "attn launch");
 }
 
@@ -424,6 +449,14 @@ fdllm_status fdllm_block_attn_ragged(const fdllm_attn_desc *desc, const int32_t 
                                      size_t ws_bytes, fdllm_stream_t stream) {
   if (!block_idx) return fail(FDLLM_EINVAL, "attn: block_idx is null");
   return block_attn(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fresh, out, lse, workspace, ws_bytes, stream);
+}
+
+fdllm_status fdllm_block_attn_update(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
+                                     void *k_cache, void *v_cache, const void *k_fresh, const void *v_fresh,
+                                     void *out, float *lse, void *workspace, size_t ws_bytes,
+                                     fdllm_stream_t stream) {
+  return block_attn(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fresh, out, lse, workspace, ws_bytes, stream,
+                    nullptr, nullptr, true);
 }
 
 size_t fdllm_select_workspace_size(const fdllm_select_desc *desc) {

@@ -162,6 +162,10 @@ struct Args {
   const int32_t *blocks;   // per-sequence DualCache block indices (null: the plan's window for all)
   int prompt_len, nblocks;
   const float *k_scale, *v_scale;   // F8KV: scales of the cached rows [b, N, Hkv]
+  // cache update fused into the call: the first `win` fresh rows (the block) are stored into cache rows
+  // [f0, f0 + win) of each sequence by the CTAs that load them (those of the KV head group's first query
+  // tile), in boxes of `win_box` rows (0: no update)
+  int win, win_box;
 };
 
 // 4 E4M3 codes (one 32-bit word) times `sc` as 4 bf16 (two words); exact: an E4M3 value has at most
@@ -275,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
                    const __grid_constant__ CUtensorMap mva, const __grid_constant__ CUtensorMap mvf,
-                   const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mo, const Args a) {
+                   const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mo,
+                   const __grid_constant__ CUtensorMap mwk, const __grid_constant__ CUtensorMap mwv, const Args a) {
   using CF = Cfg<D>;
   constexpr int NS = CF::NS;
   constexpr int TK = kKeys / KVP;                      // keys of one KV head in a key tile
@@ -325,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the merge barrier expects the other C - 1 CTAs' rows of this one
     if (C > 1) tc::mbar_arrive_expect_tx(&br.mrg, (uint32_t)(C - 1) * seg_bytes);
     for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc, &mo}) tc::prefetch_tensormap(m);
+    if (a.win_box > 0) { tc::prefetch_tensormap(&mwk); tc::prefetch_tensormap(&mwv); }
   }
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
   // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
@@ -418,6 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool run = tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag);    // Q is in TMEM
       if (!run && !*abort_flag) fail(br, a.err, 212);
       int js = gg, jp = gg;                             // next S, next PV of this group
+      // this CTA stores the block's fresh K/V into the cache window when the call asks for it and it
+      // serves the first query tile of its KV head group (every such CTA of the split covers its own keys)
+      const bool update_cache = a.win_box > 0 && qt == 0;
+      bool stored_pending = false;
       uint64_t t0 = tc::globaltimer();
       for (uint32_t spin = 0; run && jp < nt; ++spin) {
         if (jp < js && tc::mbar_test_wait(&br.pfull[gg], (uint32_t)(jp >> 1) & 1u)) {
@@ -429,6 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16_ts(tmem + CF::O_COL + (uint32_t)(gg * D), tmem + CF::P_COL + (uint32_t)(gg * 32 + ks * 8),
                             tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::KVHALF), id_o, (jp >= 2) || ks != 0);
           tc::mma_commit(&br.pvdone[gg]);
+          if (stored_pending) {                         // the cache-window stores have read the stage
+            tc::bulk_wait_read_all();
+            stored_pending = false;
+          }
           tc::mma_commit(&br.kvempty[st]);
           jp += 2;
           t0 = tc::globaltimer();
@@ -444,6 +458,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::mma_bf16_ts(tmem + CF::S_COL + (uint32_t)(gg * kKeys), tmem + CF::Q_COL + (uint32_t)(ks * 8),
                             tc::sw128_desc(ka + (ks / 4) * CF::KVHALF + (uint32_t)((ks % 4) * 32)), id_s, ks != 0);
           tc::mma_commit(&br.sfull[gg]);
+          if (update_cache) {
+            // the block's fresh rows of this tile into the cache window (rows past the block lie outside
+            // the box); the stage is released only after the stores have read it (wait below)
+            const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + js);
+            if (kt.range == 1 && kt.row0 < a.win) {
+              unsigned char *ks_ = kv_s + st * CF::STAGE;
+              for (int dh = 0; dh < CF::DH; ++dh) {
+                tc::tma_store_4d(&mwk, ks_ + dh * CF::KVHALF, dh * 64, pl.f0 + kt.row0, kvh, b);
+                tc::tma_store_4d(&mwv, ks_ + CF::KV_BYTES + dh * CF::KVHALF, dh * 64, pl.f0 + kt.row0, kvh, b);
+              }
+              tc::bulk_commit_group();
+              stored_pending = true;
+            }
+          }
           js += 2;
           atomicExch(&br.consumed_g[gg], js >> 1);
           t0 = tc::globaltimer();
@@ -457,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (update_cache) tc::bulk_wait_all();           // the cache-window writes are complete
       tc::mma_commit(&br.drain);                        // both issuers arrive: count 2
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
     }
@@ -1056,6 +1085,14 @@ Plan make_plan(const AttnProblem &p) {
   return pl;
 }
 
+// Rows per cache-window store box: whole key tiles of one KV head's keys (tk rows, the block a multiple
+// of tk), or the block alone inside one tile of a single head; 0 when neither holds.
+int update_box_rows(const Plan &pl, int win) {
+  if (win % pl.tk == 0) return pl.tk;
+  if (win < pl.tk && pl.kvp == 1) return win;
+  return 0;
+}
+
 template <int D, int KVP, bool F8KV>
 cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cudaStream_t st) {
   auto k = attn_tc_kernel<D, KVP, F8KV>;
@@ -1075,7 +1112,8 @@ cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cud
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], a);
+  e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8],
+                         maps[9], a);
   count_launches(1);
   return e;
 }
@@ -1096,6 +1134,10 @@ cudaError_t dispatch_kvp(int d, const Plan &pl, const CUtensorMap *maps, const A
 
 bool attn_tc_supported(const AttnProblem &p) { return p.in_bf16 && (p.d == 64 || p.d == 128); }
 
+bool attn_tc_fuses_update(const AttnProblem &p) {
+  return attn_tc_supported(p) && !p.f8kv && update_box_rows(make_plan(p), p.win) > 0;
+}
+
 size_t attn_tc_workspace(const AttnProblem &) { return 0; }
 
 cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
@@ -1104,7 +1146,7 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t cstride = (int64_t)p.seq_len * p.hkv * p.d;  // cache batch stride
   const int64_t fstride = (int64_t)p.nq * p.hkv * p.d;       // fresh batch stride
   const int64_t qstride = (int64_t)p.nq * p.hq * p.d;
-  CUtensorMap maps[8];
+  CUtensorMap maps[10];
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
   // per-sequence blocks: prefix and suffix tiles are read through maps of the whole cache; rows of a
   // sequence's own window that fall in a boundary tile are read and weighted by exactly zero
@@ -1131,8 +1173,19 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
          map4_kv(&maps[4], p.vc, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk, kvp, false) &&
          map4_kv(&maps[6], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk, kvp, false);
   }
+  // the cache-window store maps: the whole caches, boxes of win_box rows (unused copies otherwise)
+  int win_box = 0;
+  if (p.update) {
+    win_box = update_box_rows(pl, p.win);
+    if (win_box > 0)
+      ok = ok && map4_kv(&maps[8], p.kc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false) &&
+           map4_kv(&maps[9], p.vc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false);
+  }
+  if (win_box == 0) maps[8] = maps[9] = maps[1];
   if (!ok) return cudaErrorInvalidValue;
   Args a;
+  a.win = p.update ? p.win : 0;
+  a.win_box = win_box;
   a.pl = pl;
   a.batch = p.batch; a.n = p.seq_len; a.nq = p.nq; a.hq = p.hq; a.hkv = p.hkv; a.group = group;
   a.scale = p.scale;

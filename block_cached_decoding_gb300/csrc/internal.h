@@ -25,6 +25,10 @@ struct AttnProblem {
   int f8kv;
   const float *k_scale, *v_scale;
   int out_f32;
+  // cache-window update fused into the call (update = 1): cache rows [s, s + win) of each sequence <-
+  // the first `win` fresh rows; kc_w / vc_w are the caches, writable
+  int update, win;
+  void *kc_w, *vc_w;
   const void *q, *kc, *vc, *kf, *vf;
   void *out;
   float *lse;
@@ -76,6 +80,9 @@ cudaError_t launch_attn_simt(const AttnProblem &p, cudaStream_t st);
 bool attn_tc_supported(const AttnProblem &p);
 size_t attn_tc_workspace(const AttnProblem &p);
 cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st);
+// whether launch_attn_tc stores the cache window itself for p (p.update): the block's rows must fill
+// whole key tiles of the kernel's plan, or be a single head's rows within one tile
+bool attn_tc_fuses_update(const AttnProblem &p);
 
 // lmhead_simt.cu: per-split vocabulary partials for the masked rows
 int lmhead_simt_splits(const SelectProblem &p);

@@ -29,7 +29,7 @@ EXPORTS = (
     "fdllm_kv_splice_ragged", "fdllm_quantize_fp8_rows", "fdllm_select_fp8w_workspace_size",
     "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8", "fdllm_block_loop_create",
     "fdllm_block_loop_launch", "fdllm_block_loop_destroy", "fdllm_synth_rows_at", "fdllm_synth_hidden_at",
-    "fdllm_kv_splice_fp8_ragged",
+    "fdllm_kv_splice_fp8_ragged", "fdllm_block_attn_update",
 )
 
 # void step(void *user, fdllm_stream_t stream)
@@ -87,6 +87,8 @@ def lib() -> C.CDLL:
         L.fdllm_kv_splice.restype = i32
         L.fdllm_block_attn_ragged.argtypes = [C.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.fdllm_block_attn_ragged.restype = i32
+        L.fdllm_block_attn_update.argtypes = [C.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.fdllm_block_attn_update.restype = i32
         L.fdllm_confidence_select_ragged.argtypes = [C.POINTER(SelectDesc)] + [vp] * 10 + [sz, vp]
         L.fdllm_confidence_select_ragged.restype = i32
         L.fdllm_kv_splice_ragged.argtypes = [i32] * 4 + [vp, i32, i32] + [vp] * 5
@@ -249,6 +251,17 @@ def fdllm_block_attn_ragged(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fre
     if ws_bytes is None:
         ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().fdllm_block_attn_ragged(C.byref(desc), _ptr(block_idx), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(k_fresh), _ptr(v_fresh), _ptr(out), _ptr(lse), _ptr(workspace),
+                                         ws_bytes, _stream(stream)))
+
+
+def fdllm_block_attn_update(desc, block_idx, q, k_cache, v_cache, k_fresh, v_fresh, out, lse=None,
+                            workspace=None, ws_bytes=None, stream=None):
+    """fdllm_block_attn (block_idx None) or its per-sequence form, plus the cache-window update: cache rows
+    [s_b, s_b + block_size) <- the block's fresh K/V."""
+    if ws_bytes is None:
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fdllm_block_attn_update(C.byref(desc), _ptr(block_idx), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                          _ptr(k_fresh), _ptr(v_fresh), _ptr(out), _ptr(lse), _ptr(workspace),
                                          ws_bytes, _stream(stream)))
 

@@ -252,15 +252,42 @@ fdllm_status fdllm_kv_splice(int32_t mode, int32_t batch, int32_t seq_len, int32
  * sequence b at block block_idx[b] (device int32 [batch], in
  * [0, gen_length / block_size)); desc->block_idx is only validated.  q, k_fresh,
  * v_fresh and out are [b, block_size, H, d] as for fdllm_block_attn.  Rows of
- * sequence b's own window [s_b, s_b + block_size) in the caches are read where
- * a key tile crosses the window's edge and weighted by exactly zero, so they
- * must hold finite values (any earlier keys and values, or zeros).  Needs the
+ * sequence b's own window [s_b, s_b + block_size) in the caches may be loaded
+ * where a key tile crosses the window's edge, but they never reach the result:
+ * their scores are excluded and their values are replaced by zeros before the
+ * product, so they may hold anything (NaN and Inf included).  Needs the
  * workspace of fdllm_attn_workspace_size(desc).  FDLLM_EUNSUPPORTED for fp32 or
  * without DualCache. */
 fdllm_status fdllm_block_attn_ragged(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
                                      const void *k_cache, const void *v_cache, const void *k_fresh,
                                      const void *v_fresh, void *out, float *lse, void *workspace,
                                      size_t ws_bytes, fdllm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Block attention with the cache-window update                              */
+/* ------------------------------------------------------------------------ */
+/* The summary's fused cache update (section 3.4.2 "Cache Overhead and Fused
+ * Updates"): after a denoising step the block's freshly computed keys and
+ * values replace the cache window, and writing them from the attention call
+ * itself -- which has just read them -- saves the separate copy and its re-read.
+ *
+ * fdllm_block_attn (block_idx NULL) or fdllm_block_attn_ragged (block_idx
+ * non-NULL, DualCache) plus, for every sequence b, cache rows [s_b, s_b +
+ * block_size) <- the first block_size fresh rows (k_fresh / v_fresh rows 0 ..
+ * block_size - 1, the block), exactly as fdllm_kv_splice(FDLLM_SPLICE_WINDOW,
+ * ..., s_b, block_size) would after the attention.  The attention reads no cache
+ * row of the window (DualCache reads the block's fresh keys there; PrefixCache
+ * reads only [0, s)), so the result equals the two separate calls.  Arguments
+ * and errors as fdllm_block_attn; k_cache and v_cache are written.  Requires
+ * use_cache = 1 (else FDLLM_EUNSUPPORTED).  When the kernel cannot store the
+ * window itself -- the block does not fill whole key tiles of its plan, or fp32
+ * inputs -- a DualCache call with block_idx NULL launches the splice kernel after
+ * the attention (two kernels); per-sequence blocks and PrefixCache then return
+ * FDLLM_EUNSUPPORTED. */
+fdllm_status fdllm_block_attn_update(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
+                                     void *k_cache, void *v_cache, const void *k_fresh, const void *v_fresh,
+                                     void *out, float *lse, void *workspace, size_t ws_bytes,
+                                     fdllm_stream_t stream);
 
 /* fdllm_confidence_select with sequence b's block starting at block_start[b]
  * (device int32 [batch], in [0, seq_len - block_size]); desc->block_start is
@@ -326,9 +353,10 @@ fdllm_status fdllm_confidence_select_fp8w(const fdllm_select_desc *desc, const v
  * an FP8 cache: the result is the attention over the dequantised cache
  * (code * scale, exact in bf16).  desc->dtype must be FDLLM_BF16 and
  * desc->use_cache 1 (PrefixCache or DualCache), else FDLLM_EUNSUPPORTED; null
- * scales give FDLLM_EINVAL.  Cache rows at the fresh positions are read only
- * where a key tile crosses a range edge, weighted by exactly zero: they must
- * hold finite values (any codes written by fdllm_kv_splice_fp8 or zeros). */
+ * scales give FDLLM_EINVAL.  Cache rows at the fresh positions (codes and
+ * scales) may be loaded where a key tile crosses a range edge but never reach
+ * the result (their keys and values are replaced by zeros), so they may hold
+ * anything. */
 fdllm_status fdllm_block_attn_fp8kv(const fdllm_attn_desc *desc, const int32_t *block_idx, const void *q,
                                    const uint8_t *k_cache, const float *k_scale, const uint8_t *v_cache,
                                    const float *v_scale, const void *k_fresh, const void *v_fresh, void *out,
@@ -410,7 +438,8 @@ fdllm_status fdllm_last_device_error(fdllm_stream_t stream, int32_t *detail);
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream);
 
 /* ABI version: 100 * major + minor (101: the per-sequence block calls; 102: the
- * FP8 weight cache; 103: the FP8 KV cache; 104: the device-driven block loop). */
+ * FP8 weight cache; 103: the FP8 KV cache; 104: the device-driven block loop;
+ * 105: fdllm_block_attn_update and the loop's refresh every r steps). */
 int32_t fdllm_version(void);
 
 /* Number of kernels this library has launched in the process so far (all

@@ -49,10 +49,12 @@ def test_refresh_then_window_splice_bit_exact(dtype):
 
 
 def run_case(*, batch, prompt_len, gen_length, block_size, hq, hkv, d, mode, out_f32=1, block_idx=0, blocks=None,
-             seed=7, step=0):
+             seed=7, step=0, poison=False):
     """The cache is drawn in bf16 and written to FP8 by fdllm_kv_splice_fp8 (REFRESH), checked
     against the oracle's codes; the attention is compared with the oracle's over the dequantised
-    cache.  `blocks` (a list): sequence b at block blocks[b] (DualCache only)."""
+    cache.  `blocks` (a list): sequence b at block blocks[b] (DualCache only).  `poison`: each
+    sequence's own window rows of the FP8 cache get NaN codes and NaN scales (rows the attention
+    must not use) after the check of the codes."""
     dtype = "bf16"
     n = prompt_len + gen_length
     kc = synth.kv_cache(seed, synth.KIND_KCACHE, batch, n, hkv, d, 0, dtype)
@@ -68,6 +70,12 @@ def run_case(*, batch, prompt_len, gen_length, block_size, hq, hkv, d, mode, out
     k64, v64 = O.dequantize_kv_rows(want_kq, want_ks), O.dequantize_kv_rows(want_vq, want_vs)
     ks_per = blocks if blocks is not None else [block_idx] * batch
     windows = [O.block_window(prompt_len, block_size, k) for k in ks_per]
+    if poison:
+        for bi, (s0, e0) in enumerate(windows):
+            kq[bi, s0:e0] = 0x7F                           # E4M3 NaN
+            vq[bi, s0:e0] = 0xFF
+            ksc[bi, s0:e0] = float("nan")
+            vsc[bi, s0:e0] = float("inf")
     nq = block_size if mode == "dual" else n - windows[0][0]
     q = np.empty((batch, nq, hq, d), dtype=np.uint16)
     kf = np.empty((batch, nq, hkv, d), dtype=np.uint16)
@@ -129,6 +137,14 @@ def test_heads_packed_per_tile():
 def test_each_sequence_at_its_own_block():
     run_case(batch=4, prompt_len=70, gen_length=128, block_size=32, hq=4, hkv=4, d=128, mode="dual",
              blocks=[2, 0, 3, 1])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_rows_holding_nan_do_not_reach_the_output(d):
+    """NaN codes and NaN / Inf scales in each sequence's own window rows (read with weight zero where a
+    key tile crosses the window's edge) leave the output finite and equal to the oracle's."""
+    run_case(batch=4, prompt_len=70, gen_length=128, block_size=32, hq=4, hkv=4, d=d, mode="dual",
+             blocks=[2, 0, 3, 1], poison=True)
 
 
 @pytest.mark.parametrize("k", [0, -9, 5, -111, 111])

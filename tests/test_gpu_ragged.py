@@ -40,10 +40,11 @@ def seq_cache(seed, kind, b, n, hkv, d, epoch, dtype):
 # ---------------------------------------------------------------------------
 
 def ragged_attention_case(*, blocks, prompt_len, gen_length, block_size, hq, hkv, d, out_f32, seed=3, step=0,
-                          bad=None):
+                          bad=None, poison=False):
     """Sequence b at block blocks[b]; returns the worst relative L2 over valid sequences.
 
-    `bad` (a sequence index) has its block index replaced by an out-of-range one."""
+    `bad` (a sequence index) has its block index replaced by an out-of-range one.  `poison` writes NaN
+    and Inf into each sequence's own window rows of the cache (rows the attention must not use)."""
     batch = len(blocks)
     n = prompt_len + gen_length
     dtype = "bf16"
@@ -60,6 +61,13 @@ def ragged_attention_case(*, blocks, prompt_len, gen_length, block_size, hq, hkv
     idx = list(blocks)
     if bad is not None:
         idx[bad] = gen_length // block_size
+    kc_in, vc_in = kc, vc
+    if poison:
+        kc_in, vc_in = kc.copy(), vc.copy()
+        for b, k in enumerate(blocks):
+            s, e = O.block_window(prompt_len, block_size, k)
+            kc_in[b, s:e] = 0x7FC0                       # bf16 NaN
+            vc_in[b, s:e] = 0x7F80                       # bf16 +Inf
     desc = F.attn_desc(batch=batch, prompt_len=prompt_len, gen_length=gen_length, block_size=block_size,
                        block_idx=0, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, use_cache=1, dual_cache=1,
                        dtype=F.BF16, out_f32=out_f32)
@@ -69,7 +77,7 @@ def ragged_attention_case(*, blocks, prompt_len, gen_length, block_size, hq, hkv
     wsb = F.fdllm_attn_workspace_size(desc)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
     assert F.fdllm_last_device_error() == (F.OK, 0)
-    F.fdllm_block_attn_ragged(desc, _ints(idx), dev(q, dtype), dev(kc, dtype), dev(vc, dtype), dev(kf, dtype),
+    F.fdllm_block_attn_ragged(desc, _ints(idx), dev(q, dtype), dev(kc_in, dtype), dev(vc_in, dtype), dev(kf, dtype),
                               dev(vf, dtype), out, lse, ws, ws_bytes=wsb)
     torch.cuda.synchronize()
     err = F.fdllm_last_device_error()
@@ -99,6 +107,18 @@ def ragged_attention_case(*, blocks, prompt_len, gen_length, block_size, hq, hkv
 def test_attention_each_sequence_at_its_own_block(blocks, prompt, gen, B, hq, hkv, d, out_f32):
     ragged_attention_case(blocks=blocks, prompt_len=prompt, gen_length=gen, block_size=B, hq=hq, hkv=hkv, d=d,
                           out_f32=out_f32)
+
+
+@pytest.mark.parametrize("blocks,prompt,gen,B,hq,hkv,d", [
+    ([2, 0, 3, 1], 70, 128, 32, 4, 4, 128),           # windows off the 64-key tile boundaries
+    ([1, 2], 77, 60, 20, 4, 4, 64),                   # block size off the key tile
+])
+def test_window_rows_holding_nan_and_inf_do_not_reach_the_output(blocks, prompt, gen, B, hq, hkv, d):
+    """A key tile at the edge of the prefix reads cache rows of the sequence's own window with weight
+    zero; NaN keys and infinite values there must leave the output finite and equal to the oracle's
+    (which never reads those rows)."""
+    ragged_attention_case(blocks=blocks, prompt_len=prompt, gen_length=gen, block_size=B, hq=hq, hkv=hkv, d=d,
+                          out_f32=1, poison=True)
 
 
 def test_attention_heads_packed_per_tile():
