@@ -10,7 +10,11 @@
 // the body starts with the loop's condition set, so it runs at least once.
 //
 // The graph: [reset the step counter] -> [while (condition) { body }], body =
-// [captured step] -> [control].
+// [captured step] -> [control]; with a cache refresh every r steps (the
+// refresh-every-r-steps cache variant of the summary's section 5, Table 10),
+// body = [if (refresh condition) { captured refresh }] -> [captured step] ->
+// [control], the control kernel setting the refresh condition for step c of
+// the block when r divides c.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,8 +28,12 @@ namespace {
 
 __global__ void loop_reset_kernel(int64_t *counter) { *counter = 0; }
 
+// After the step that brought the counter to c: keep looping while some sequence has a masked position
+// and c < max_steps; with a refresh every r steps, arm the refresh node of the next iteration when r
+// divides c (the step about to run is step c of the block, and the cache refresh comes first).
 __global__ void loop_control_kernel(cudaGraphConditionalHandle cond, const int32_t *__restrict__ n_left,
-                                    int batch, int64_t *counter, int64_t *total, int64_t max_steps) {
+                                    int batch, int64_t *counter, int64_t *total, int64_t max_steps,
+                                    cudaGraphConditionalHandle refresh_cond, int64_t refresh_every) {
   __shared__ int any;
   if (threadIdx.x == 0) any = 0;
   __syncthreads();
@@ -37,6 +45,7 @@ __global__ void loop_control_kernel(cudaGraphConditionalHandle cond, const int32
     *counter = c;
     if (total != nullptr) *total += 1;
     cudaGraphSetConditional(cond, any && c < max_steps ? 1u : 0u);
+    if (refresh_every > 0) cudaGraphSetConditional(refresh_cond, c % refresh_every == 0 ? 1u : 0u);
   }
 }
 
@@ -45,11 +54,12 @@ __global__ void loop_control_kernel(cudaGraphConditionalHandle cond, const int32
 
 using namespace fdllm;
 
-extern "C" fdllm_status fdllm_block_loop_create(fdllm_block_loop **out, fdllm_step_fn step, void *user,
-                                                const int32_t *n_masked_left, int32_t batch, int32_t max_steps,
-                                                int64_t *step_counter, int64_t *total_steps) {
+static fdllm_status loop_create(fdllm_block_loop **out, fdllm_step_fn step, fdllm_step_fn refresh, void *user,
+                                const int32_t *n_masked_left, int32_t batch, int32_t max_steps,
+                                int32_t refresh_every, int64_t *step_counter, int64_t *total_steps) {
   if (!out || !step || !n_masked_left || !step_counter) return FDLLM_EINVAL;
-  if (batch < 1 || max_steps < 1) return FDLLM_EINVAL;
+  if (batch < 1 || max_steps < 1 || refresh_every < 0) return FDLLM_EINVAL;
+  if (refresh_every > 0 && !refresh) return FDLLM_EINVAL;
   *out = nullptr;
   cudaGraph_t g = nullptr;
   cudaStream_t cs = nullptr;
@@ -78,11 +88,38 @@ extern "C" fdllm_status fdllm_block_loop_create(fdllm_block_loop **out, fdllm_st
     if (e == cudaSuccess) body = cp.conditional.phGraph_out[0];
   }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed);
+  // with a refresh every r steps, the body starts with an IF node holding the captured refresh; its
+  // condition is 0 at each launch (the caller refreshes before step 0) and set by the control kernel
+  cudaGraphConditionalHandle rcond = 0;
+  cudaGraphNode_t ifnode = nullptr;
+  if (e == cudaSuccess && refresh_every > 0) {
+    e = cudaGraphConditionalHandleCreate(&rcond, body, 0, cudaGraphCondAssignDefault);
+    cudaGraph_t if_body = nullptr;
+    if (e == cudaSuccess) {
+      cudaGraphNodeParams ip = {};
+      ip.type = cudaGraphNodeTypeConditional;
+      ip.conditional.handle = rcond;
+      ip.conditional.type = cudaGraphCondTypeIf;
+      ip.conditional.size = 1;
+      e = cudaGraphAddNode(&ifnode, body, nullptr, nullptr, 0, &ip);
+      if (e == cudaSuccess) if_body = ip.conditional.phGraph_out[0];
+    }
+    if (e == cudaSuccess) e = cudaStreamBeginCaptureToGraph(cs, if_body, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed);
+    if (e == cudaSuccess) {
+      refresh(user, (fdllm_stream_t)cs);
+      const cudaError_t le = cudaGetLastError();
+      cudaGraph_t captured_if = nullptr;
+      e = cudaStreamEndCapture(cs, &captured_if);
+      if (e == cudaSuccess) e = le;
+    }
+  }
+  if (e == cudaSuccess)
+    e = cudaStreamBeginCaptureToGraph(cs, body, ifnode ? &ifnode : nullptr, nullptr, ifnode ? 1 : 0,
+                                      cudaStreamCaptureModeRelaxed);
   if (e == cudaSuccess) {
     step(user, (fdllm_stream_t)cs);
     loop_control_kernel<<<1, 256, 0, cs>>>(cond, n_masked_left, batch, step_counter, total_steps,
-                                           (int64_t)max_steps);
+                                           (int64_t)max_steps, rcond, (int64_t)refresh_every);
     const cudaError_t le = cudaGetLastError();
     e = cudaStreamEndCapture(cs, &captured);
     if (e == cudaSuccess) e = le;
@@ -96,6 +133,22 @@ extern "C" fdllm_status fdllm_block_loop_create(fdllm_block_loop **out, fdllm_st
   }
   *out = new fdllm_block_loop{g, exec};
   return FDLLM_OK;
+}
+
+extern "C" fdllm_status fdllm_block_loop_create(fdllm_block_loop **out, fdllm_step_fn step, void *user,
+                                                const int32_t *n_masked_left, int32_t batch, int32_t max_steps,
+                                                int64_t *step_counter, int64_t *total_steps) {
+  return loop_create(out, step, nullptr, user, n_masked_left, batch, max_steps, 0, step_counter, total_steps);
+}
+
+extern "C" fdllm_status fdllm_block_loop_create_refresh(fdllm_block_loop **out, fdllm_step_fn step,
+                                                        fdllm_step_fn refresh, void *user,
+                                                        const int32_t *n_masked_left, int32_t batch,
+                                                        int32_t max_steps, int32_t refresh_every,
+                                                        int64_t *step_counter, int64_t *total_steps) {
+  if (refresh_every < 1) return FDLLM_EINVAL;
+  return loop_create(out, step, refresh, user, n_masked_left, batch, max_steps, refresh_every, step_counter,
+                     total_steps);
 }
 
 extern "C" fdllm_status fdllm_block_loop_launch(fdllm_block_loop *loop, fdllm_stream_t stream) {

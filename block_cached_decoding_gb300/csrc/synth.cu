@@ -46,8 +46,10 @@ __global__ void normals_kernel(uint64_t key, int64_t n, int64_t offset, float si
 
 // one stream per (b, epoch): out [b, per]
 template <typename T>
-__global__ void kv_kernel(uint64_t seed, int kind, int64_t epoch, int64_t per, float sigma, T *out) {
+__global__ void kv_kernel(uint64_t seed, int kind, int64_t epoch, int64_t per, float sigma, T *out,
+                          const int64_t *epoch_add = nullptr, int64_t epoch_div = 1) {
   const int b = blockIdx.y;
+  if (epoch_add != nullptr) epoch += *epoch_add / epoch_div;
   const uint64_t key = splitmix(splitmix(splitmix(seed, (uint64_t)kind), (uint64_t)b), (uint64_t)epoch);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -130,16 +132,24 @@ extern "C" int32_t fdllm_synth_kv_cache(uint64_t seed, int32_t kind, int32_t bat
                                         int32_t n_kv_heads, int32_t head_dim, int64_t epoch,
                                         float sigma, int32_t dtype, void *out,
                                         fdllm_stream_t stream) {
-  if (batch < 1 || batch > 65535 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1 || !out ||
+  return fdllm_synth_kv_cache_at(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch, nullptr, 1, sigma, dtype,
+                                 out, stream);
+}
+
+extern "C" int32_t fdllm_synth_kv_cache_at(uint64_t seed, int32_t kind, int32_t batch, int32_t seq_len,
+                                           int32_t n_kv_heads, int32_t head_dim, int64_t epoch,
+                                           const int64_t *epoch_add, int64_t epoch_div, float sigma, int32_t dtype,
+                                           void *out, fdllm_stream_t stream) {
+  if (batch < 1 || batch > 65535 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1 || !out || epoch_div < 1 ||
       (dtype != FDLLM_BF16 && dtype != FDLLM_F32))
     return FDLLM_EINVAL;
   const int64_t per = (int64_t)seq_len * n_kv_heads * head_dim;
   dim3 grid(grid_for(per) / (unsigned)batch + 1, batch);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
-    kv_kernel<<<grid, 256, 0, st>>>(seed, kind, epoch, per, sigma, (__nv_bfloat16 *)out);
+    kv_kernel<<<grid, 256, 0, st>>>(seed, kind, epoch, per, sigma, (__nv_bfloat16 *)out, epoch_add, epoch_div);
   else
-    kv_kernel<<<grid, 256, 0, st>>>(seed, kind, epoch, per, sigma, (float *)out);
+    kv_kernel<<<grid, 256, 0, st>>>(seed, kind, epoch, per, sigma, (float *)out, epoch_add, epoch_div);
   return finish();
 }
 

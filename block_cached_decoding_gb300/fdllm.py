@@ -29,7 +29,8 @@ EXPORTS = (
     "fdllm_kv_splice_ragged", "fdllm_quantize_fp8_rows", "fdllm_select_fp8w_workspace_size",
     "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8", "fdllm_block_loop_create",
     "fdllm_block_loop_launch", "fdllm_block_loop_destroy", "fdllm_synth_rows_at", "fdllm_synth_hidden_at",
-    "fdllm_kv_splice_fp8_ragged", "fdllm_block_attn_update",
+    "fdllm_kv_splice_fp8_ragged", "fdllm_block_attn_update", "fdllm_block_loop_create_refresh",
+    "fdllm_synth_kv_cache_at",
 )
 
 # void step(void *user, fdllm_stream_t stream)
@@ -127,12 +128,15 @@ def lib() -> C.CDLL:
         L.fdllm_synth_hidden_at.argtypes = [u64, i32, i64, vp, i32, i32, i32, i32, C.c_double, vp, i32, vp, vp]
         L.fdllm_block_loop_create.argtypes = [C.POINTER(vp), STEP_FN, vp, vp, i32, i32, vp, vp]
         L.fdllm_block_loop_create.restype = i32
+        L.fdllm_block_loop_create_refresh.argtypes = [C.POINTER(vp), STEP_FN, STEP_FN, vp, vp, i32, i32, i32, vp, vp]
+        L.fdllm_block_loop_create_refresh.restype = i32
+        L.fdllm_synth_kv_cache_at.argtypes = [u64, i32, i32, i32, i32, i32, i64, vp, i64, C.c_float, i32, vp, vp]
         L.fdllm_block_loop_launch.argtypes = [vp, vp]
         L.fdllm_block_loop_launch.restype = i32
         L.fdllm_block_loop_destroy.argtypes = [vp]
         L.fdllm_block_loop_destroy.restype = None
         for f in ("fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
-                  "fdllm_synth_prompt", "fdllm_synth_rows_at", "fdllm_synth_hidden_at"):
+                  "fdllm_synth_prompt", "fdllm_synth_rows_at", "fdllm_synth_hidden_at", "fdllm_synth_kv_cache_at"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -343,6 +347,13 @@ def fdllm_synth_kv_cache(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch
                                       _ptr(out), _stream(stream)))
 
 
+def fdllm_synth_kv_cache_at(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch, epoch_add, epoch_div, sigma,
+                            dtype, out, stream=None):
+    """fdllm_synth_kv_cache with the epoch epoch + *epoch_add // epoch_div (epoch_add: device int64)."""
+    _check(lib().fdllm_synth_kv_cache_at(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch, _ptr(epoch_add),
+                                         epoch_div, sigma, dtype, _ptr(out), _stream(stream)))
+
+
 def fdllm_synth_rows(seed, kind, batch, step, pos0, npos, width, sigma, dtype, out, stream=None):
     _check(lib().fdllm_synth_rows(seed, kind, batch, step, pos0, npos, width, sigma, dtype, _ptr(out),
                                   _stream(stream)))
@@ -370,20 +381,29 @@ class BlockLoop:
     until n_masked_left is all zero or max_steps steps have run; `counter` (device int64) counts them per
     launch, `total` (device int64 or None) across launches."""
 
-    def __init__(self, step, n_masked_left, batch, max_steps, counter, total=None):
+    def __init__(self, step, n_masked_left, batch, max_steps, counter, total=None, refresh=None, refresh_every=0):
+        """With `refresh(stream)` and refresh_every = r, fdllm_block_loop_create_refresh: the captured refresh
+        runs before step c of each launch whenever c > 0 and r divides c."""
         self._h = None
         errors = []
 
-        def body(user, stream):
-            try:
-                step(stream)
-            except BaseException as e:           # an exception cannot cross the C frame: keep it
-                errors.append(e)
+        def wrap(fn):
+            def body(user, stream):
+                try:
+                    fn(stream)
+                except BaseException as e:       # an exception cannot cross the C frame: keep it
+                    errors.append(e)
+            return body
 
-        self._cb = STEP_FN(body)                 # kept alive with the loop
+        self._cb = STEP_FN(wrap(step))           # kept alive with the loop
         h = C.c_void_p()
-        st = lib().fdllm_block_loop_create(C.byref(h), self._cb, None, _ptr(n_masked_left), batch, max_steps,
-                                           _ptr(counter), _ptr(total))
+        if refresh is not None and refresh_every:
+            self._rcb = STEP_FN(wrap(refresh))
+            st = lib().fdllm_block_loop_create_refresh(C.byref(h), self._cb, self._rcb, None, _ptr(n_masked_left),
+                                                       batch, max_steps, refresh_every, _ptr(counter), _ptr(total))
+        else:
+            st = lib().fdllm_block_loop_create(C.byref(h), self._cb, None, _ptr(n_masked_left), batch, max_steps,
+                                               _ptr(counter), _ptr(total))
         if st == OK:
             self._h = h
         if errors:

@@ -156,8 +156,7 @@ class BlockDecoder:
         the running device step index, the attention and the select -- repeats on the device until the
         block has no mask.  Returns the loops and the device counters (steps per block, running total)."""
         wl = self.wl
-        if self.refresh_interval:
-            raise ValueError("graph loops refresh the cache only at block boundaries")
+        r = self.refresh_interval or 0
         cap = max_steps_per_block or wl.block_size
         nb = wl.gen_length // wl.block_size
         dev = self.w.device
@@ -186,7 +185,16 @@ class BlockDecoder:
                 F.fdllm_confidence_select(sdesc, self.hidden, self.w, self.tokens, self.unmasked, self.conf,
                                           self.kappa, self.argmax, self.n_left, self.sel_ws, stream=stream)
 
-            loops.append(F.BlockLoop(step, self.n_left, b, cap, per_block[k:k + 1], total))
+            def refresh(stream, k=k, counter=per_block[k:k + 1]):
+                # the caches of epoch k * 1000 + (step in block) // r, the step read from the loop's counter
+                for kind, stage in ((F.SYNTH_KCACHE, self.k_stage), (F.SYNTH_VCACHE, self.v_stage)):
+                    F.fdllm_synth_kv_cache_at(wl.seed, kind, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim,
+                                              k * 1000, counter, r, 1.0, self.code, stage, stream)
+                F.fdllm_kv_splice(F.SPLICE_REFRESH, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim, 0, wl.seq_len,
+                                  self.code, self.kc, self.vc, self.k_stage, self.v_stage, stream=stream)
+
+            loops.append(F.BlockLoop(step, self.n_left, b, cap, per_block[k:k + 1], total,
+                                     refresh=refresh if r else None, refresh_every=r))
         return loops, per_block, total
 
     def run_graph(self, max_steps_per_block: int | None = None, loops=None):

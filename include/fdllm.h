@@ -407,6 +407,20 @@ fdllm_status fdllm_block_loop_create(fdllm_block_loop **loop, fdllm_step_fn step
                                      const int32_t *n_masked_left, int32_t batch, int32_t max_steps,
                                      int64_t *step_counter, int64_t *total_steps);
 
+/* The same loop with the cache refreshed every `refresh_every` steps inside the
+ * block (the summary's refresh-every-r-steps cache, section 5 Table 10, reported
+ * for LLaDA-V): `refresh` is called once, with a capture stream, and must enqueue
+ * the refresh (the recomputed caches written with FDLLM_SPLICE_REFRESH); it runs
+ * on the device before step c of a launch whenever c > 0 and refresh_every
+ * divides c (the caller refreshes before step 0, at the block boundary).
+ * Captured work may read *step_counter (step c of the block) to key the refresh.
+ * FDLLM_EINVAL for refresh_every < 1 or a null refresh, else as
+ * fdllm_block_loop_create. */
+fdllm_status fdllm_block_loop_create_refresh(fdllm_block_loop **loop, fdllm_step_fn step, fdllm_step_fn refresh,
+                                             void *user, const int32_t *n_masked_left, int32_t batch,
+                                             int32_t max_steps, int32_t refresh_every, int64_t *step_counter,
+                                             int64_t *total_steps);
+
 /* Run the loop once on `stream` (asynchronous). */
 fdllm_status fdllm_block_loop_launch(fdllm_block_loop *loop, fdllm_stream_t stream);
 

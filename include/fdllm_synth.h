@@ -49,6 +49,13 @@ int32_t fdllm_synth_kv_cache(uint64_t seed, int32_t kind, int32_t batch, int32_t
                              int32_t n_kv_heads, int32_t head_dim, int64_t epoch, float sigma,
                              int32_t dtype, void *out, fdllm_stream_t stream);
 
+/* fdllm_synth_kv_cache with the epoch taken as epoch + *epoch_add / epoch_div, epoch_add a device int64
+ * read when the kernel runs (NULL: epoch alone; epoch_div >= 1): a cache refresh inside a captured CUDA
+ * graph whose step counter lives on the device (refresh epoch = base + step / r). */
+int32_t fdllm_synth_kv_cache_at(uint64_t seed, int32_t kind, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
+                                int32_t head_dim, int64_t epoch, const int64_t *epoch_add, int64_t epoch_div,
+                                float sigma, int32_t dtype, void *out, fdllm_stream_t stream);
+
 /* Per-position rows: out [b, npos, width]; row (b, p) uses key (seed, kind, b, step, pos0 + p). */
 int32_t fdllm_synth_rows(uint64_t seed, int32_t kind, int32_t batch, int64_t step, int32_t pos0,
                          int32_t npos, int32_t width, float sigma, int32_t dtype, void *out,

@@ -145,3 +145,50 @@ def test_device_driven_loop_stops_at_the_step_cap():
                                   head_dim=64, hidden=256, vocab=2000, mode="dual")
     with pytest.raises(RuntimeError, match="did not finish within 15 steps"):
         BlockDecoder(wl, tau=1.0).run_graph(max_steps_per_block=15)    # tau = 1: 16 steps per block
+
+
+@pytest.mark.parametrize("r", [1, 2, 4])
+def test_device_loop_refresh_every_r_steps(r):
+    """The refresh-every-r-steps cache inside the device-driven loop (a conditional graph node before step
+    c of a block whenever r divides c > 0, keyed by the loop's device step counter) gives the host loop's
+    tokens and step counts exactly; the host loop is itself checked against the oracle in lock step
+    (test_refresh_every_two_steps)."""
+    wl = configs.LLADA_BATCH.with_(batch=2, prompt_len=24, gen_length=32, block_size=16, n_q_heads=4, n_kv_heads=4,
+                                   head_dim=64, hidden=256, vocab=1500)
+    t_host, s_host = BlockDecoder(wl, tau=1.0, refresh_interval=r).run()
+    t_host = t_host.clone()
+    t_dev, s_dev = BlockDecoder(wl, tau=1.0, refresh_interval=r).run_graph()
+    assert s_dev == s_host == [16, 16]
+    assert torch.equal(t_dev, t_host)
+
+
+def test_refresh_every_step_equals_full_attention_on_the_gpu():
+    """With the cache refreshed from this step's keys and values at every position (refresh every step,
+    r = 1), the DualCache attention of the block equals the no-cache attention over the whole sequence
+    at the block's rows (the pages' exactness claim for a fresh cache), up to bf16 rounding of the
+    outputs, and both equal the oracle's full attention."""
+    b, P, G, B, k, h, d = 2, 40, 64, 16, 2, 4, 128
+    n = P + G
+    s = P + k * B
+    seed, step = 5, 3
+    full_k = synth.per_position(seed, synth.KIND_KFRESH, b, step, range(n), h * d, "bf16").reshape(b, n, h, d)
+    full_v = synth.per_position(seed, synth.KIND_VFRESH, b, step, range(n), h * d, "bf16").reshape(b, n, h, d)
+    q_all = synth.per_position(seed, synth.KIND_Q, b, step, range(n), h * d, "bf16").reshape(b, n, h, d)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    kc, vc = dev(full_k), dev(full_v)                      # the refreshed cache: this step's K/V everywhere
+    common = dict(batch=b, prompt_len=P, gen_length=G, block_size=B, block_idx=k, n_q_heads=h, n_kv_heads=h,
+                  head_dim=d, dtype=F.BF16, out_f32=1)
+    dual = F.attn_desc(use_cache=1, dual_cache=1, **common)
+    none = F.attn_desc(use_cache=0, dual_cache=0, **common)
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    o_dual = torch.empty(b, B, h, d, dtype=torch.float32, device="cuda")
+    o_full = torch.empty(b, n, h, d, dtype=torch.float32, device="cuda")
+    F.fdllm_block_attn(dual, dev(q_all[:, s:s + B]), kc, vc, dev(full_k[:, s:s + B]), dev(full_v[:, s:s + B]), o_dual,
+                       None, ws, ws_bytes=0)
+    F.fdllm_block_attn(none, dev(q_all), kc, vc, kc, vc, o_full, None, ws, ws_bytes=0)
+    torch.cuda.synchronize()
+    a, c = o_dual.cpu().numpy().astype(np.float64), o_full.cpu().numpy().astype(np.float64)[:, s:s + B]
+    assert_attention_close(a, c)                          # the same keys: equal up to bf16 rounding of P
+    f = lambda x: synth.as_f32(x, "bf16").astype(np.float64)
+    ref, _ = O.attention_full(f(q_all[:, s:s + B]), f(full_k), f(full_v), h, h)
+    assert_attention_close(a, ref)
