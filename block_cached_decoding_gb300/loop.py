@@ -46,7 +46,10 @@ class StepResult:
 class BlockDecoder:
     def __init__(self, wl: Workload, *, tau: float = 0.9, strategy: int = F.SELECT_THRESHOLD,
                  factor: float = 1.0, topk: int = 1, sigma_w: float | None = None, device: str = "cuda",
-                 refresh_interval: int | None = None):
+                 refresh_interval: int | None = None, w: torch.Tensor | None = None, fused_update: bool = False):
+        """`w`: an LM-head weight already drawn for this workload's (seed, sigma_w, vocab, hidden) to share
+        instead of drawing another; `fused_update`: each step's attention also writes the block's fresh K/V
+        into the cache window (fdllm_block_attn_update), as a serving loop would."""
         self.wl = wl
         self.refresh_interval = refresh_interval
         self.tau, self.strategy, self.factor, self.topk = tau, strategy, factor, topk
@@ -55,8 +58,13 @@ class BlockDecoder:
         self.code = F.F32 if wl.dtype == "f32" else F.BF16
         b, n, hq, hkv, d, B = wl.batch, wl.seq_len, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.block_size
         dev = torch.device(device)
-        self.w = torch.empty(wl.vocab, wl.hidden, dtype=self.dt, device=dev)
-        F.fdllm_synth_normals(wl.seed, F.SYNTH_W, [], wl.vocab * wl.hidden, 0, self.sigma_w, self.code, self.w)
+        self.fused_update = fused_update
+        if w is not None:
+            assert w.shape == (wl.vocab, wl.hidden) and w.dtype == self.dt
+            self.w = w
+        else:
+            self.w = torch.empty(wl.vocab, wl.hidden, dtype=self.dt, device=dev)
+            F.fdllm_synth_normals(wl.seed, F.SYNTH_W, [], wl.vocab * wl.hidden, 0, self.sigma_w, self.code, self.w)
         self.kc = torch.empty(b, n, hkv, d, dtype=self.dt, device=dev)
         self.vc = torch.empty_like(self.kc)
         self.k_stage = torch.empty_like(self.kc)
@@ -129,6 +137,19 @@ class BlockDecoder:
         F.fdllm_synth_hidden(wl.seed, b, g, s, wl.block_size, wl.hidden, wl.vocab, wl.p_plant, self.w, self.code,
                              self.hidden)
 
+    def attend(self, desc, q, kf, vf, out, stream=None):
+        """The step's block attention (with the cache-window update when the decoder fuses it)."""
+        if self.fused_update:
+            F.fdllm_block_attn_update(desc, None, q, self.kc, self.vc, kf, vf, out, None, self.attn_ws,
+                                      ws_bytes=self.attn_ws_bytes, stream=stream)
+        else:
+            F.fdllm_block_attn(desc, q, self.kc, self.vc, kf, vf, out, None, self.attn_ws, ws_bytes=self.attn_ws_bytes,
+                               stream=stream)
+
+    def reset_tokens(self):
+        """Every generated position masked again (the prompt kept): a fresh decode of the same prompt."""
+        self.tokens[:, self.wl.prompt_len:] = self.wl.mask_id
+
     def epoch(self, k: int, n: int) -> int:
         """Refresh epoch of the caches at step n (0-based) of block k."""
         r = self.refresh_interval
@@ -143,8 +164,7 @@ class BlockDecoder:
         b, hq, hkv, d = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
         q, out = _packed(self.q, (b, nq, hq, d)), _packed(self.attn_out, (b, nq, hq, d))
         kf, vf = _packed(self.kf, (b, nq, hkv, d)), _packed(self.vf, (b, nq, hkv, d))
-        F.fdllm_block_attn(self.attn_desc(k), q, self.kc, self.vc, kf, vf, out, None, self.attn_ws,
-                           ws_bytes=self.attn_ws_bytes)
+        self.attend(self.attn_desc(k), q, kf, vf, out)
         s = wl.prompt_len + k * wl.block_size
         F.fdllm_confidence_select(self.select_desc(s), self.hidden, self.w, self.tokens, self.unmasked, self.conf,
                                   self.kappa, self.argmax, self.n_left, self.sel_ws)
@@ -180,8 +200,7 @@ class BlockDecoder:
                                       stream)
                 F.fdllm_synth_hidden_at(wl.seed, b, 0, total, s, B, wl.hidden, wl.vocab, wl.p_plant, self.w,
                                         self.code, self.hidden, stream)
-                F.fdllm_block_attn(adesc, q, self.kc, self.vc, kf, vf, out, None, self.attn_ws,
-                                   ws_bytes=self.attn_ws_bytes, stream=stream)
+                self.attend(adesc, q, kf, vf, out, stream)
                 F.fdllm_confidence_select(sdesc, self.hidden, self.w, self.tokens, self.unmasked, self.conf,
                                           self.kappa, self.argmax, self.n_left, self.sel_ws, stream=stream)
 
@@ -197,6 +216,18 @@ class BlockDecoder:
                                      refresh=refresh if r else None, refresh_every=r))
         return loops, per_block, total
 
+    def launch_graph(self, loops):
+        """Launch every block's captured loop after its cache refresh, without waiting: returns the device
+        counters (steps per block) and the masked count left at the end of each block."""
+        graphs, per_block, total = loops
+        total.zero_()
+        left = torch.zeros(len(graphs), dtype=torch.int32, device=total.device)
+        for k, g in enumerate(graphs):
+            self.refresh(self.epoch(k, 0))
+            g.launch()
+            left[k] = self.n_left.max()             # stream-ordered, no host wait
+        return per_block, left
+
     def run_graph(self, max_steps_per_block: int | None = None, loops=None):
         """The same decode as `run` with every block a device-driven loop (`capture_blocks`, or the given
         capture): the host only launches each block's loop after its cache refresh and reads the step
@@ -206,13 +237,8 @@ class BlockDecoder:
         own = loops is None
         if own:
             loops = self.capture_blocks(max_steps_per_block)
-        graphs, per_block, total = loops
-        total.zero_()
-        left = torch.zeros(len(graphs), dtype=torch.int32, device=total.device)
-        for k, g in enumerate(graphs):
-            self.refresh(self.epoch(k, 0))
-            g.launch()
-            left[k] = self.n_left.max()             # stream-ordered, no host wait
+        graphs = loops[0]
+        per_block, left = self.launch_graph(loops)
         steps = per_block.tolist()                  # one synchronisation for the whole decode
         left = left.tolist()
         if own:

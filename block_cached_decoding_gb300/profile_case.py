@@ -3,6 +3,7 @@
     python -m block_cached_decoding_gb300.profile_case select --vocab 32768 --reps 3
     python -m block_cached_decoding_gb300.profile_case select --fp8w --reps 3
     python -m block_cached_decoding_gb300.profile_case attn --mode prefix --reps 3
+    python -m block_cached_decoding_gb300.profile_case attn --mode prefix --update --reps 3
     python -m block_cached_decoding_gb300.profile_case splice --reps 3
 
 Inputs come from the device twin of the seeded generator; shapes default to
@@ -35,6 +36,8 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fp8w", action="store_true", help="select through the FP8 weight cache")
     ap.add_argument("--fp8kv", action="store_true", help="attention over the FP8 KV cache")
+    ap.add_argument("--update", action="store_true",
+                    help="attention with the cache-window update (fdllm_block_attn_update)")
     ap.add_argument("--ragged", action="store_true",
                     help="per-sequence blocks: sequence i at block i mod (gen / block) (DualCache attention, select)")
     ap.add_argument("--time", action="store_true", help="report the mean call time over the reps (CUDA events)")
@@ -106,6 +109,9 @@ def main():
             if a.fp8kv:
                 F.fdllm_block_attn_fp8kv(d, blocks if a.ragged else None, q, kq, ksc, vq, vsc, kf, vf, out, None, ws,
                                          ws_bytes=wsb)
+            elif a.update:
+                F.fdllm_block_attn_update(d, blocks if a.ragged else None, q, kc, vc, kf, vf, out, None, ws,
+                                          ws_bytes=wsb)
             elif a.ragged:
                 F.fdllm_block_attn_ragged(d, blocks, q, kc, vc, kf, vf, out, None, ws, ws_bytes=wsb)
             else:

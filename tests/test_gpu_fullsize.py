@@ -109,10 +109,12 @@ def run_loop(wl, tau, sample_steps, w64, check_attn=True, attn_rows=12, attn_seq
 
 
 def test_llada_single_step_as_benchmarked():
-    """The benchmark's step: PrefixCache block 0, 256 queries over 768 positions, 32 masked rows."""
+    """The benchmark's step: PrefixCache block 0, 256 queries over 768 positions, 32 masked rows; the
+    attention writes the block's fresh K/V into the cache window in the same call, and its output is
+    checked in both output types (the benchmark times the bf16 one)."""
     wl = configs.LLADA_STEP
     w64 = weight_f64(wl.seed, wl.vocab, wl.hidden, wl.sigma_w)
-    dec = BlockDecoder(wl, tau=0.9)
+    dec = BlockDecoder(wl, tau=0.9, fused_update=True)
     dec.refresh(0)
     r = dec.step(0, 0)
     torch.cuda.synchronize()
@@ -120,6 +122,32 @@ def test_llada_single_step_as_benchmarked():
     _bound_exempt({"exempt": ex, "rows": rows, "checked": 1}, "llada8b prefix step")
     _check_attention(wl, dec, r, np.random.default_rng(0), n_seq=1, n_rows=None)   # all 256 query rows
     assert int(r.unmasked.sum()) >= 1
+    # the cache window now holds the block's fresh K/V, bit for bit; every other row is the refresh's
+    s, B = wl.prompt_len, wl.block_size
+    nq = wl.seq_len - s
+    shp = (wl.batch, nq, wl.n_kv_heads, wl.head_dim)
+    kf, vf = dec.kf.view(-1)[:kf_numel(shp)].view(shp), dec.vf.view(-1)[:kf_numel(shp)].view(shp)
+    assert torch.equal(dec.kc[:, s:s + B], kf[:, :B]) and torch.equal(dec.vc[:, s:s + B], vf[:, :B])
+    assert torch.equal(dec.kc[:, :s], dec.k_stage[:, :s]) and torch.equal(dec.kc[:, s + B:], dec.k_stage[:, s + B:])
+    assert torch.equal(dec.vc[:, :s], dec.v_stage[:, :s]) and torch.equal(dec.vc[:, s + B:], dec.v_stage[:, s + B:])
+    # bf16 output, as timed
+    out16 = torch.empty(wl.batch, nq, wl.n_q_heads, wl.head_dim, dtype=torch.bfloat16, device="cuda")
+    d16 = F.attn_desc(batch=wl.batch, prompt_len=wl.prompt_len, gen_length=wl.gen_length, block_size=B, block_idx=0,
+                      n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, head_dim=wl.head_dim, use_cache=1,
+                      dual_cache=0, dtype=F.BF16, out_f32=0)
+    qshp = (wl.batch, nq, wl.n_q_heads, wl.head_dim)
+    F.fdllm_block_attn_update(d16, None, dec.q.view(-1)[:kf_numel(qshp)].view(qshp), dec.kc, dec.vc, kf, vf, out16,
+                              None, dec.attn_ws, ws_bytes=dec.attn_ws_bytes)
+    torch.cuda.synchronize()
+    r16 = type(r)(**{**r.__dict__, "attn_out": out16})
+    _check_attention(wl, dec, r16, np.random.default_rng(0), n_seq=1, n_rows=None)
+
+
+def kf_numel(shape):
+    n = 1
+    for x in shape:
+        n *= x
+    return n
 
 
 @pytest.mark.parametrize("tau", [0.9, 1.0])
