@@ -13,8 +13,9 @@
 //   TMEM   Q (128 rows x d bf16, written once), S0 / S1 (64 fp32 score columns
 //          each), P0 / P1 (the probabilities as bf16 pairs), O0 / O1 (d fp32
 //          columns each)
-//   warp 0     TMA: the query tile once (into the last ring stage), then K and
-//              V tiles into a 6-stage ring (d = 128; 8 stages at d = 64)
+//   warp 0     TMA: the query tile once (into the last pipeline stage), then K
+//              and V tiles into a ring of 7 stages (d = 128; 8 at d = 64), less
+//              the one or two stages a split merge receives into
 //   warp 1     TMEM owner, MMA issuer: S_i = Q K_i^T (M=128, N=64 keys, K=d,
 //              A from TMEM) and O_g += P_i V_i (N=d, K=64 keys, P from TMEM, V
 //              read MN-major), each issued as soon as its inputs are ready
@@ -29,11 +30,15 @@
 //              computes its softmax the tensor core works on the other's tile.
 // At the end the two groups' rows are combined in the CTA.  Splits of one unit
 // form a thread block cluster (<= 8) and merge through distributed shared
-// memory: every CTA stages its rows, unnormalised, with the row's (max, sum) in
-// its own shared memory, grouped by the CTA that owns each row (CTA c owns rows
-// [c R/C, (c+1) R/C)), then sends each group to its owner with one bulk copy
-// whose bytes complete on the owner's mbarrier; each owner combines the C copies
-// of its rows with weights 2^(m_c - M) / L and writes them.
+// memory.  Only the tile rows that can hold a query are merged (a DualCache
+// tile of one MHA head has 32 such rows of 128); CTA c owns an equal share of
+// them, [c R, (c + 1) R) in whole 8-row groups.  Every CTA stages its
+// normalised copies of the rows it does not own in its own shared memory,
+// grouped by owner, with each row's (max, sum), and sends each group to its
+// owner with bulk copies that complete on the owner's mbarrier.  The owner
+// receives them in ring stages the K/V pipeline leaves out, so no CTA waits for
+// a peer's pipeline to finish before sending; it combines the C copies of its
+// rows with weights 2^(m_c - M) L_c and writes them.
 //
 // K/V maps view [b, N, Hkv, d] as (d, position, head, b), so one box brings a
 // tile half's keys of all heads packed in the tile, head-major.
@@ -46,6 +51,7 @@
 // the V codes into the bf16 V tile after the tile's scores are done.  The
 // products and the softmax arithmetic are unchanged.  Fresh K/V tiles are loaded
 // as bf16 directly.
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -63,6 +69,7 @@ constexpr int kTile = 128;       // rows per query tile
 constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMergeStages = 2;  // ring stages the split merge may take out of the K/V pipeline
 
 struct Plan {
   int f0, f1;           // cached prefix [0, f0), cached suffix [f1, N)
@@ -77,6 +84,9 @@ struct Plan {
   int tk;               // keys per KV head per key tile (64 / kvp)
   int abs_suffix;       // suffix rows are absolute cache rows (per-sequence blocks: full-cache maps)
   int units;            // batch * (Hkv / kvp) * nqt
+  int nvr;              // tile rows that can hold a query (the rest are padding in every unit)
+  int rpc;              // split merge: rows owned per CTA of a cluster (multiple of 8; 128 without a split)
+  int nsp;              // ring stages of the K/V pipeline (the ring's last stages receive merged rows)
 };
 
 template <int D>
@@ -88,22 +98,22 @@ struct Cfg {
   static constexpr int STAGE = 2 * KV_BYTES;          // K + V
   static constexpr int NS = D == 128 ? 7 : 8;         // K/V ring stages
   static_assert(kTile * D * 2 <= STAGE, "the query tile is staged in one ring stage");
-  // split merge: a row sent to its owner is D fp32 values normalised by the row's sum, then the row's
-  // max (log2 units) and sum, padded to a multiple of 16 bytes.  A send area (the rows this CTA
-  // does not own, grouped by owner) and a receive area (the C - 1 copies of the rows it owns),
-  // C * ceil(128 / C) <= 136 rows each, then the output tile.
-  static constexpr int SRP = D * 4 + 16;
-  static constexpr int MERGE_ROWS = 136;
-  static constexpr int MERGE_BYTES = 2 * MERGE_ROWS * SRP;
   static constexpr int RING = NS * STAGE;
-  // after the pipeline the ring also holds the output tile (one 128-row block of 128 bytes per 64 bf16 or
-  // 32 fp32 columns, 128-byte swizzle; with a cluster, after the merge areas) and, at its end, the two
-  // groups' (max, sum) per row
+  // Split merge: a row sent to its owner is D fp32 values normalised by the row's sum (RB bytes), with
+  // the row's (max in log2 units, sum) as a separate 8-byte pair.  The owner receives its peers' rows in
+  // the ring's last stages, which the K/V pipeline then leaves out (at most kMergeStages), and their
+  // pairs after the barriers (RECV_ML_BYTES).  Once the pipeline is done, its first stages hold the rows
+  // this CTA sends (row r at r * RB) and their pairs, the output tile (one 128-row block of 128 bytes per
+  // 64 bf16 or 32 fp32 columns, 128-byte swizzle: the layout a tile load of the output map writes), and
+  // the two groups' (max, sum) per row.
+  static constexpr int RB = D * 4;                   // (16-byte chunk j of row r stored at chunk j ^ (r & 7))
+  static constexpr int SEND_ML_OFF = kTile * RB;
+  static constexpr int OUT_OFF = (SEND_ML_OFF + kTile * 8 + 1023) / 1024 * 1024;
   static constexpr int OUT_BYTES = kTile * D * 4;
-  static constexpr int OUT_OFF = (MERGE_BYTES + 1023) / 1024 * 1024;
-  static constexpr int ML_OFF = RING - 2 * kTile * 8;
-  static_assert(OUT_OFF + OUT_BYTES <= ML_OFF, "ring areas after the pipeline");
-  static constexpr int SMEM = RING + 1024 + 512;    // + alignment + Bars
+  static constexpr int ML_OFF = OUT_OFF + OUT_BYTES;
+  static_assert(ML_OFF + 2 * kTile * 8 <= (NS - kMergeStages) * STAGE, "post-pipeline areas inside the pipeline");
+  static constexpr int RECV_ML_BYTES = 1280;
+  static constexpr int SMEM = RING + 1024 + 512 + RECV_ML_BYTES;    // + alignment + Bars + received pairs
   // TMEM columns
   static constexpr uint32_t Q_COL = 0;               // D / 2 columns of bf16 pairs
   static constexpr uint32_t S_COL = D / 2;           // S0, S1: 64 fp32 columns each
@@ -258,7 +268,7 @@ static_assert(sizeof(Bars) <= 512, "Bars must fit its shared-memory reservation"
 // cluster, the rows a CTA owns when they fall inside one slot; 0 when a CTA's rows do not fall on such
 // boundaries (multiples of 8 rows), and its threads then store their rows directly.
 __host__ __device__ __forceinline__ int out_box_rows(const Plan &pl) {
-  const int C = pl.nsplit, rpc = (kTile + C - 1) / C;
+  const int C = pl.nsplit, rpc = pl.rpc;
   const int br = C == 1 ? pl.qr : (rpc % pl.qr == 0 ? pl.qr : (pl.qr % rpc == 0 ? rpc : 0));
   return br % 8 == 0 ? br : 0;
 }
@@ -266,11 +276,6 @@ __host__ __device__ __forceinline__ int out_box_rows(const Plan &pl) {
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
 }
 
@@ -286,10 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int TK = kKeys / KVP;                      // keys of one KV head in a key tile
   extern __shared__ unsigned char smem_raw[];
   unsigned char *kv_s = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);   // NS stages
-  unsigned char *q_s = kv_s + (NS - 1) * CF::STAGE;    // the query tile, until it is in TMEM
   Bars &br = *(Bars *)(kv_s + CF::RING);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Plan pl = a.pl;   // per-sequence blocks fill in this CTA's ranges after the dependency wait
+  const int ns = pl.nsp;                               // K/V pipeline stages
+  // the query tile, until it is in TMEM: in the first receive stage of a split merge (no peer sends
+  // before every CTA of the cluster has moved its query tile out, see below), else in the last stage
+  unsigned char *q_s = kv_s + (pl.nsplit > 1 ? ns : ns - 1) * CF::STAGE;
 
   const int split = blockIdx.x % pl.nsplit;
   const int unit = blockIdx.x / pl.nsplit;
@@ -306,8 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     h0 = qt / pl.qtiles_per_head; nh = 1; q0 = (qt % pl.qtiles_per_head) * kTile;
   }
   const int C = pl.nsplit;                             // CTAs of this unit's cluster
-  const int rpc = (kTile + C - 1) / C;                 // rows owned per CTA in the split merge
-  const uint32_t seg_bytes = (uint32_t)(rpc * CF::SRP);   // one owner's rows, as sent
+  const int rpc = pl.rpc;                              // rows owned per CTA in the split merge
+  const int crank = C > 1 ? (int)tc::cluster_ctarank() : 0;
+  // rows of owner c that are merged: its share of the rows that can hold a query
+  auto seg_rows = [&](int c) { return max(0, min(rpc, pl.nvr - c * rpc)); };
 
   if (threadIdx.x == 0) {
     br.abort = 0; br.issued = 0; br.consumed_g[0] = 0; br.consumed_g[1] = 0; br.cvt_stop = 0;
@@ -327,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&br.drain, F8KV ? 1 : 2);          // one arrival per MMA issuer
     tc::mbar_init(&br.mrg, 1);
     tc::fence_barrier_init();
-    // the merge barrier expects the other C - 1 CTAs' rows of this one
-    if (C > 1) tc::mbar_arrive_expect_tx(&br.mrg, (uint32_t)(C - 1) * seg_bytes);
+    // the merge barrier expects the other C - 1 CTAs' copies of this one's rows and their pairs
+    if (C > 1) tc::mbar_arrive_expect_tx(&br.mrg, (uint32_t)((C - 1) * seg_rows(crank) * (CF::RB + 8)));
     for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc, &mo}) tc::prefetch_tensormap(m);
     if (a.win_box > 0) { tc::prefetch_tensormap(&mwk); tc::prefetch_tensormap(&mwv); }
   }
@@ -378,14 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int dh = 0; dh < CF::DH; ++dh)
           tc::tma_load_4d(q_s + dh * CF::QHALF + hs * pl.qr * 128, &mq, &br.qfull, dh * 64,
                           kvh * a.group + h0 + hs, q0, b, pol_q);
-      for (int i = 0; i < nt && !*abort_flag; ++i) {
-        const int st = i % NS;
-        // the last stage holds the query tile until group 0 has copied it into TMEM
-        if (i == NS - 1 && !tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag)) {
+      int st = 0;                                      // tile i's ring stage and that stage's phase parity
+      uint32_t ph = 0;
+      for (int i = 0; i < nt && !*abort_flag; ++i, st = st + 1 == ns ? 0 : st + 1, ph ^= st == 0 ? 1u : 0u) {
+        // without a cluster the last stage holds the query tile until group 0 has copied it into TMEM
+        if (C == 1 && i == ns - 1 && !tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag)) {
           if (!*abort_flag) fail(br, a.err, 210);
           break;
         }
-        if (!tc::mbar_wait_or_abort(&br.kvempty[st], ((uint32_t)(i / NS) & 1u) ^ 1u, abort_flag)) {
+        if (!tc::mbar_wait_or_abort(&br.kvempty[st], ph ^ 1u, abort_flag)) {
           if (!*abort_flag) fail(br, a.err, 211);
           break;
         }
@@ -424,6 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool run = tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag);    // Q is in TMEM
       if (!run && !*abort_flag) fail(br, a.err, 212);
       int js = gg, jp = gg;                             // next S, next PV of this group
+      int js_st = gg, jp_st = gg;                       // their ring stages
+      uint32_t js_ph = 0;                               // phase parity of js's stage
       // this CTA stores the block's fresh K/V into the cache window when the call asks for it and it
       // serves the first query tile of its KV head group (every such CTA of the split covers its own keys)
       const bool update_cache = a.win_box > 0 && qt == 0;
@@ -431,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t t0 = tc::globaltimer();
       for (uint32_t spin = 0; run && jp < nt; ++spin) {
         if (jp < js && tc::mbar_test_wait(&br.pfull[gg], (uint32_t)(jp >> 1) & 1u)) {
-          const int st = jp % NS;
+          const int st = jp_st;
           tc::fence_after_sync();
           const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
 #pragma unroll
@@ -445,12 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::mma_commit(&br.kvempty[st]);
           jp += 2;
+          jp_st += 2;
+          if (jp_st >= ns) jp_st -= ns;
           t0 = tc::globaltimer();
           continue;
         }
-        if (js < nt && tc::mbar_test_wait(&br.kvfull[js % NS], (uint32_t)(js / NS) & 1u) &&
+        if (js < nt && tc::mbar_test_wait(&br.kvfull[js_st], js_ph) &&
             tc::mbar_test_wait(&br.sempty[gg], ((uint32_t)(js >> 1) & 1u) ^ 1u)) {
-          const int st = js % NS;
+          const int st = js_st;
           tc::fence_after_sync();
           const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
 #pragma unroll
@@ -473,6 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           js += 2;
+          js_st += 2;
+          if (js_st >= ns) { js_st -= ns; js_ph ^= 1u; }
           atomicExch(&br.consumed_g[gg], js >> 1);
           t0 = tc::globaltimer();
           continue;
@@ -485,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (update_cache) tc::bulk_wait_all();           // the cache-window writes are complete
+      if (update_cache) tc::bulk_wait_read_all();      // the window stores have read the ring
       tc::mma_commit(&br.drain);                        // both issuers arrive: count 2
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
     }
@@ -502,14 +519,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool run = tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag);    // Q is in TMEM
       if (!run && !*abort_flag) fail(br, a.err, 212);
       int js = 0, jp = 0;                               // next S, next PV
+      int js_st = 0, jp_st = 0;                         // their ring stages
+      uint32_t js_ph = 0;                               // phase parity of js's stage
       uint64_t t0 = tc::globaltimer();
       auto s_ready = [&]() {
-        return tc::mbar_test_wait(&br.kvfull[js % NS], (uint32_t)(js / NS) & 1u) &&
+        return tc::mbar_test_wait(&br.kvfull[js_st], js_ph) &&
                tc::mbar_test_wait(&br.sempty[js & 1], ((uint32_t)(js >> 1) & 1u) ^ 1u);
       };
       for (uint32_t spin = 0; run && jp < nt; ++spin) {
         if (jp < js && tc::mbar_try_wait_hint(&br.pfull[jp & 1], (uint32_t)(jp >> 1) & 1u, js < nt ? 200u : 2000u)) {
-          const int st = jp % NS, gg = jp & 1;
+          const int st = jp_st, gg = jp & 1;
           tc::fence_after_sync();
           const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
 #pragma unroll
@@ -519,13 +538,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_commit(&br.pvdone[gg]);
           tc::mma_commit(&br.kvempty[st]);
           ++jp;
+          if (++jp_st == ns) jp_st = 0;
           t0 = tc::globaltimer();
           continue;
         }
-        if (js < nt && (s_ready() || (jp >= js && tc::mbar_try_wait_hint(&br.kvfull[js % NS],
-                                                                          (uint32_t)(js / NS) & 1u, 2000u) &&
+        if (js < nt && (s_ready() || (jp >= js && tc::mbar_try_wait_hint(&br.kvfull[js_st], js_ph, 2000u) &&
                                        s_ready()))) {
-          const int st = js % NS, gg = js & 1;
+          const int st = js_st, gg = js & 1;
           tc::fence_after_sync();
           const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
 #pragma unroll
@@ -535,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_commit(&br.sfull[gg]);
           atomicExch(&br.consumed_g[js & 1], (js >> 1) + 1);
           ++js;
+          if (++js_st == ns) { js_st = 0; js_ph ^= 1u; }
           t0 = tc::globaltimer();
           continue;
         }
@@ -573,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = (r % pl.tk) < key_tile(pl, a.nq, a.n, k0 + i).nvalid;
       inext = next_cache_tile(i + 1);
       ksn = load_scale(inext);
-      const int st = i % NS;
+      const int st = i % ns;
       if (!tc::mbar_wait_or_abort(&br.raw[st], (rawpar >> st) & 1u, abort_flag)) {
         if (!*abort_flag) fail(br, a.err, 220);
         br.cvt_stop = 1;
@@ -628,6 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&br.qtmem);
     }
+    // the query tile has left the receive stage (its loads are complete: their values are in TMEM)
+    if (C > 1 && g == 0) tc::cluster_arrive_relaxed();
     if (KVP > 1) {
       // each row writes only its head's block of P: the rest of its P row stays zero
       uint32_t z[32];
@@ -640,14 +662,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // F8KV: phase parity of raw[st] for tile i (the cache tiles loaded into its stage before it)
     auto raw_phase = [&](int i) -> uint32_t {
       int uses = 0;
-      for (int j = i % NS; j < i; j += NS) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
+      for (int j = i % ns; j < i; j += ns) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
       return (uint32_t)uses & 1u;
     };
     int u = 0;                                         // this group's tile count
-    for (int i = g; i < nt; i += 2, ++u) {
+    int st = g;                                        // tile i's ring stage
+    for (int i = g; i < nt; i += 2, ++u, st = st + 2 >= ns ? st + 2 - ns : st + 2) {
       const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + i);
       const int nv = kt.nvalid;
-      const int st = i % NS;
       if (!tc::mbar_wait_or_abort(&br.sfull[g], (uint32_t)u & 1u, abort_flag)) {
         if (!*abort_flag) fail(br, a.err, 218);
         ok = false;
@@ -781,20 +803,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- every role is done: all copies consumed, all MMAs complete ----
+  // With a cluster, the first cluster barrier says that this CTA's merge barrier is initialised and its
+  // receive stage free: softmax group 0 arrived once the query tile was in TMEM, the other warps arrive
+  // here.  Every CTA waits for it before its first copy to a peer.
+  if (C > 1 && (warp < 4 || warp >= 8)) tc::cluster_arrive_relaxed();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (*abort_flag) {
     if (threadIdx.x == 0) {
       // copies issued but never consumed still land in shared memory: wait for them (bounded)
+      tc::mbar_wait(&br.qfull, 0);
       for (int i = 0; i < br.issued; ++i) {
         if ((i >> 1) < br.consumed_g[i & 1]) continue;
         if (F8KV && key_tile(pl, a.nq, a.n, k0 + i).range != 1) {
           int uses = 0;                                // earlier cache tiles in this stage: raw's phase
-          for (int j = i % NS; j < i; j += NS) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
-          tc::mbar_wait(&br.raw[i % NS], (uint32_t)uses & 1u);
+          for (int j = i % ns; j < i; j += ns) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
+          tc::mbar_wait(&br.raw[i % ns], (uint32_t)uses & 1u);
         } else {
-          tc::mbar_wait(&br.kvfull[i % NS], (uint32_t)(i / NS) & 1u);
+          tc::mbar_wait(&br.kvfull[i % ns], (uint32_t)(i / ns) & 1u);
         }
       }
     }
@@ -802,24 +829,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- combine the two groups' rows: row r's final (M, L) and D values ----
-  // The ring is idle now.  It holds: the two groups' (max, sum) per row at ML_OFF; the output tile
-  // (blocks of 128 rows x 128 bytes: 64 bf16 or 32 fp32 columns each, 128-byte swizzle, the layout a tile
-  // load of the output map would write), written by TMA; with a cluster, before it, the send and
-  // receive areas of the split merge.
-  unsigned char *send = kv_s;
-  unsigned char *recv = kv_s + CF::MERGE_ROWS * CF::SRP;
-  unsigned char *ot = kv_s + (C == 1 ? 0 : CF::OUT_OFF);
+  unsigned char *send = kv_s;                           // rows sent to their owners (row r at r * RB)
+  float2 *send_ml = (float2 *)(kv_s + CF::SEND_ML_OFF);
+  unsigned char *recv = kv_s + ns * CF::STAGE;          // peers' copies of the owned rows, by peer slot
+  float2 *recv_ml = (float2 *)(kv_s + CF::RING + 512);
+  unsigned char *ot = kv_s + CF::OUT_OFF;
   float2 *ml = (float2 *)(kv_s + CF::ML_OFF);           // [group][row]
   const int out_f32 = a.out_f32;
   const int cw = out_f32 ? 32 : 64;                     // columns per 128-byte output block
-  const int crank = C > 1 ? (int)tc::cluster_ctarank() : 0;
-  const int r0 = crank * rpc, r1 = min(kTile, r0 + rpc);   // the rows this CTA writes
+  const int r0 = min(kTile, crank * rpc), r1 = min(kTile, r0 + rpc);   // the rows this CTA writes
+  const int seg_own = seg_rows(crank);                  // of which the merged ones: [r0, r0 + seg_own)
   // rows per TMA store box: a head slot (qr rows), or the owned rows when they lie in one slot; 0 when
   // the owned rows do not fall on slot boundaries (the owners then store their rows directly)
   const int br_rows = out_box_rows(pl);
   constexpr int DHALF = D / 2;                         // a softmax thread's columns [g D/2, (g + 1) D/2)
   float v[DHALF];
   float Mrow = kNegInf, Lrow = 0.f;                    // the CTA's row: max (raw score units), sum
+  const int owner = r / rpc;                           // the CTA that writes row r
+  const bool merged = C > 1 && owner < C && r - owner * rpc < seg_rows(owner);
   if (warp >= 4) {
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -840,62 +867,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 32; ++e)
         v[c0 + e] = (w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f) + (w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f);
     }
-    if (C > 1 && r / rpc != crank) {
-      // a row another CTA owns: normalised half row (g) and, from group 0, (max, sum) to the send area
-      unsigned char *row = send + (size_t)r * CF::SRP;
+    if (merged && owner != crank) {
+      // a merged row another CTA writes: this half row (g) normalised and, from group 0, (max, sum);
+      // 16-byte chunk j of row r goes to chunk j ^ (r & 7), so that a warp's 32 rows spread over the banks
+      unsigned char *row = send + (size_t)r * CF::RB;
       const float inv = Lrow > 0.f ? 1.f / Lrow : 0.f;
 #pragma unroll
       for (int c = 0; c < DHALF / 4; ++c)
-        *(float4 *)(row + g * DHALF * 4 + 16 * c) =
+        *(float4 *)(row + (((g * DHALF / 4 + c) ^ (r & 7)) * 16)) =
             make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
-      if (g == 0) *(float2 *)(row + D * 4) = make_float2(Lrow > 0.f ? Mrow * a.scale_log2 : kNegInf, Lrow);
+      if (g == 0) send_ml[r] = make_float2(Lrow > 0.f ? Mrow * a.scale_log2 : kNegInf, Lrow);
       tc::fence_proxy_async_smem();                    // the bulk copies read these rows
     }
   }
 
   if (C > 1) {
-    // ---- split merge through the cluster: the rows go to their owners ----
-    // The cluster barriers only say "reached here": a peer's ring is idle once it arrives (its loads
-    // landed and its products completed before that, as it observed), and its staged rows are read by
-    // its own bulk copies after the softmax barrier below.  Neither publishes memory, so the arrivals
-    // are relaxed.
-    tc::cluster_arrive_relaxed();                      // this CTA's ring is free
-    if (warp >= 4) softmax_bar();                      // its staged rows are complete
-    tc::cluster_wait();                                // every peer's ring is free
+    // ---- split merge through the cluster: the merged rows go to their owners ----
+    // Each owner receives its rows from every peer into the ring stages the pipeline left out, so no
+    // CTA waits for a peer to finish before sending; the cluster barrier begun at the start only
+    // ensures that every peer's merge barrier has been initialised.
+    tc::cluster_wait();
+    if (warp >= 4) softmax_bar();                      // the rows to send are complete
     if (threadIdx.x == 128) {
       for (int c = 0; c < C; ++c) {
-        if (c == crank) continue;
-        tc::bulk_copy_to_cluster(tc::cluster_map(recv + (size_t)crank * rpc * CF::SRP, (uint32_t)c),
-                                 send + (size_t)c * rpc * CF::SRP, seg_bytes, tc::cluster_map(&br.mrg, (uint32_t)c));
+        const int nr = seg_rows(c);
+        if (c == crank || nr == 0) continue;
+        const int slot = crank < c ? crank : crank - 1;   // this CTA's slot among owner c's peers
+        const uint32_t bar = tc::cluster_map(&br.mrg, (uint32_t)c);
+        tc::bulk_copy_to_cluster(tc::cluster_map(recv + (size_t)slot * rpc * CF::RB, (uint32_t)c),
+                                 send + (size_t)c * rpc * CF::RB, (uint32_t)(nr * CF::RB), bar);
+        tc::bulk_copy_to_cluster(tc::cluster_map(recv_ml + slot * rpc, (uint32_t)c), send_ml + c * rpc,
+                                 (uint32_t)(nr * 8), bar);
       }
     }
-    if (warp >= 4 && r / rpc == crank) {
-      // an owned row: combine this CTA's part (registers, relative to Mrow) with the peers' normalised
-      // copies; weight of source s: L_s 2^(m_s - M), M = max_s m_s (log2 units)
-      if (!tc::mbar_wait_or_abort(&br.mrg, 0, abort_flag)) {   // the peers' copies of this CTA's rows
-        if (!*abort_flag) fail(br, a.err, 221);
-      }
+    if (warp >= 4 && merged && owner == crank) {
+      // an owned merged row: combine this CTA's part (registers, relative to Mrow) with the peers'
+      // normalised copies; weight of source s: L_s 2^(m_s - M), M = max_s m_s (log2 units)
+      // The peers' copies of this CTA's rows.  Every peer sends them, after an abort too, so this wait
+      // ignores the abort flag: the CTA must not leave while a copy into it is still on its way.
+      if (!tc::mbar_wait(&br.mrg, 0)) fail(br, a.err, 221);
       const float mown = Lrow > 0.f ? Mrow * a.scale_log2 : kNegInf;
       float M = mown;
-      for (int c = 0; c < C; ++c) {
-        if (c == crank) continue;
-        const float2 mlc = lds_f2(tc::smem_u32(recv + (size_t)(c * rpc + r - r0) * CF::SRP + D * 4));
+      for (int sl = 0; sl < C - 1; ++sl) {
+        const float2 mlc = recv_ml[sl * rpc + r - r0];
         if (mlc.y > 0.f) M = fmaxf(M, mlc.x);
       }
       const float wown = Lrow > 0.f ? tc::ex2_approx(mown - M) : 0.f;
       float W = wown * Lrow;
 #pragma unroll
       for (int e = 0; e < DHALF; ++e) v[e] = wown > 0.f ? v[e] * wown : 0.f;
-      for (int c = 0; c < C; ++c) {
-        if (c == crank) continue;
-        const uint32_t rowa = tc::smem_u32(recv + (size_t)(c * rpc + r - r0) * CF::SRP);
-        const float2 mlc = lds_f2(rowa + D * 4);
+      for (int sl = 0; sl < C - 1; ++sl) {
+        const float2 mlc = recv_ml[sl * rpc + r - r0];
         if (!(mlc.y > 0.f)) continue;                  // an empty split: its values may be anything
         const float wc = mlc.y * tc::ex2_approx(mlc.x - M);
         W += wc;
+        const uint32_t rowa = tc::smem_u32(recv + (size_t)(sl * rpc + r - r0) * CF::RB);
 #pragma unroll
         for (int cc = 0; cc < DHALF / 4; ++cc) {
-          const float4 x = lds_f4(rowa + (uint32_t)(g * DHALF * 4 + 16 * cc));
+          const float4 x = lds_f4(rowa + (uint32_t)(((g * DHALF / 4 + cc) ^ (r & 7)) * 16));
           v[4 * cc] = fmaf(x.x, wc, v[4 * cc]); v[4 * cc + 1] = fmaf(x.y, wc, v[4 * cc + 1]);
           v[4 * cc + 2] = fmaf(x.z, wc, v[4 * cc + 2]); v[4 * cc + 3] = fmaf(x.w, wc, v[4 * cc + 3]);
         }
@@ -904,7 +933,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       Mrow = M / a.scale_log2;
       Lrow = W;
     }
-    tc::cluster_arrive_relaxed();                      // every copy into this CTA has landed
+    // every copy into this CTA has landed (its merging threads waited for them); the barrier completes
+    // before any CTA of the cluster leaves, so no copy ever targets a CTA that has exited
+    tc::cluster_arrive_relaxed();
   }
 
   // ---- output: this CTA's rows [r0, r1) ----
@@ -958,10 +989,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_store_4d(&mo, ot + blk * CF::QHALF + rb * 128, blk * cw, kvh * a.group + h0 + hs, qi, b);
       }
       tc::bulk_commit_group();
-      tc::bulk_wait_all();
     }
   }
-  if (C > 1) tc::cluster_wait();                      // every copy out of this CTA has landed too
+  // the bulk stores have read the tile (their global writes complete with the grid); with a cluster,
+  // every copy this CTA sent has landed once the cluster barrier completes
+  if (threadIdx.x == 128) tc::bulk_wait_read_all();
+  if (C > 1) tc::cluster_wait();
 
   tc::fence_before_sync();
   __syncthreads();
@@ -1081,7 +1114,21 @@ Plan make_plan(const AttnProblem &p) {
   int ns = sm_count() / pl.units;
   if (ns > kMaxCluster) ns = kMaxCluster;
   if (ns > kt_max) ns = kt_max;
+  // Split merge: the tile rows that can hold a query (in any unit) are owned by the cluster's CTAs in
+  // equal shares of whole 8-row groups.  An owner receives its peers' copies in ring stages taken out
+  // of the K/V pipeline (at most kMergeStages) and their (max, sum) pairs after the barriers; a cluster
+  // whose copies would not fit is made smaller.
+  pl.nvr = pl.kvp > 1 || pl.qtiles_per_head != 0 ? kTile : std::min(pl.ht, group) * pl.qr;
+  const int stage = 2 * kKeys * p.d * 2, nstages = p.d == 128 ? Cfg<128>::NS : Cfg<64>::NS;
+  auto rows_per = [&](int c) { return ((pl.nvr + c - 1) / c + 7) / 8 * 8; };
+  auto merge_stages = [&](int c) {
+    const int64_t bytes = (int64_t)(c - 1) * rows_per(c) * p.d * 4;
+    return (int)((bytes + stage - 1) / stage);
+  };
+  while (ns > 1 && (merge_stages(ns) > kMergeStages || (ns - 1) * rows_per(ns) * 8 > Cfg<128>::RECV_ML_BYTES)) --ns;
   pl.nsplit = ns < 1 ? 1 : ns;
+  pl.rpc = pl.nsplit > 1 ? rows_per(pl.nsplit) : kTile;
+  pl.nsp = nstages - (pl.nsplit > 1 ? merge_stages(pl.nsplit) : 0);
   return pl;
 }
 
