@@ -140,6 +140,8 @@ __device__ __forceinline__ void quadrant_bar(int q) { asm volatile("bar.sync %0,
 __device__ __forceinline__ void convert_bar() { asm volatile("bar.sync 6, 64;" ::: "memory"); }
 // The four warps of softmax group g.
 __device__ __forceinline__ void group_bar(int g) { asm volatile("bar.sync %0, 128;" ::"r"(7 + g) : "memory"); }
+// The softmax warps and warp 3, which sends the split merge's rows once the softmax warps have staged them.
+__device__ __forceinline__ void send_bar() { asm volatile("bar.sync 9, 288;" ::: "memory"); }
 
 struct KeyTile {
   int range;   // 0 prefix cache, 1 fresh, 2 suffix cache
@@ -857,15 +859,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float w0 = ml0.y > 0.f ? tc::ex2_approx((ml0.x - Mrow) * a.scale_log2) : 0.f;
     const float w1 = ml1.y > 0.f ? tc::ex2_approx((ml1.x - Mrow) * a.scale_log2) : 0.f;
     Lrow = w0 * ml0.y + w1 * ml1.y;
+    // a quadrant whose rows are all padding (past the rows that can hold a query) reads nothing
+    if (q * 32 < pl.nvr) {
 #pragma unroll
-    for (int c0 = 0; c0 < DHALF; c0 += 32) {
-      uint32_t o0[32], o1[32];
-      tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::O_COL + (uint32_t)(g * DHALF + c0), o0);
-      tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::O_COL + (uint32_t)(D + g * DHALF + c0), o1);
-      tc::tmem_ld_wait();
+      for (int c0 = 0; c0 < DHALF; c0 += 32) {
+        uint32_t o0[32], o1[32];
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::O_COL + (uint32_t)(g * DHALF + c0), o0);
+        tc::tmem_ld_32x32b_x32(tmem + lane_base + CF::O_COL + (uint32_t)(D + g * DHALF + c0), o1);
+        tc::tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        v[c0 + e] = (w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f) + (w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f);
+        for (int e = 0; e < 32; ++e)
+          v[c0 + e] = (w0 > 0.f ? w0 * __uint_as_float(o0[e]) : 0.f) + (w1 > 0.f ? w1 * __uint_as_float(o1[e]) : 0.f);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < DHALF; ++e) v[e] = 0.f;
     }
     if (merged && owner != crank) {
       // a merged row another CTA writes: this half row (g) normalised and, from group 0, (max, sum);
@@ -887,8 +895,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // CTA waits for a peer to finish before sending; the cluster barrier begun at the start only
     // ensures that every peer's merge barrier has been initialised.
     tc::cluster_wait();
-    if (warp >= 4) softmax_bar();                      // the rows to send are complete
-    if (threadIdx.x == 128) {
+    // Warp 3 (idle by now) sends: the thread that issues the copies would otherwise be held at its next
+    // proxy fence (before the output stores) until they have landed.
+    if (warp >= 3) send_bar();                         // the rows to send are complete
+    if (threadIdx.x == 96) {
       for (int c = 0; c < C; ++c) {
         const int nr = seg_rows(c);
         if (c == crank || nr == 0) continue;
