@@ -662,15 +662,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float sl2 = a.scale_log2;
     // F8KV: phase parity of raw[st] for tile i (the cache tiles loaded into its stage before it)
-    auto raw_phase = [&](int i) -> uint32_t {
-      int uses = 0;
-      for (int j = i % ns; j < i; j += ns) uses += key_tile(pl, a.nq, a.n, k0 + j).range != 1;
-      return (uint32_t)uses & 1u;
+    // F8KV: the raw barriers' phase parities (bit st: cache tiles loaded into stage st so far), advanced
+    // over every tile before this group's next one; and this thread's V scale, loaded one tile ahead
+    uint32_t rawpar = 0;
+    int seen = 0, seen_st = 0;
+    auto v_scale_of = [&](int i) -> float {
+      if (!F8KV || i >= nt) return 0.f;
+      const KeyTile t = key_tile(pl, a.nq, a.n, k0 + i);
+      if (t.range == 1 || ((gt >> 1) % pl.tk) >= t.nvalid) return 0.f;
+      return cache_scale(a, pl, t, b, kvh, gt >> 1, a.v_scale);
     };
+    float vsc_next = v_scale_of(g);
     int u = 0;                                         // this group's tile count
     int st = g;                                        // tile i's ring stage
     for (int i = g; i < nt; i += 2, ++u, st = st + 2 >= ns ? st + 2 - ns : st + 2) {
       const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + i);
+      const float vsc_cur = vsc_next;
+      if constexpr (F8KV) {
+        vsc_next = v_scale_of(i + 2);                  // used one tile later: the load has time to land
+        for (; seen < i; ++seen, seen_st = seen_st + 1 == ns ? 0 : seen_st + 1)
+          if (key_tile(pl, a.nq, a.n, k0 + seen).range != 1) rawpar ^= 1u << seen_st;
+      }
       const int nv = kt.nvalid;
       if (!tc::mbar_wait_or_abort(&br.sfull[g], (uint32_t)u & 1u, abort_flag)) {
         if (!*abort_flag) fail(br, a.err, 218);
@@ -693,8 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (cvt) {
             // the codes' arrival, for this thread: complete long ago (the converters waited for it, and
             // the tile's scores are done), and raw[st] cannot move on before this tile's P is released
-            if (!tc::mbar_wait_or_abort(&br.raw[st], raw_phase(i), abort_flag)) ok = false;
-            const float vsc = rvalid ? cache_scale(a, pl, kt, b, kvh, vr, a.v_scale) : 0.f;
+            if (!tc::mbar_wait_or_abort(&br.raw[st], (rawpar >> st) & 1u, abort_flag)) ok = false;
+            const float vsc = vsc_cur;                 // 0 for a row outside the sequence's key range
             uint4 cq[HB / 16];
 #pragma unroll
             for (int c = 0; c < HB / 16; ++c)
