@@ -2,6 +2,7 @@
 
     python -m block_cached_decoding_gb300.profile_case select --vocab 32768 --reps 3
     python -m block_cached_decoding_gb300.profile_case select --fp8w --reps 3
+    python -m block_cached_decoding_gb300.profile_case select --f32 --vocab 32768 --hidden 1024 --reps 3
     python -m block_cached_decoding_gb300.profile_case attn --mode prefix --reps 3
     python -m block_cached_decoding_gb300.profile_case attn --mode prefix --update --reps 3
     python -m block_cached_decoding_gb300.profile_case splice --reps 3
@@ -35,6 +36,8 @@ def main():
     ap.add_argument("--mode", default="prefix", choices=["dual", "prefix", "none"])
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fp8w", action="store_true", help="select through the FP8 weight cache")
+    ap.add_argument("--f32", action="store_true",
+                    help="fp32 hidden rows and weight (the CUDA-core LM head, then select_kernel)")
     ap.add_argument("--fp8kv", action="store_true", help="attention over the FP8 KV cache")
     ap.add_argument("--update", action="store_true",
                     help="attention with the cache-window update (fdllm_block_attn_update)")
@@ -48,9 +51,12 @@ def main():
     s = a.prompt + a.block_idx * B
     code = F.BF16
     if a.op == "select":
-        W = torch.empty(a.vocab, a.hidden, dtype=torch.bfloat16, device=dev)
+        if a.f32:
+            code = F.F32
+        tdt = torch.float32 if a.f32 else torch.bfloat16
+        W = torch.empty(a.vocab, a.hidden, dtype=tdt, device=dev)
         F.fdllm_synth_normals(wl.seed, F.SYNTH_W, [], a.vocab * a.hidden, 0, wl.sigma_w, code, W)
-        hid = torch.empty(b, B, a.hidden, dtype=torch.bfloat16, device=dev)
+        hid = torch.empty(b, B, a.hidden, dtype=tdt, device=dev)
         F.fdllm_synth_hidden(wl.seed, b, 0, s, B, a.hidden, a.vocab, wl.p_plant, W, code, hid)
         tokens0 = torch.full((b, n), a.vocab, dtype=torch.int32, device=dev)
         tokens = tokens0.clone()
