@@ -103,14 +103,10 @@ struct Cfg {
   // the row's (max in log2 units, sum) as a separate 8-byte pair.  The owner receives its peers' rows in
   // the ring's last stages, which the K/V pipeline then leaves out (at most kMergeStages), and their
   // pairs after the barriers (RECV_ML_BYTES).  Once the pipeline is done, its first stages hold the rows
-  // this CTA sends (row r at r * RB) and their pairs, the output tile (one 128-row block of 128 bytes per
-  // 64 bf16 or 32 fp32 columns, 128-byte swizzle: the layout a tile load of the output map writes), and
-  // the two groups' (max, sum) per row.
+  // this CTA sends (row r at r * RB) and their pairs, and the two groups' (max, sum) per row.
   static constexpr int RB = D * 4;                   // (16-byte chunk j of row r stored at chunk j ^ (r & 7))
   static constexpr int SEND_ML_OFF = kTile * RB;
-  static constexpr int OUT_OFF = (SEND_ML_OFF + kTile * 8 + 1023) / 1024 * 1024;
-  static constexpr int OUT_BYTES = kTile * D * 4;
-  static constexpr int ML_OFF = OUT_OFF + OUT_BYTES;
+  static constexpr int ML_OFF = (SEND_ML_OFF + kTile * 8 + 1023) / 1024 * 1024;
   static_assert(ML_OFF + 2 * kTile * 8 <= (NS - kMergeStages) * STAGE, "post-pipeline areas inside the pipeline");
   static constexpr int RECV_ML_BYTES = 1280;
   static constexpr int SMEM = RING + 1024 + 512 + RECV_ML_BYTES;    // + alignment + Bars + received pairs
@@ -132,8 +128,6 @@ struct Bars {
   int32_t consumed_g[2];   // per group: key tiles whose arrival its MMA issuer waited for
 };
 
-// The 256 softmax threads (warps 4-11) synchronise among themselves.
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 // The two softmax warps of TMEM lane quadrant q (warps 4 + q and 8 + q) synchronise as a pair.
 __device__ __forceinline__ void quadrant_bar(int q) { asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory"); }
 // The two FP8 conversion warps synchronise among themselves.
@@ -266,15 +260,6 @@ __device__ __forceinline__ void store_row_part(void *dst, bool f32, const float 
 
 static_assert(sizeof(Bars) <= 512, "Bars must fit its shared-memory reservation");
 
-// Rows of one TMA store box of the output (its map's box height): a head slot's qr rows, or, with a
-// cluster, the rows a CTA owns when they fall inside one slot; 0 when a CTA's rows do not fall on such
-// boundaries (multiples of 8 rows), and its threads then store their rows directly.
-__host__ __device__ __forceinline__ int out_box_rows(const Plan &pl) {
-  const int C = pl.nsplit, rpc = pl.rpc;
-  const int br = C == 1 ? pl.qr : (rpc % pl.qr == 0 ? pl.qr : (pl.qr % rpc == 0 ? rpc : 0));
-  return br % 8 == 0 ? br : 0;
-}
-
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
@@ -286,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mka,
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
                    const __grid_constant__ CUtensorMap mva, const __grid_constant__ CUtensorMap mvf,
-                   const __grid_constant__ CUtensorMap mvc, const __grid_constant__ CUtensorMap mo,
+                   const __grid_constant__ CUtensorMap mvc,
                    const __grid_constant__ CUtensorMap mwk, const __grid_constant__ CUtensorMap mwv, const Args a) {
   using CF = Cfg<D>;
   constexpr int NS = CF::NS;
@@ -341,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_barrier_init();
     // the merge barrier expects the other C - 1 CTAs' copies of this one's rows and their pairs
     if (C > 1) tc::mbar_arrive_expect_tx(&br.mrg, (uint32_t)((C - 1) * seg_rows(crank) * (CF::RB + 8)));
-    for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc, &mo}) tc::prefetch_tensormap(m);
+    for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc}) tc::prefetch_tensormap(m);
     if (a.win_box > 0) { tc::prefetch_tensormap(&mwk); tc::prefetch_tensormap(&mwv); }
   }
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
@@ -847,15 +832,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   float2 *send_ml = (float2 *)(kv_s + CF::SEND_ML_OFF);
   unsigned char *recv = kv_s + ns * CF::STAGE;          // peers' copies of the owned rows, by peer slot
   float2 *recv_ml = (float2 *)(kv_s + CF::RING + 512);
-  unsigned char *ot = kv_s + CF::OUT_OFF;
   float2 *ml = (float2 *)(kv_s + CF::ML_OFF);           // [group][row]
   const int out_f32 = a.out_f32;
-  const int cw = out_f32 ? 32 : 64;                     // columns per 128-byte output block
   const int r0 = min(kTile, crank * rpc), r1 = min(kTile, r0 + rpc);   // the rows this CTA writes
   const int seg_own = seg_rows(crank);                  // of which the merged ones: [r0, r0 + seg_own)
-  // rows per TMA store box: a head slot (qr rows), or the owned rows when they lie in one slot; 0 when
-  // the owned rows do not fall on slot boundaries (the owners then store their rows directly)
-  const int br_rows = out_box_rows(pl);
   constexpr int DHALF = D / 2;                         // a softmax thread's columns [g D/2, (g + 1) D/2)
   float v[DHALF];
   float Mrow = kNegInf, Lrow = 0.f;                    // the CTA's row: max (raw score units), sum
@@ -968,54 +948,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = kvh * a.group + h0 + hs;
     if (valid && g == 0 && a.lse && Lrow > 0.f)
       a.lse[((int64_t)b * a.nq + qi) * a.hq + h] = Mrow * a.scale + __logf(Lrow);
-    if (br_rows > 0) {
-      // normalised row part into the output tile: 16-byte chunk j of row r of a block at (j ^ (r & 7))
-      if (!out_f32) {
-#pragma unroll
-        for (int c = 0; c < DHALF / 8; ++c) {          // 8 bf16 per chunk
-          const int col = g * DHALF + 8 * c;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * c + 2 * e] * inv, v[8 * c + 2 * e + 1] * inv);
-            w[e] = *(uint32_t *)&h2;
-          }
-          const int blk = col / 64, j = (col % 64) / 8;
-          *(uint4 *)(ot + blk * CF::QHALF + r * 128 + ((j ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < DHALF / 4; ++c) {          // 4 fp32 per chunk
-          const int col = g * DHALF + 4 * c;
-          const int blk = col / 32, j = (col % 32) / 4;
-          *(float4 *)(ot + blk * CF::QHALF + r * 128 + ((j ^ (r & 7)) * 16)) =
-              make_float4(v[4 * c] * inv, v[4 * c + 1] * inv, v[4 * c + 2] * inv, v[4 * c + 3] * inv);
-        }
-      }
-      tc::fence_proxy_async_smem();                    // the TMA stores read the tile
-    } else if (valid && Lrow > 0.f) {
+    // the normalised half row straight to the output: 16-byte stores, a row's 128 or 256 bytes
+    // contiguous (measured faster than staging the tile for TMA stores, at every workload shape)
+    if (valid) {
       const int64_t obase = (((int64_t)b * a.nq + qi) * a.hq + h) * D + g * DHALF;
       void *dst = out_f32 ? (void *)((float *)a.out + obase) : (void *)((__nv_bfloat16 *)a.out + obase);
       store_row_part<DHALF>(dst, out_f32 != 0, v, inv);
     }
   }
-  if (warp >= 4 && br_rows > 0) {
-    softmax_bar();
-    if (threadIdx.x == 128) {
-      // one box per br_rows rows of a head slot and column block; rows past nq lie outside the map
-      for (int rb = r0; rb < r1; rb += br_rows) {
-        int hs, qi;
-        row_target(pl, a.nq, nh, q0, rb, hs, qi);
-        if (hs >= nh) continue;
-        for (int blk = 0; blk < D / cw; ++blk)
-          tc::tma_store_4d(&mo, ot + blk * CF::QHALF + rb * 128, blk * cw, kvh * a.group + h0 + hs, qi, b);
-      }
-      tc::bulk_commit_group();
-    }
-  }
-  // the bulk stores have read the tile (their global writes complete with the grid); with a cluster,
-  // every copy this CTA sent has landed once the cluster barrier completes
-  if (threadIdx.x == 128) tc::bulk_wait_read_all();
+  // with a cluster, every copy this CTA sent has landed once the exit barrier completes
   if (C > 1) tc::cluster_wait();
 
   tc::fence_before_sync();
@@ -1050,20 +991,6 @@ bool map4(CUtensorMap *m, const void *base, int d, int heads, int rows, int batc
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The same view of an fp32 tensor, box {32, 1, box_rows, 1} (128-byte rows in the swizzled layout).
-bool map4_f32(CUtensorMap *m, const void *base, int d, int heads, int rows, int batch, int64_t batch_stride,
-              int box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)batch};
-  const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4, (cuuint64_t)batch_stride * 4};
-  const cuuint32_t box[4] = {32, 1, (cuuint32_t)box_rows, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void *>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1182,7 +1109,7 @@ cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cud
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8],
-                         maps[9], a);
+                         a);
   count_launches(1);
   return e;
 }
@@ -1215,7 +1142,7 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t cstride = (int64_t)p.seq_len * p.hkv * p.d;  // cache batch stride
   const int64_t fstride = (int64_t)p.nq * p.hkv * p.d;       // fresh batch stride
   const int64_t qstride = (int64_t)p.nq * p.hq * p.d;
-  CUtensorMap maps[10];
+  CUtensorMap maps[9];
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
   // per-sequence blocks: prefix and suffix tiles are read through maps of the whole cache; rows of a
   // sequence's own window that fall in a boundary tile are read and weighted by exactly zero
@@ -1223,11 +1150,7 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t off_c = per_seq ? 0 : (int64_t)pl.f1 * p.hkv * p.d;
   const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
   const int kvp = pl.kvp;
-  // the output [b, nq, Hq, d] like the queries: bf16 boxes of 64 columns, or fp32 boxes of 32
-  const int obr = out_box_rows(pl) > 0 ? out_box_rows(pl) : pl.qr;
-  bool ok = (p.out_f32 ? map4_f32(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, obr)
-                       : map4(&maps[7], p.out, p.d, p.hq, p.nq, p.batch, qstride, obr)) &&
-            map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
+  bool ok = map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
             map4_kv(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false) &&
             map4_kv(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false);
   if (p.f8kv) {   // the cache as E4M3 codes (one byte per element)
@@ -1247,10 +1170,10 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   if (p.update) {
     win_box = update_box_rows(pl, p.win);
     if (win_box > 0)
-      ok = ok && map4_kv(&maps[8], p.kc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false) &&
-           map4_kv(&maps[9], p.vc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false);
+      ok = ok && map4_kv(&maps[7], p.kc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false) &&
+           map4_kv(&maps[8], p.vc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false);
   }
-  if (win_box == 0) maps[8] = maps[9] = maps[1];
+  if (win_box == 0) maps[7] = maps[8] = maps[1];
   if (!ok) return cudaErrorInvalidValue;
   Args a;
   a.win = p.update ? p.win : 0;
