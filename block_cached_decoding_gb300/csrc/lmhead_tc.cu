@@ -8,7 +8,8 @@
 // loads 1/CS of each W tile and multicasts it to all of them, so W leaves HBM
 // once per cluster and each CTA reads only its own hidden rows.  Per CTA (256
 // threads):
-//   warp 0  TMA producer: its hidden-row tile (128-row box) and its share of
+//   warp 0  TMA producer: its hidden-row tile (a box of the block rows rounded
+//           up to 16 when one CTA holds them all, else 128 rows) and its share of
 //           the W tile (64-row boxes, 128-byte swizzle, L2 evict-first) per
 //           64-wide K chunk, into an S-stage ring guarded by full/empty
 //           mbarriers; a stage is refilled only when every CTA of the cluster
@@ -61,7 +62,15 @@ constexpr int kMapElemBytes = 2;
 constexpr int kMapX = kRowBytes / kMapElemBytes;   // map units per stage along a row
 template <bool F8>
 constexpr int kChunk = F8 ? 128 : 64;   // K elements per stage: E4M3 or bf16
-constexpr int kABox = 128;       // block rows per hidden-tile box
+constexpr int kABox = 128;       // block rows per hidden-tile (one CTA's row tile)
+
+// Rows of the hidden-tile TMA box: the block rows rounded up to 16 when one CTA holds them all, else the
+// whole 128-row tile.  (A 128-row box over a tensor of fewer than 16 rows, the rest zero-filled, slowed
+// the whole W stream on GB300: 230 instead of 172 us for one sequence's 4 block rows.)  Tile rows past
+// the box are never written; they only feed accumulator rows that no block row owns.
+__host__ __device__ __forceinline__ int hidden_box_rows(int rows, int cs) {
+  return cs == 1 && rows <= kABox ? ((rows > 16 ? rows : 16) + 15) / 16 * 16 : kABox;
+}
 constexpr int kMaxSelectors = 8; // CTAs that run the merge + select at the end
 constexpr int kPrefetchers = 24; // first CTAs to start that warm L2 with the head of every CTA's W range
 constexpr int kPrefetchBytes = 1536;  // bytes of each W row of a first tile warmed in L2
@@ -161,7 +170,7 @@ __device__ __forceinline__ uint32_t share_bytes(int r, int nu) {
 // commits are settled the same way on the empty barriers: arrivals of CTAs that never committed a
 // stage are made by this CTA itself, and the phase then completes when the real ones have landed.
 template <int CS>
-__device__ void settle_after_abort(Shared &sh, int c, int u0, int u1, int kchunks, int32_t *err) {
+__device__ void settle_after_abort(Shared &sh, int c, int u0, int u1, int kchunks, uint32_t a_bytes, int32_t *err) {
   using C = Cfg;
   int iss[CS], con[CS];
   int hi_iss = 0, hi_con = 0;
@@ -182,12 +191,12 @@ __device__ void settle_after_abort(Shared &sh, int c, int u0, int u1, int kchunk
     const int st = it % C::STAGES;
     const int t = it / kchunks;
     const int nu = min(C::UNITS, u1 - (u0 + t * C::UNITS));
-    uint32_t sent = iss[c] > it ? (uint32_t)C::A_BYTES : 0u;   // this CTA's own hidden tile
+    uint32_t sent = iss[c] > it ? a_bytes : 0u;             // this CTA's own hidden tile
 #pragma unroll
     for (int r = 0; r < CS; ++r)
       if (iss[r] > it) sent += share_bytes<CS>(r, nu);
     if (iss[c] > it) {
-      const uint32_t armed = (uint32_t)C::A_BYTES + (uint32_t)nu * (uint32_t)(kUnit * kRowBytes);
+      const uint32_t armed = a_bytes + (uint32_t)nu * (uint32_t)(kUnit * kRowBytes);
       if (armed > sent) tc::mbar_complete_tx(&sh.full[st], armed - sent);
     } else {
       tc::mbar_arrive_expect_tx(&sh.full[st], sent);
@@ -226,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x, g = blockIdx.x;
   const int c = CS > 1 ? (int)tc::cluster_ctarank() : 0;   // this CTA's row tile
   const int ncl = G / CS, k = g / CS;                      // vocabulary splits = clusters; this cluster
+  const uint32_t a_bytes = (uint32_t)(hidden_box_rows(rows, CS) * kRowBytes);   // hidden tile per stage
   constexpr uint16_t kAll = (uint16_t)((1u << CS) - 1u);   // every CTA of the cluster
 
   // vocabulary units [u0, u1) of this cluster
@@ -312,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < ntiles && go; ++t) {
           const int tu0 = u0 + t * C::UNITS;
           const int nu = min(C::UNITS, u1 - tu0);
-          const uint32_t bytes = (uint32_t)(kABox * kRowBytes + nu * kUnit * kRowBytes);
+          const uint32_t bytes = a_bytes + (uint32_t)(nu * kUnit * kRowBytes);
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int st = it % C::STAGES;
             const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
@@ -447,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barrier every CTA of the cluster has stopped too, and an abort anywhere is visible everywhere, so
   // either no CTA or every CTA settles.
   if (CS > 1 && shape_ok) tc::cluster_sync();
-  if (*abort_flag && run && threadIdx.x == 0) settle_after_abort<CS>(sh, c, u0, u1, kchunks, err);
+  if (*abort_flag && run && threadIdx.x == 0) settle_after_abort<CS>(sh, c, u0, u1, kchunks, a_bytes, err);
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
   if (CS > 1 && shape_ok) tc::cluster_sync();          // no CTA leaves while a peer may still address it
@@ -526,7 +536,8 @@ template <int CS, bool F8>
 cudaError_t launch_cs(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, uint32_t epoch,
                       int splits, cudaStream_t st) {
   CUtensorMap mh, mw;
-  if (!make_map(&mh, F8 ? p.hq : p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H, kABox, F8) ||
+  if (!make_map(&mh, F8 ? p.hq : p.hidden, (uint64_t)p.batch * p.B, (uint64_t)p.H,
+                (uint32_t)hidden_box_rows(p.batch * p.B, CS), F8) ||
       !make_map(&mw, p.w, (uint64_t)p.V, (uint64_t)p.H, kUnit, F8))
     return cudaErrorInvalidValue;
   auto kfn = lmhead_tc_kernel<CS, F8>;
