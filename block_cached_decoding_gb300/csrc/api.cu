@@ -315,7 +315,7 @@ using namespace fdllm;
 
 extern "C" {
 
-int32_t fdllm_version(void) { return 105; }
+int32_t fdllm_version(void) { return 106; }
 
 fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream) {
   if (limit_ms < 1 || limit_ms > 1000) return fail(FDLLM_EINVAL, "selftest: limit_ms must be in 1..1000");

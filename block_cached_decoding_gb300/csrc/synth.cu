@@ -44,11 +44,14 @@ __global__ void normals_kernel(uint64_t key, int64_t n, int64_t offset, float si
     store(out + i, __fmul_rn(normal12(key, (uint64_t)(offset + i)), sigma));
 }
 
-// one stream per (b, epoch): out [b, per]
+// one stream per (b, epoch): out [b, per]; per-sequence epochs and a sequence filter when given
 template <typename T>
 __global__ void kv_kernel(uint64_t seed, int kind, int64_t epoch, int64_t per, float sigma, T *out,
-                          const int64_t *epoch_add = nullptr, int64_t epoch_div = 1) {
+                          const int64_t *epoch_add = nullptr, int64_t epoch_div = 1,
+                          const int32_t *epoch_seq = nullptr, const uint8_t *only = nullptr) {
   const int b = blockIdx.y;
+  if (only != nullptr && only[b] == 0) return;
+  if (epoch_seq != nullptr) epoch = epoch_seq[b];
   if (epoch_add != nullptr) epoch += *epoch_add / epoch_div;
   const uint64_t key = splitmix(splitmix(splitmix(seed, (uint64_t)kind), (uint64_t)b), (uint64_t)epoch);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per;
@@ -62,12 +65,15 @@ __device__ __forceinline__ uint64_t row_key(uint64_t seed, int kind, int b, int6
 }
 
 // rows [b, npos, width]: grid (npos, b); the step is step + *step_add when step_add is given (a device
-// counter, e.g. a graph loop's)
+// counter, e.g. a graph loop's); per-sequence steps and first positions when step_seq / pos_seq are given
 template <typename T>
 __global__ void rows_kernel(uint64_t seed, int kind, int64_t step, const int64_t *step_add, int pos0, int npos,
-                            int width, float sigma, T *out) {
+                            int width, float sigma, T *out, const int32_t *step_seq = nullptr,
+                            const int32_t *pos_seq = nullptr) {
   const int p = blockIdx.x, b = blockIdx.y;
   if (step_add != nullptr) step += *step_add;
+  if (step_seq != nullptr) step = step_seq[b];
+  if (pos_seq != nullptr) pos0 = pos_seq[b];
   const uint64_t key = row_key(seed, kind, b, step, pos0 + p);
   T *row = out + ((int64_t)b * npos + p) * width;
   for (int i = threadIdx.x; i < width; i += blockDim.x)
@@ -76,9 +82,12 @@ __global__ void rows_kernel(uint64_t seed, int kind, int64_t step, const int64_t
 
 template <typename T>
 __global__ void hidden_kernel(uint64_t seed, int64_t step, const int64_t *step_add, int pos0, int npos, int hidden,
-                              int vocab, uint64_t plant_thr, const T *w, T *out) {
+                              int vocab, uint64_t plant_thr, const T *w, T *out, const int32_t *step_seq = nullptr,
+                              const int32_t *pos_seq = nullptr) {
   const int p = blockIdx.x, b = blockIdx.y;
   if (step_add != nullptr) step += *step_add;
+  if (step_seq != nullptr) step = step_seq[b];
+  if (pos_seq != nullptr) pos0 = pos_seq[b];
   const uint64_t pk = row_key(seed, FDLLM_SYNTH_PLANT, b, step, pos0 + p);
   const bool planted = (splitmix(pk, 0) >> 40) < plant_thr;
   const int64_t target = (int64_t)(((splitmix(pk, 1) >> 32) * (uint64_t)vocab) >> 32);
@@ -199,6 +208,59 @@ extern "C" int32_t fdllm_synth_hidden_at(uint64_t seed, int32_t batch, int64_t s
   else
     hidden_kernel<<<grid, 128, 0, st>>>(seed, step, step_add, pos0, npos, hidden, vocab, thr, (const float *)w,
                                         (float *)out);
+  return finish();
+}
+
+extern "C" int32_t fdllm_synth_rows_seq(uint64_t seed, int32_t kind, int32_t batch, const int32_t *step,
+                                        const int32_t *pos0, int32_t npos, int32_t width, float sigma, int32_t dtype,
+                                        void *out, fdllm_stream_t stream) {
+  if (batch < 1 || batch > 65535 || npos < 0 || width < 1 || !step || !pos0 || (npos > 0 && !out) ||
+      (dtype != FDLLM_BF16 && dtype != FDLLM_F32))
+    return FDLLM_EINVAL;
+  if (npos == 0) return FDLLM_OK;
+  dim3 grid(npos, batch);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (dtype == FDLLM_BF16)
+    rows_kernel<<<grid, 128, 0, st>>>(seed, kind, 0, nullptr, 0, npos, width, sigma, (__nv_bfloat16 *)out, step,
+                                      pos0);
+  else
+    rows_kernel<<<grid, 128, 0, st>>>(seed, kind, 0, nullptr, 0, npos, width, sigma, (float *)out, step, pos0);
+  return finish();
+}
+
+extern "C" int32_t fdllm_synth_hidden_seq(uint64_t seed, int32_t batch, const int32_t *step, const int32_t *pos0,
+                                          int32_t npos, int32_t hidden, int32_t vocab, double p_plant, const void *w,
+                                          int32_t dtype, void *out, fdllm_stream_t stream) {
+  if (batch < 1 || batch > 65535 || npos < 0 || hidden < 1 || vocab < 1 || !w || !step || !pos0 ||
+      (npos > 0 && !out) || (dtype != FDLLM_BF16 && dtype != FDLLM_F32) || !(p_plant >= 0.0))
+    return FDLLM_EINVAL;
+  if (npos == 0) return FDLLM_OK;
+  const uint64_t thr = (uint64_t)floor(p_plant * (double)(1 << 24));
+  dim3 grid(npos, batch);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (dtype == FDLLM_BF16)
+    hidden_kernel<<<grid, 128, 0, st>>>(seed, 0, nullptr, 0, npos, hidden, vocab, thr, (const __nv_bfloat16 *)w,
+                                        (__nv_bfloat16 *)out, step, pos0);
+  else
+    hidden_kernel<<<grid, 128, 0, st>>>(seed, 0, nullptr, 0, npos, hidden, vocab, thr, (const float *)w,
+                                        (float *)out, step, pos0);
+  return finish();
+}
+
+extern "C" int32_t fdllm_synth_kv_cache_seq(uint64_t seed, int32_t kind, int32_t batch, int32_t seq_len,
+                                            int32_t n_kv_heads, int32_t head_dim, const int32_t *epoch,
+                                            const uint8_t *only, float sigma, int32_t dtype, void *out,
+                                            fdllm_stream_t stream) {
+  if (batch < 1 || batch > 65535 || seq_len < 1 || n_kv_heads < 1 || head_dim < 1 || !out || !epoch ||
+      (dtype != FDLLM_BF16 && dtype != FDLLM_F32))
+    return FDLLM_EINVAL;
+  const int64_t per = (int64_t)seq_len * n_kv_heads * head_dim;
+  dim3 grid(grid_for(per) / (unsigned)batch + 1, batch);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (dtype == FDLLM_BF16)
+    kv_kernel<<<grid, 256, 0, st>>>(seed, kind, 0, per, sigma, (__nv_bfloat16 *)out, nullptr, 1, epoch, only);
+  else
+    kv_kernel<<<grid, 256, 0, st>>>(seed, kind, 0, per, sigma, (float *)out, nullptr, 1, epoch, only);
   return finish();
 }
 

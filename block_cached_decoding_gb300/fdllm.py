@@ -30,7 +30,8 @@ EXPORTS = (
     "fdllm_confidence_select_fp8w", "fdllm_block_attn_fp8kv", "fdllm_kv_splice_fp8", "fdllm_block_loop_create",
     "fdllm_block_loop_launch", "fdllm_block_loop_destroy", "fdllm_synth_rows_at", "fdllm_synth_hidden_at",
     "fdllm_kv_splice_fp8_ragged", "fdllm_block_attn_update", "fdllm_block_loop_create_refresh",
-    "fdllm_synth_kv_cache_at",
+    "fdllm_synth_kv_cache_at", "fdllm_block_loop_create_ragged", "fdllm_synth_rows_seq", "fdllm_synth_hidden_seq",
+    "fdllm_synth_kv_cache_seq",
 )
 
 # void step(void *user, fdllm_stream_t stream)
@@ -131,12 +132,19 @@ def lib() -> C.CDLL:
         L.fdllm_block_loop_create_refresh.argtypes = [C.POINTER(vp), STEP_FN, STEP_FN, vp, vp, i32, i32, i32, vp, vp]
         L.fdllm_block_loop_create_refresh.restype = i32
         L.fdllm_synth_kv_cache_at.argtypes = [u64, i32, i32, i32, i32, i32, i64, vp, i64, C.c_float, i32, vp, vp]
+        L.fdllm_block_loop_create_ragged.argtypes = [C.POINTER(vp), STEP_FN, STEP_FN, vp, vp, i32, i32, i32, i32,
+                                                     vp, vp, vp, vp, vp, vp, vp]
+        L.fdllm_block_loop_create_ragged.restype = i32
+        L.fdllm_synth_rows_seq.argtypes = [u64, i32, i32, vp, vp, i32, i32, C.c_float, i32, vp, vp]
+        L.fdllm_synth_hidden_seq.argtypes = [u64, i32, vp, vp, i32, i32, i32, C.c_double, vp, i32, vp, vp]
+        L.fdllm_synth_kv_cache_seq.argtypes = [u64, i32, i32, i32, i32, i32, vp, vp, C.c_float, i32, vp, vp]
         L.fdllm_block_loop_launch.argtypes = [vp, vp]
         L.fdllm_block_loop_launch.restype = i32
         L.fdllm_block_loop_destroy.argtypes = [vp]
         L.fdllm_block_loop_destroy.restype = None
         for f in ("fdllm_synth_normals", "fdllm_synth_kv_cache", "fdllm_synth_rows", "fdllm_synth_hidden",
-                  "fdllm_synth_prompt", "fdllm_synth_rows_at", "fdllm_synth_hidden_at", "fdllm_synth_kv_cache_at"):
+                  "fdllm_synth_prompt", "fdllm_synth_rows_at", "fdllm_synth_hidden_at", "fdllm_synth_kv_cache_at",
+                  "fdllm_synth_rows_seq", "fdllm_synth_hidden_seq", "fdllm_synth_kv_cache_seq"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -376,14 +384,36 @@ def fdllm_synth_hidden_at(seed, batch, step, step_add, pos0, npos, hidden, vocab
                                        _ptr(w), dtype, _ptr(out), _stream(stream)))
 
 
+def fdllm_synth_rows_seq(seed, kind, batch, step, pos0, npos, width, sigma, dtype, out, stream=None):
+    """fdllm_synth_rows with sequence b at step[b] and first position pos0[b] (device int32 [batch])."""
+    _check(lib().fdllm_synth_rows_seq(seed, kind, batch, _ptr(step), _ptr(pos0), npos, width, sigma, dtype,
+                                      _ptr(out), _stream(stream)))
+
+
+def fdllm_synth_hidden_seq(seed, batch, step, pos0, npos, hidden, vocab, p_plant, w, dtype, out, stream=None):
+    _check(lib().fdllm_synth_hidden_seq(seed, batch, _ptr(step), _ptr(pos0), npos, hidden, vocab, p_plant, _ptr(w),
+                                        dtype, _ptr(out), _stream(stream)))
+
+
+def fdllm_synth_kv_cache_seq(seed, kind, batch, seq_len, n_kv_heads, head_dim, epoch, only, sigma, dtype, out,
+                             stream=None):
+    """Cache rows of sequence b for epoch epoch[b] (device int32), only where only[b] (device uint8, or None)."""
+    _check(lib().fdllm_synth_kv_cache_seq(seed, kind, batch, seq_len, n_kv_heads, head_dim, _ptr(epoch), _ptr(only),
+                                          sigma, dtype, _ptr(out), _stream(stream)))
+
+
 class BlockLoop:
     """fdllm_block_loop: `step(stream)` is captured once as the body of a device-side while-loop that runs
     until n_masked_left is all zero or max_steps steps have run; `counter` (device int64) counts them per
     launch, `total` (device int64 or None) across launches."""
 
-    def __init__(self, step, n_masked_left, batch, max_steps, counter, total=None, refresh=None, refresh_every=0):
+    def __init__(self, step, n_masked_left, batch, max_steps, counter, total=None, refresh=None, refresh_every=0,
+                 ragged=None):
         """With `refresh(stream)` and refresh_every = r, fdllm_block_loop_create_refresh: the captured refresh
-        runs before step c of each launch whenever c > 0 and r divides c."""
+        runs before step c of each launch whenever c > 0 and r divides c.  With `ragged` = dict(n_blocks,
+        block_size, block_idx, block_start, seq_steps, refresh_flags, done) (device tensors),
+        fdllm_block_loop_create_ragged: one loop over the whole per-sequence generation, `refresh(stream)`
+        (optional) running whenever some sequence moved to its next block."""
         self._h = None
         errors = []
 
@@ -397,7 +427,14 @@ class BlockLoop:
 
         self._cb = STEP_FN(wrap(step))           # kept alive with the loop
         h = C.c_void_p()
-        if refresh is not None and refresh_every:
+        if ragged is not None:
+            self._rcb = STEP_FN(wrap(refresh)) if refresh is not None else STEP_FN(0)
+            st = lib().fdllm_block_loop_create_ragged(
+                C.byref(h), self._cb, self._rcb, None, _ptr(n_masked_left), batch, ragged["n_blocks"],
+                ragged["block_size"], max_steps, _ptr(ragged["block_idx"]), _ptr(ragged["block_start"]),
+                _ptr(ragged["seq_steps"]), _ptr(ragged["refresh_flags"]), _ptr(ragged["done"]), _ptr(counter),
+                _ptr(total))
+        elif refresh is not None and refresh_every:
             self._rcb = STEP_FN(wrap(refresh))
             st = lib().fdllm_block_loop_create_refresh(C.byref(h), self._cb, self._rcb, None, _ptr(n_masked_left),
                                                        batch, max_steps, refresh_every, _ptr(counter), _ptr(total))

@@ -249,6 +249,130 @@ class BlockDecoder:
                 raise RuntimeError(f"block {k} did not finish within {cap} steps")
         return self.tokens, steps
 
+    # -- per-sequence blocks (each sequence moves on as soon as its own block is decoded) --------------
+    def _ragged_state(self):
+        """Device state of a per-sequence generation, reset to every sequence at its first block with
+        its caches refreshed for it (refresh epoch = the sequence's block index)."""
+        wl = self.wl
+        if wl.mode != "dual":
+            raise ValueError("per-sequence blocks need DualCache")
+        b, dev = wl.batch, self.w.device
+        if not hasattr(self, "rg"):
+            self.rg = {"n_blocks": wl.gen_length // wl.block_size, "block_size": wl.block_size,
+                       "block_idx": torch.zeros(b, dtype=torch.int32, device=dev),
+                       "block_start": torch.zeros(b, dtype=torch.int32, device=dev),
+                       "seq_steps": torch.zeros(b, dtype=torch.int32, device=dev),
+                       "refresh_flags": torch.zeros(b, dtype=torch.uint8, device=dev),
+                       "done": torch.zeros(b, dtype=torch.uint8, device=dev)}
+        rg = self.rg
+        rg["block_idx"].zero_()
+        rg["block_start"].fill_(wl.prompt_len)
+        rg["seq_steps"].zero_()
+        rg["refresh_flags"].zero_()
+        rg["done"].zero_()
+        self.reset_tokens()
+        self.ragged_refresh(None, only=None)
+        return rg
+
+    def ragged_refresh(self, stream, only="flags"):
+        """The caches of the flagged sequences (all with only=None) recomputed for their current block:
+        the synthetic stand-in draws refresh epoch block_idx[b] straight into the caches."""
+        wl, rg = self.wl, self.rg
+        flags = rg["refresh_flags"] if only == "flags" else None
+        for kind, cache in ((F.SYNTH_KCACHE, self.kc), (F.SYNTH_VCACHE, self.vc)):
+            F.fdllm_synth_kv_cache_seq(wl.seed, kind, wl.batch, wl.seq_len, wl.n_kv_heads, wl.head_dim,
+                                       rg["block_idx"], flags, 1.0, self.code, cache, stream)
+
+    def ragged_step(self, stream=None):
+        """One step of every sequence at its own block: inputs drawn at the sequence's own step and
+        window, attention with the window update, select (the *_ragged calls)."""
+        wl, rg = self.wl, self.rg
+        b, hq, hkv, d, B = wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.head_dim, wl.block_size
+        q, out = _packed(self.q, (b, B, hq, d)), _packed(self.attn_out, (b, B, hq, d))
+        kf, vf = _packed(self.kf, (b, B, hkv, d)), _packed(self.vf, (b, B, hkv, d))
+        st, p0 = rg["seq_steps"], rg["block_start"]
+        F.fdllm_synth_rows_seq(wl.seed, F.SYNTH_Q, b, st, p0, B, hq * d, 1.0, self.code, q, stream)
+        F.fdllm_synth_rows_seq(wl.seed, F.SYNTH_KFRESH, b, st, p0, B, hkv * d, 1.0, self.code, kf, stream)
+        F.fdllm_synth_rows_seq(wl.seed, F.SYNTH_VFRESH, b, st, p0, B, hkv * d, 1.0, self.code, vf, stream)
+        F.fdllm_synth_hidden_seq(wl.seed, b, st, p0, B, wl.hidden, wl.vocab, wl.p_plant, self.w, self.code,
+                                 self.hidden, stream)
+        F.fdllm_block_attn_update(self.attn_desc(0), rg["block_idx"], q, self.kc, self.vc, kf, vf, out, None,
+                                  self.attn_ws, ws_bytes=self.attn_ws_bytes, stream=stream)
+        F.fdllm_confidence_select_ragged(self.select_desc(wl.prompt_len), p0, self.hidden, self.w, self.tokens,
+                                         self.unmasked, self.conf, self.kappa, self.argmax, self.n_left,
+                                         self.sel_ws, stream=stream)
+        return out
+
+    def run_ragged(self, hook=None):
+        """Host-driven per-sequence generation: after each step the host reads the masked counts and moves
+        each finished block's sequence on (as fdllm_block_loop_create_ragged's control kernel does), then
+        refreshes the moved sequences' caches.  `hook(decoder, out, blocks, starts, steps, done)` sees
+        each step's outputs and the state it ran with.  Returns (tokens, steps per sequence)."""
+        wl = self.wl
+        rg = self._ragged_state()
+        nb, B = rg["n_blocks"], wl.block_size
+        blk = [0] * wl.batch
+        steps = [0] * wl.batch
+        done = [False] * wl.batch
+        for _ in range(nb * B):
+            if all(done):
+                break
+            out = self.ragged_step()
+            left = self.n_left.cpu().tolist()
+            if hook is not None:
+                hook(self, out, list(blk), [wl.prompt_len + k * B for k in blk], list(steps), list(done))
+            flags = [0] * wl.batch
+            for i in range(wl.batch):
+                if done[i]:
+                    continue
+                steps[i] += 1
+                if left[i] == 0:
+                    if blk[i] + 1 == nb:
+                        done[i] = True
+                    else:
+                        blk[i] += 1
+                        flags[i] = 1
+            rg["block_idx"].copy_(torch.tensor(blk, dtype=torch.int32))
+            rg["block_start"].copy_(torch.tensor([wl.prompt_len + k * B for k in blk], dtype=torch.int32))
+            rg["seq_steps"].copy_(torch.tensor(steps, dtype=torch.int32))
+            rg["refresh_flags"].copy_(torch.tensor(flags, dtype=torch.uint8))
+            if any(flags):
+                self.ragged_refresh(None)
+        if not all(done):
+            raise RuntimeError("a sequence did not finish within n_blocks * block_size steps")
+        return self.tokens, steps
+
+    def capture_ragged(self):
+        """The per-sequence generation captured as one device-driven loop (fdllm_block_loop_create_ragged);
+        returns (loop, device step counter)."""
+        wl = self.wl
+        rg = self._ragged_state()
+        counter = torch.zeros(1, dtype=torch.int64, device=self.w.device)
+        loop = F.BlockLoop(lambda stream: self.ragged_step(stream), self.n_left, wl.batch,
+                           rg["n_blocks"] * wl.block_size, counter, refresh=lambda stream: self.ragged_refresh(stream),
+                           ragged=rg)
+        return loop, counter
+
+    def launch_ragged(self, loop):
+        """A fresh generation through a captured per-sequence loop: state, tokens and caches reset on the
+        device, then the loop launched; nothing waits on the host."""
+        self._ragged_state()
+        loop.launch()
+
+    def run_ragged_graph(self):
+        """The same generation as `run_ragged` as one device-driven loop: the host launches it once and reads
+        the per-sequence step counts at the end."""
+        loop, _ = self.capture_ragged()
+        try:
+            self.launch_ragged(loop)
+            steps = self.rg["seq_steps"].tolist()
+            done = self.rg["done"].tolist()
+        finally:
+            loop.close()
+        if not all(done):
+            raise RuntimeError("a sequence did not finish within n_blocks * block_size steps")
+        return self.tokens, steps
+
     def run(self, hook=None, max_steps_per_block: int | None = None):
         """Decode every block left to right; returns (tokens, steps per block)."""
         wl = self.wl

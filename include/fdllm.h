@@ -421,6 +421,41 @@ fdllm_status fdllm_block_loop_create_refresh(fdllm_block_loop **loop, fdllm_step
                                              int32_t max_steps, int32_t refresh_every, int64_t *step_counter,
                                              int64_t *total_steps);
 
+/* A whole generation in the per-sequence regime as one device-driven loop
+ * (Fast-dLLM summary §5 "Throughput scaling with batch size" and Appendix
+ * C.5: each sequence of the batch moves to its next block as soon as its own
+ * block has no mask, rather than waiting for the whole batch).  The caller's
+ * `step` reads the per-sequence state below (typically through the *_ragged
+ * calls: block_idx for the attention, block_start for the select and splice)
+ * and writes n_masked_left.  After each step the control kernel, for every
+ * unfinished sequence b: adds 1 to seq_steps[b]; if n_masked_left[b] is 0,
+ * either moves it to its next block (block_idx[b] += 1, block_start[b] +=
+ * block_size, refresh_flags[b] = 1) or, after block n_blocks - 1, sets
+ * done[b] = 1.  refresh_flags of sequences that did not move are cleared.
+ * The loop repeats while some done[b] is 0 and fewer than max_steps steps
+ * have run (n_blocks * block_size always suffices: every step unmasks at
+ * least one position of every unfinished sequence).  With a non-null
+ * `refresh`, it is captured into a conditional node that runs before the next
+ * step whenever some sequence moved: it should recompute the caches of the
+ * flagged sequences (reading refresh_flags and block_idx).  A finished
+ * sequence keeps its last block index, so the captured calls stay in range;
+ * it has no masked position left, so its outputs no longer change.
+ *
+ * Arguments (all device memory, int32 / uint8 [batch], caller-initialised
+ * before each launch: block_idx the first block of each sequence, block_start
+ * = prompt_len + block_idx * block_size, seq_steps 0, refresh_flags 0, done 0,
+ * and the caches refreshed for the first blocks): as listed; step_counter /
+ * total_steps as in fdllm_block_loop_create (steps of this launch / all
+ * launches).  FDLLM_EINVAL for a null state pointer, batch < 1,
+ * n_blocks < 1, block_size < 1 or max_steps < 1; FDLLM_ECUDA if capture or
+ * instantiation fails. */
+fdllm_status fdllm_block_loop_create_ragged(fdllm_block_loop **loop, fdllm_step_fn step, fdllm_step_fn refresh,
+                                            void *user, const int32_t *n_masked_left, int32_t batch,
+                                            int32_t n_blocks, int32_t block_size, int32_t max_steps,
+                                            int32_t *block_idx, int32_t *block_start, int32_t *seq_steps,
+                                            uint8_t *refresh_flags, uint8_t *done, int64_t *step_counter,
+                                            int64_t *total_steps);
+
 /* Run the loop once on `stream` (asynchronous). */
 fdllm_status fdllm_block_loop_launch(fdllm_block_loop *loop, fdllm_stream_t stream);
 
@@ -453,7 +488,8 @@ fdllm_status fdllm_selftest_bounded_wait(int32_t limit_ms, fdllm_stream_t stream
 
 /* ABI version: 100 * major + minor (101: the per-sequence block calls; 102: the
  * FP8 weight cache; 103: the FP8 KV cache; 104: the device-driven block loop;
- * 105: fdllm_block_attn_update and the loop's refresh every r steps). */
+ * 105: fdllm_block_attn_update and the loop's refresh every r steps; 106: the
+ * per-sequence device-driven loop). */
 int32_t fdllm_version(void);
 
 /* Number of kernels this library has launched in the process so far (all

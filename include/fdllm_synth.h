@@ -78,6 +78,23 @@ int32_t fdllm_synth_hidden_at(uint64_t seed, int32_t batch, int64_t step, const 
                               int32_t npos, int32_t hidden, int32_t vocab, double p_plant, const void *w,
                               int32_t dtype, void *out, fdllm_stream_t stream);
 
+/* Per-sequence forms, for sequences that each sit at their own block and step (a generation in which
+ * every sequence moves to its next block on its own): sequence b uses step[b] and positions
+ * pos0[b] + p (device int32 [b] arrays read when the kernel runs), the same keys as the lock-step calls
+ * above with that step and position. */
+int32_t fdllm_synth_rows_seq(uint64_t seed, int32_t kind, int32_t batch, const int32_t *step, const int32_t *pos0,
+                             int32_t npos, int32_t width, float sigma, int32_t dtype, void *out,
+                             fdllm_stream_t stream);
+int32_t fdllm_synth_hidden_seq(uint64_t seed, int32_t batch, const int32_t *step, const int32_t *pos0, int32_t npos,
+                               int32_t hidden, int32_t vocab, double p_plant, const void *w, int32_t dtype, void *out,
+                               fdllm_stream_t stream);
+/* Cache rows of sequence b drawn for refresh epoch epoch[b] (device int32 [b]) into out [b, N, Hkv, d], only
+ * for the sequences whose only[b] is nonzero (device uint8 [b]; NULL: every sequence); the others are left
+ * untouched. */
+int32_t fdllm_synth_kv_cache_seq(uint64_t seed, int32_t kind, int32_t batch, int32_t seq_len, int32_t n_kv_heads,
+                                 int32_t head_dim, const int32_t *epoch, const uint8_t *only, float sigma,
+                                 int32_t dtype, void *out, fdllm_stream_t stream);
+
 /* Prompt ids out int32 [b, P], uniform over [0, vocab). */
 int32_t fdllm_synth_prompt(uint64_t seed, int32_t batch, int32_t prompt_len, int32_t vocab,
                            int32_t *out, fdllm_stream_t stream);

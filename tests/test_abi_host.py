@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert F.fdllm_version() == 105
+    assert F.fdllm_version() == 106
     for s in range(5):
         assert lib.fdllm_status_string(s).decode().startswith("FDLLM_")
 

@@ -192,3 +192,80 @@ def test_refresh_every_step_equals_full_attention_on_the_gpu():
     f = lambda x: synth.as_f32(x, "bf16").astype(np.float64)
     ref, _ = O.attention_full(f(q_all[:, s:s + B]), f(full_k), f(full_v), h, h)
     assert_attention_close(a, ref)
+
+
+# ---------------------------------------------------------------------------
+# per-sequence blocks: each sequence moves to its next block on its own
+# ---------------------------------------------------------------------------
+
+def _ragged_wl():
+    return configs.LLADA_BATCH.with_(batch=4, prompt_len=40, gen_length=64, block_size=16, n_q_heads=4,
+                                     n_kv_heads=2, head_dim=128, hidden=256, vocab=1500, p_plant=0.3, seed=9)
+
+
+def test_per_sequence_blocks_host_loop_against_the_oracle():
+    """Each sequence moves to its next block as soon as its own block is decoded, its caches then
+    recomputed for that block (the per-sequence reading of the batched loop).  At every step the oracle
+    evaluates each unfinished sequence at its own block, step and cache epoch: the attention of every
+    query row and the select of every masked row."""
+    wl, tau = _ragged_wl(), 0.9
+    b, B, hq, hkv, d = wl.batch, wl.block_size, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    w64 = f64(synth.lm_head_weight(wl.seed, wl.vocab, wl.hidden, wl.sigma_w, wl.dtype), wl.dtype)
+    dec = BlockDecoder(wl, tau=tau, fused_update=True)
+    state = {"exempt": 0, "apart": 0, "checked": 0}
+
+    def hook(dd, out, blocks, starts, steps, done):
+        state["apart"] += len({blocks[i] for i in range(b) if not done[i]}) > 1
+        t_after = dd.tokens.cpu().numpy().astype(np.int64)
+        um = dd.unmasked.cpu().numpy().astype(bool)
+        got = {"unmask": um, "conf": dd.conf.cpu().numpy(), "kappa": dd.kappa.cpu().numpy(),
+               "token": dd.argmax.cpu().numpy()}
+        o_gpu = out.cpu().numpy().astype(np.float64)
+        for i in range(b):
+            if done[i]:
+                continue
+            s, g, ep = starts[i], steps[i], blocks[i]
+            pos = range(s, s + B)
+            kc = f64(synth.kv_cache(wl.seed, synth.KIND_KCACHE, b, wl.seq_len, hkv, d, ep, wl.dtype), wl.dtype)[i:i + 1]
+            vc = f64(synth.kv_cache(wl.seed, synth.KIND_VCACHE, b, wl.seq_len, hkv, d, ep, wl.dtype), wl.dtype)[i:i + 1]
+            q = f64(synth.per_position(wl.seed, synth.KIND_Q, b, g, pos, hq * d, wl.dtype), wl.dtype)[i:i + 1]
+            kf = f64(synth.per_position(wl.seed, synth.KIND_KFRESH, b, g, pos, hkv * d, wl.dtype), wl.dtype)[i:i + 1]
+            vf = f64(synth.per_position(wl.seed, synth.KIND_VFRESH, b, g, pos, hkv * d, wl.dtype), wl.dtype)[i:i + 1]
+            o_ref, _ = O.block_attention(q.reshape(1, B, hq, d), kc, vc, kf.reshape(1, B, hkv, d),
+                                         vf.reshape(1, B, hkv, d), mode="dual", s=s, e=s + B, n_q_heads=hq,
+                                         n_kv_heads=hkv)
+            assert_attention_close(o_gpu[i:i + 1], o_ref)
+            t_before = t_after[i:i + 1].copy()
+            t_before[:, s:s + B][um[i:i + 1]] = wl.mask_id
+            hid, _, _ = synth.hidden_states(wl.seed, b, g, pos, wl.hidden, wl.vocab, wl.sigma_w, wl.dtype, wl.p_plant)
+            _, info = O.decode_step(t_before, f64(hid, wl.dtype)[i:i + 1], w64, s=s, block_size=B,
+                                    mask_id=wl.mask_id, tau=tau)
+            state["exempt"] += compare_select(info, {k: v[i:i + 1] for k, v in got.items()}, tau)
+            state["checked"] += 1
+
+    tokens, steps = dec.run_ragged(hook=hook)
+    t = tokens.cpu().numpy()
+    assert not (t == wl.mask_id).any() and t.max() < wl.vocab
+    assert all(n <= wl.gen_length for n in steps)
+    assert state["apart"] >= 3                     # the sequences were at different blocks at times
+    assert state["exempt"] <= 2 + 0.01 * state["checked"] * B
+
+
+@pytest.mark.parametrize("tau", [0.9, 1.0])
+def test_per_sequence_device_loop_matches_the_host_loop(tau):
+    """The whole per-sequence generation as one CUDA-graph while-loop (fdllm_block_loop_create_ragged:
+    each sequence's block index, window start and step advanced on the device, the moved sequences'
+    caches refreshed in a conditional node) gives the host loop's tokens and per-sequence step counts
+    exactly."""
+    wl = _ragged_wl()
+    t_host, s_host = BlockDecoder(wl, tau=tau, fused_update=True).run_ragged()
+    t_host = t_host.clone()
+    dec = BlockDecoder(wl, tau=tau, fused_update=True)
+    t_dev, s_dev = dec.run_ragged_graph()
+    assert s_dev == s_host
+    assert torch.equal(t_dev, t_host)
+    assert dec.rg["block_idx"].tolist() == [wl.gen_length // wl.block_size - 1] * wl.batch
+    if tau >= 1.0:
+        assert s_dev == [wl.gen_length] * wl.batch    # one position per step, every sequence
+    t_again, s_again = dec.run_ragged_graph()          # a second launch of a fresh loop starts over
+    assert s_again == s_host and torch.equal(t_again, t_host)

@@ -47,3 +47,31 @@ def test_rows_hidden_and_prompt(dtype):
     pr = torch.empty(2, 77, dtype=torch.int32, device="cuda")
     F.fdllm_synth_prompt(11, 2, 77, 126464, pr)
     assert np.array_equal(pr.cpu().numpy(), synth.prompt_tokens(11, 2, 77, 126464))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_per_sequence_draws(dtype):
+    """Sequence b at its own step and window, and a cache redraw of the flagged sequences only: the
+    lock-step draws' bytes for that sequence, step, position and epoch."""
+    dc = F.F32 if dtype == "f32" else F.BF16
+    steps, starts, epochs = [3, 0, 7], [40, 56, 72], [2, 0, 1]
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    q = torch.empty(3, 8, 128, dtype=tdtype(dtype), device="cuda")
+    F.fdllm_synth_rows_seq(13, F.SYNTH_KFRESH, 3, i32(steps), i32(starts), 8, 128, 1.0, dc, q)
+    for b in range(3):
+        ref = synth.per_position(13, synth.KIND_KFRESH, 3, steps[b], range(starts[b], starts[b] + 8), 128, dtype)[b]
+        assert np.array_equal(_bits(q)[b], ref)
+    V, H = 700, 128
+    w = dev(synth.lm_head_weight(13, V, H, 0.2236, dtype), dtype)
+    hid = torch.empty(3, 8, H, dtype=tdtype(dtype), device="cuda")
+    F.fdllm_synth_hidden_seq(13, 3, i32(steps), i32(starts), 8, H, V, 0.5, w, dc, hid)
+    for b in range(3):
+        ref, _, _ = synth.hidden_states(13, 3, steps[b], range(starts[b], starts[b] + 8), H, V, 0.2236, dtype, 0.5)
+        assert np.array_equal(_bits(hid)[b], ref[b])
+    kc = torch.zeros(3, 24, 2, 64, dtype=tdtype(dtype), device="cuda")
+    only = torch.tensor([1, 0, 1], dtype=torch.uint8, device="cuda")
+    F.fdllm_synth_kv_cache_seq(13, F.SYNTH_VCACHE, 3, 24, 2, 64, i32(epochs), only, 1.0, dc, kc)
+    got = _bits(kc)
+    for b in range(3):
+        ref = synth.kv_cache(13, synth.KIND_VCACHE, 3, 24, 2, 64, epochs[b], dtype)[b]
+        assert np.array_equal(got[b], ref) if only[b] else not got[b].any()
