@@ -16,10 +16,11 @@
 //   warp 0     TMA: the query tile once (into the last pipeline stage), then K
 //              and V tiles into a ring of 7 stages (d = 128; 8 at d = 64), less
 //              the one or two stages a split merge receives into
-//   warp 1     TMEM owner, MMA issuer: S_i = Q K_i^T (M=128, N=64 keys, K=d,
-//              A from TMEM) and O_g += P_i V_i (N=d, K=64 keys, P from TMEM, V
-//              read MN-major), each issued as soon as its inputs are ready
-//   warps 2-3  FP8 KV cache only: cache K tiles from E4M3 codes to bf16
+//   warps 1-2  MMA issuers, one per softmax group (warp 1 also owns TMEM):
+//              S_i = Q K_i^T (M=128, N=64 keys, K=d, A from TMEM) and
+//              O_g += P_i V_i (N=d, K=64 keys, P from TMEM, V read MN-major),
+//              each issued as soon as its inputs are ready
+//   warp 3     sends the split merge's rows to their owners
 //   warps 4-7  softmax group 0: the even key tiles; warps 8-11 group 1: the odd
 //              ones.  One thread per query row holds the tile's whole score row:
 //              row max, lazy reference max (it moves only when a row's max
@@ -45,12 +46,13 @@
 //
 // FP8 KV cache (F8KV): cached K and V are E4M3 codes with one power-of-two scale
 // per (sequence, position, KV head) row.  A cache tile is loaded as bytes into
-// the V half of its ring stage; warps 2-3 (one thread per key row) turn the K
-// codes into the bf16 K tile TMA would have written -- code * scale is exact in
-// bf16 -- and release it to the MMA issuer; the softmax group of the tile turns
-// the V codes into the bf16 V tile after the tile's scores are done.  The
-// products and the softmax arithmetic are unchanged.  Fresh K/V tiles are loaded
-// as bf16 directly.
+// the V half of its ring stage.  The softmax group that owns the tile turns its
+// K codes into the bf16 K tile TMA would have written -- code * scale is exact
+// in bf16 -- one of the group's tiles ahead (while it works on the previous
+// one), which releases the tile to the group's MMA issuer, and its V codes into
+// the bf16 V tile right after reading the tile's scores.  The products and the
+// softmax arithmetic are unchanged.  Fresh K/V tiles are loaded as bf16
+// directly.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -64,7 +66,7 @@
 namespace fdllm {
 namespace {
 
-constexpr int kThreads = 384;   // warps 0-3: TMA, MMA, FP8 K conversion (2, 3); 4-11: two softmax groups
+constexpr int kThreads = 384;   // warps 0-3: TMA, two MMA issuers, merge sender; 4-11: two softmax groups
 constexpr int kTile = 128;       // rows per query tile
 constexpr int kKeys = 64;        // keys per key tile
 constexpr int kMaxCluster = 8;   // portable thread-block cluster size
@@ -122,7 +124,6 @@ struct Cfg {
 struct Bars {
   uint64_t qfull, qtmem, kvfull[8], kvempty[8], raw[8], sfull[2], sempty[2], pfull[2], pvdone[2], drain, mrg;
   uint32_t tmem_base;
-  int32_t cvt_stop;   // F8KV: the converters stop (written before, read between their two barriers)
   int32_t abort;
   int32_t issued;     // K/V tiles issued by the producer
   int32_t consumed_g[2];   // per group: key tiles whose arrival its MMA issuer waited for
@@ -130,8 +131,6 @@ struct Bars {
 
 // The two softmax warps of TMEM lane quadrant q (warps 4 + q and 8 + q) synchronise as a pair.
 __device__ __forceinline__ void quadrant_bar(int q) { asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory"); }
-// The two FP8 conversion warps synchronise among themselves.
-__device__ __forceinline__ void convert_bar() { asm volatile("bar.sync 6, 64;" ::: "memory"); }
 // The four warps of softmax group g.
 __device__ __forceinline__ void group_bar(int g) { asm volatile("bar.sync %0, 128;" ::"r"(7 + g) : "memory"); }
 // The softmax warps and warp 3, which sends the split merge's rows once the softmax warps have staged them.
@@ -204,6 +203,46 @@ __device__ __forceinline__ void store_bf16_row(unsigned char *tile, int r, const
     const int j = (cc & 3) * 2;                      // first of the two 16-byte bf16 chunks
     *(uint4 *)(half + ((j ^ (r & 7)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
     *(uint4 *)(half + (((j + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
+  }
+}
+
+// Rotation of the code chunks of half h of row r: a quarter warp (four rows, both halves) then reads its
+// codes and writes its bf16 chunks in eight distinct 16-byte bank groups.
+template <int D>
+__device__ __forceinline__ int half_rot(int r, int h) { return D == 128 ? r + 2 * h : (r >> 1) + h; }
+
+// The D / 2 codes of half h of row r (D / 32 chunks of 16), slot c holding chunk (c + half_rot) mod D / 32.
+template <int D>
+__device__ __forceinline__ void load_code_half(const unsigned char *half, int r, int h, uint4 (&codes)[D / 32]) {
+  constexpr int NC = D / 32;
+  const int rot = half_rot<D>(r, h);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) codes[c] = *(const uint4 *)(half + ((c + rot) & (NC - 1)) * 16);
+}
+
+// Half h of row r of a bf16 K or V tile in the layout the 128-byte-swizzled TMA load writes (64-column
+// halves of kKeys rows x 128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7); d = 128: half h is the
+// whole row of 64-column half h, d = 64: chunks [4 h, 4 h + 4) of the single row): sc x the codes that
+// load_code_half read, or zeros where !valid (not code x 0, which is NaN for a NaN code).
+template <int D>
+__device__ __forceinline__ void store_bf16_half(unsigned char *tile, int r, int h, const uint4 (&codes)[D / 32],
+                                                float sc, bool valid) {
+  constexpr int NC = D / 32;
+  unsigned char *row = tile + (D == 128 ? h * (kKeys * 128) : 0) + r * 128;
+  const int j0 = D == 128 ? 0 : 4 * h;
+  const int rot = half_rot<D>(r, h);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int j = j0 + 2 * ((c + rot) & (NC - 1));
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+    if (valid) {
+      const uint2 x0 = e4m3x4_to_bf16x4(codes[c].x, sc), x1 = e4m3x4_to_bf16x4(codes[c].y, sc);
+      const uint2 x2 = e4m3x4_to_bf16x4(codes[c].z, sc), x3 = e4m3x4_to_bf16x4(codes[c].w, sc);
+      lo = make_uint4(x0.x, x0.y, x1.x, x1.y);
+      hi = make_uint4(x2.x, x2.y, x3.x, x3.y);
+    }
+    *(uint4 *)(row + ((j ^ (r & 7)) * 16)) = lo;
+    *(uint4 *)(row + (((j + 1) ^ (r & 7)) * 16)) = hi;
   }
 }
 
@@ -307,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto seg_rows = [&](int c) { return max(0, min(rpc, pl.nvr - c * rpc)); };
 
   if (threadIdx.x == 0) {
-    br.abort = 0; br.issued = 0; br.consumed_g[0] = 0; br.consumed_g[1] = 0; br.cvt_stop = 0;
+    br.abort = 0; br.issued = 0; br.consumed_g[0] = 0; br.consumed_g[1] = 0;
     tc::mbar_init(&br.qfull, 1);
     tc::mbar_init(&br.qtmem, 4);
     for (int i = 0; i < NS; ++i) {
@@ -321,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&br.pfull[g], 4);
       tc::mbar_init(&br.pvdone[g], 1);
     }
-    tc::mbar_init(&br.drain, F8KV ? 1 : 2);          // one arrival per MMA issuer
+    tc::mbar_init(&br.drain, 2);                     // one arrival per MMA issuer
     tc::mbar_init(&br.mrg, 1);
     tc::fence_barrier_init();
     // the merge barrier expects the other C - 1 CTAs' copies of this one's rows and their pairs
@@ -393,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char *ks = kv_s + st * CF::STAGE;
         if (F8KV && kt.range != 1) {
           // cache tile: K codes then V codes (kKeys rows x D bytes each) into the stage's V half; the
-          // converters write the bf16 tiles and complete kvfull
+          // tile's softmax group writes the bf16 tiles (the K tile completes kvfull)
           tc::mbar_arrive_expect_tx(&br.raw[st], (uint32_t)(2 * kKeys * D));
           // one box: kKeys / KVP keys of each of the KVP heads, head-major
           tc::tma_load_4d(ks + CF::KV_BYTES, mk, &br.raw[st], 0, kt.row0, kvh, b, pol_kv);
@@ -409,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicExch(&br.issued, i + 1);
       }
     }
-  } else if (!F8KV && (warp == 1 || warp == 2)) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
       // ---------------- MMA issuers, one per softmax group ----------------
       // Warp 1 serves group 0 (the even key tiles), warp 2 group 1 (the odd ones).  Each issues its
@@ -493,114 +532,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(&br.drain);                        // both issuers arrive: count 2
       if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
     }
-  } else if (F8KV && warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer (FP8 cache: one thread for both groups) ----------------
-      // S_j and PV_i are issued in whatever order their inputs become ready (a PV first when both
-      // are): S_j needs its K/V tile and the group's score buffer (released when the group has read
-      // S_{j-2}); PV_i needs the group's P_i.  The thread sleeps in mbarrier try_wait (with a short
-      // time hint) on the input it expects next, rather than spinning on the issue slots the softmax
-      // warps of its sub-partition need.
-      const uint32_t id_s = tc::idesc_bf16_f32(128, kKeys, 0);
-      const uint32_t id_o = tc::idesc_bf16_f32(128, D, 1);
-      bool run = tc::mbar_wait_or_abort(&br.qtmem, 0, abort_flag);    // Q is in TMEM
-      if (!run && !*abort_flag) fail(br, a.err, 212);
-      int js = 0, jp = 0;                               // next S, next PV
-      int js_st = 0, jp_st = 0;                         // their ring stages
-      uint32_t js_ph = 0;                               // phase parity of js's stage
-      uint64_t t0 = tc::globaltimer();
-      auto s_ready = [&]() {
-        return tc::mbar_test_wait(&br.kvfull[js_st], js_ph) &&
-               tc::mbar_test_wait(&br.sempty[js & 1], ((uint32_t)(js >> 1) & 1u) ^ 1u);
-      };
-      for (uint32_t spin = 0; run && jp < nt; ++spin) {
-        if (jp < js && tc::mbar_try_wait_hint(&br.pfull[jp & 1], (uint32_t)(jp >> 1) & 1u, js < nt ? 200u : 2000u)) {
-          const int st = jp_st, gg = jp & 1;
-          tc::fence_after_sync();
-          const uint32_t va = tc::smem_u32(kv_s + st * CF::STAGE + CF::KV_BYTES);
-#pragma unroll
-          for (int ks = 0; ks < kKeys / 16; ++ks)
-            tc::mma_bf16_ts(tmem + CF::O_COL + (uint32_t)(gg * D), tmem + CF::P_COL + (uint32_t)(gg * 32 + ks * 8),
-                            tc::sw128_mn_desc(va + (uint32_t)(ks * 2048), CF::KVHALF), id_o, (jp >= 2) || ks != 0);
-          tc::mma_commit(&br.pvdone[gg]);
-          tc::mma_commit(&br.kvempty[st]);
-          ++jp;
-          if (++jp_st == ns) jp_st = 0;
-          t0 = tc::globaltimer();
-          continue;
-        }
-        if (js < nt && (s_ready() || (jp >= js && tc::mbar_try_wait_hint(&br.kvfull[js_st], js_ph, 2000u) &&
-                                       s_ready()))) {
-          const int st = js_st, gg = js & 1;
-          tc::fence_after_sync();
-          const uint32_t ka = tc::smem_u32(kv_s + st * CF::STAGE);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            tc::mma_bf16_ts(tmem + CF::S_COL + (uint32_t)(gg * kKeys), tmem + CF::Q_COL + (uint32_t)(ks * 8),
-                            tc::sw128_desc(ka + (ks / 4) * CF::KVHALF + (uint32_t)((ks % 4) * 32)), id_s, ks != 0);
-          tc::mma_commit(&br.sfull[gg]);
-          atomicExch(&br.consumed_g[js & 1], (js >> 1) + 1);
-          ++js;
-          if (++js_st == ns) { js_st = 0; js_ph ^= 1u; }
-          t0 = tc::globaltimer();
-          continue;
-        }
-        if ((spin & 15u) == 0) {
-          if (*abort_flag) break;
-          if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
-            fail(br, a.err, jp < js ? 215 : 213);
-            break;
-          }
-        }
-      }
-      tc::mma_commit(&br.drain);
-      if (!tc::mbar_wait(&br.drain, 0)) record_device_error(a.err, 217);
-    }
-  } else if (F8KV && (warp == 2 || warp == 3)) {
-    // FP8 cache K tiles to bf16: thread r converts key row r (KV head kvh + r / tk, key r % tk)
-    const int r = threadIdx.x - 64;
-    // Every converter thread takes each exit decision from cvt_stop, which is only written before the
-    // first barrier of an iteration and read between its two barriers: no thread can leave while
-    // another waits at a barrier.
-    uint32_t rawpar = 0;                               // bit st: parity of raw[st]'s next phase
-    // this row's K scale, loaded one cache tile ahead so that its latency overlaps a conversion
-    auto next_cache_tile = [&](int j) {
-      while (j < nt && key_tile(pl, a.nq, a.n, k0 + j).range == 1) ++j;
-      return j;
-    };
-    auto load_scale = [&](int j) -> float {
-      if (j >= nt) return 0.f;
-      const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + j);
-      return (r % pl.tk) < kt.nvalid ? cache_scale(a, pl, kt, b, kvh, r, a.k_scale) : 0.f;
-    };
-    int inext = next_cache_tile(0);
-    float ksn = load_scale(inext);
-    for (int i = inext; i < nt; i = inext) {
-      const float ksc = ksn;
-      const bool valid = (r % pl.tk) < key_tile(pl, a.nq, a.n, k0 + i).nvalid;
-      inext = next_cache_tile(i + 1);
-      ksn = load_scale(inext);
-      const int st = i % ns;
-      if (!tc::mbar_wait_or_abort(&br.raw[st], (rawpar >> st) & 1u, abort_flag)) {
-        if (!*abort_flag) fail(br, a.err, 220);
-        br.cvt_stop = 1;
-      }
-      rawpar ^= 1u << st;
-      if (r == 0 && br.abort) br.cvt_stop = 1;
-      convert_bar();
-      if (br.cvt_stop) break;
-      unsigned char *ks = kv_s + st * CF::STAGE;
-      uint4 codes[D / 16];
-      load_code_row<D>(ks + CF::KV_BYTES + r * D, r, codes);
-      if (!valid) {                                    // a row outside the sequence's key range: zeros
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) codes[c] = make_uint4(0u, 0u, 0u, 0u);
-      }
-      store_bf16_row<D>(ks, r, codes, ksc);            // K: codes in the V half, bf16 into the K half
-      tc::fence_proxy_async_smem();
-      convert_bar();
-      if (r == 0) tc::mbar_arrive(&br.kvfull[st]);     // V is converted by the tile's softmax group
-    }
   } else if (warp >= 4) {
     // Every softmax warp runs every tile of its group and meets every named barrier the same number of
     // times, whatever its waits return: a wait that gives up only marks this thread's result invalid
@@ -646,27 +577,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_st_wait();
     }
     const float sl2 = a.scale_log2;
-    // F8KV: phase parity of raw[st] for tile i (the cache tiles loaded into its stage before it)
-    // F8KV: the raw barriers' phase parities (bit st: cache tiles loaded into stage st so far), advanced
-    // over every tile before this group's next one; and this thread's V scale, loaded one tile ahead
+    // F8KV: the group converts its cache tiles' K rows one of its tiles ahead (tile i + 2 while it works on
+    // tile i, its first before the loop) and their V rows at the tile itself; thread gt handles half hh of
+    // key row kr of both.  rawpar: the raw barriers' phase parities (bit st: cache tiles loaded into stage
+    // st so far), advanced over every tile before the one whose codes are awaited.
+    const int kr = gt >> 1, hh = gt & 1;
     uint32_t rawpar = 0;
     int seen = 0, seen_st = 0;
-    auto v_scale_of = [&](int i) -> float {
-      if (!F8KV || i >= nt) return 0.f;
-      const KeyTile t = key_tile(pl, a.nq, a.n, k0 + i);
-      if (t.range == 1 || ((gt >> 1) % pl.tk) >= t.nvalid) return 0.f;
-      return cache_scale(a, pl, t, b, kvh, gt >> 1, a.v_scale);
+    auto scale_of = [&](int j, const float *sc) -> float {   // row kr's scale in tile j (0: none)
+      if (!F8KV || j >= nt) return 0.f;
+      const KeyTile t = key_tile(pl, a.nq, a.n, k0 + j);
+      if (t.range == 1 || (kr % pl.tk) >= t.nvalid) return 0.f;
+      return cache_scale(a, pl, t, b, kvh, kr, sc);
     };
-    float vsc_next = v_scale_of(g);
+    auto convert_k = [&](int j, int stj, float ksc) {        // cache tile j's K rows; completes kvfull
+      for (; seen < j; ++seen, seen_st = seen_st + 1 == ns ? 0 : seen_st + 1)
+        if (key_tile(pl, a.nq, a.n, k0 + seen).range != 1) rawpar ^= 1u << seen_st;
+      const bool got = tc::mbar_wait_or_abort(&br.raw[stj], (rawpar >> stj) & 1u, abort_flag);
+      if (!got) {
+        if (!*abort_flag) fail(br, a.err, 220);
+        ok = false;
+      }
+      unsigned char *sj = kv_s + stj * CF::STAGE;
+      uint4 kc[D / 32];
+      load_code_half<D>(sj + CF::KV_BYTES + kr * D + hh * (D / 2), kr, hh, kc);
+      store_bf16_half<D>(sj, kr, hh, kc, ksc, (kr % pl.tk) < key_tile(pl, a.nq, a.n, k0 + j).nvalid);
+      tc::fence_proxy_async_smem();
+      group_bar(g);                                    // every K row of the tile is written
+      if (gt == 0 && got) tc::mbar_arrive(&br.kvfull[stj]);
+    };
+    float ksc_n = scale_of(g + 2, a.k_scale);          // K scale of the tile converted in the next iteration
+    float vsc_n = scale_of(g, a.v_scale);              // V scale of the next iteration's tile
+    if (F8KV && g < nt && key_tile(pl, a.nq, a.n, k0 + g).range != 1) convert_k(g, g, scale_of(g, a.k_scale));
     int u = 0;                                         // this group's tile count
     int st = g;                                        // tile i's ring stage
     for (int i = g; i < nt; i += 2, ++u, st = st + 2 >= ns ? st + 2 - ns : st + 2) {
       const KeyTile kt = key_tile(pl, a.nq, a.n, k0 + i);
-      const float vsc_cur = vsc_next;
-      if constexpr (F8KV) {
-        vsc_next = v_scale_of(i + 2);                  // used one tile later: the load has time to land
-        for (; seen < i; ++seen, seen_st = seen_st + 1 == ns ? 0 : seen_st + 1)
-          if (key_tile(pl, a.nq, a.n, k0 + seen).range != 1) rawpar ^= 1u << seen_st;
+      const float ksc2 = ksc_n, vsc = vsc_n;
+      if constexpr (F8KV) {                            // loaded one iteration ahead of their use
+        ksc_n = scale_of(i + 4, a.k_scale);
+        vsc_n = scale_of(i + 2, a.v_scale);
       }
       const int nv = kt.nvalid;
       if (!tc::mbar_wait_or_abort(&br.sfull[g], (uint32_t)u & 1u, abort_flag)) {
@@ -674,50 +624,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       }
       tc::fence_after_sync();
-      // The tile's V (its K codes were consumed before S_i): FP8 codes into bf16 (cache tiles), or zeros
-      // over rows outside the sequence's key range (per-sequence blocks read window rows at the edge of
-      // the prefix; they must not reach the product even as 0 * inf).  Thread gt handles half (vh) of
-      // key row vr.
-      const bool cvt = F8KV && kt.range != 1;
-      const bool zero_rows = !cvt && a.blocks != nullptr && kt.range == 0 && nv < pl.tk;
-      if (cvt || zero_rows) {
-        const int vr = gt >> 1, vh = gt & 1;
-        const bool rvalid = (vr % pl.tk) < nv;
-        unsigned char *vt = kv_s + st * CF::STAGE + CF::KV_BYTES;
-        constexpr int HB = D / 2;                      // bf16 values (and codes) per half row
-        uint32_t w[HB / 2];
-        if constexpr (F8KV) {
-          if (cvt) {
-            // the codes' arrival, for this thread: complete long ago (the converters waited for it, and
-            // the tile's scores are done), and raw[st] cannot move on before this tile's P is released
-            if (!tc::mbar_wait_or_abort(&br.raw[st], (rawpar >> st) & 1u, abort_flag)) ok = false;
-            const float vsc = vsc_cur;                 // 0 for a row outside the sequence's key range
-            uint4 cq[HB / 16];
+      // bf16 cache, per-sequence blocks: zeros over the tile's V rows outside the sequence's key range
+      // (window rows at the edge of the prefix, which must not reach the product even as 0 * inf)
+      if (!F8KV && a.blocks != nullptr && kt.range == 0 && nv < pl.tk) {
+        if ((kr % pl.tk) >= nv) {
+          unsigned char *row = kv_s + st * CF::STAGE + CF::KV_BYTES + (D == 128 ? hh * CF::KVHALF : 0) + kr * 128;
 #pragma unroll
-            for (int c = 0; c < HB / 16; ++c)
-              cq[c] = *(const uint4 *)(vt + kKeys * D + vr * D + vh * HB + c * 16);
-            group_bar(g);                              // every V code of the tile has been read
-#pragma unroll
-            for (int c = 0; c < HB / 16; ++c) {
-              const uint2 x0 = e4m3x4_to_bf16x4(cq[c].x, vsc), x1 = e4m3x4_to_bf16x4(cq[c].y, vsc);
-              const uint2 x2 = e4m3x4_to_bf16x4(cq[c].z, vsc), x3 = e4m3x4_to_bf16x4(cq[c].w, vsc);
-              w[8 * c] = x0.x; w[8 * c + 1] = x0.y; w[8 * c + 2] = x1.x; w[8 * c + 3] = x1.y;
-              w[8 * c + 4] = x2.x; w[8 * c + 5] = x2.y; w[8 * c + 6] = x3.x; w[8 * c + 7] = x3.y;
-            }
-          }
-        }
-        if (!rvalid || !cvt) {
-#pragma unroll
-          for (int e = 0; e < HB / 2; ++e) w[e] = 0u;
-        }
-        if (cvt || !rvalid) {
-          // half vh of row vr in the 128-byte swizzle layout: d = 128: the whole 128-byte row of d-half
-          // vh; d = 64: chunks [4 vh, 4 vh + 4) of the single 128-byte row
-          unsigned char *row = vt + (D == 128 ? vh * CF::KVHALF : 0) + vr * 128;
-#pragma unroll
-          for (int c = 0; c < HB / 8; ++c) {
-            const int j = (D == 128 ? 0 : 4 * vh) + c;
-            *(uint4 *)(row + ((j ^ (vr & 7)) * 16)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          for (int c = 0; c < D / 16; ++c) {
+            const int j = (D == 128 ? 0 : 4 * hh) + c;
+            *(uint4 *)(row + ((j ^ (kr & 7)) * 16)) = make_uint4(0u, 0u, 0u, 0u);
           }
         }
         tc::fence_proxy_async_smem();
@@ -740,6 +655,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&br.sempty[g]);  // S_g may be overwritten by this group's next S
+      if constexpr (F8KV) {
+        // the K rows of this group's next tile (its score product may then start), and this tile's V rows:
+        // their codes landed with its K codes (waited for then); they are read before the barrier, as the
+        // bf16 V tile is written over them
+        const int st2 = st + 2 >= ns ? st + 2 - ns : st + 2;
+        if (i + 2 < nt && key_tile(pl, a.nq, a.n, k0 + i + 2).range != 1) convert_k(i + 2, st2, ksc2);
+        if (kt.range != 1) {
+          unsigned char *vt = kv_s + st * CF::STAGE + CF::KV_BYTES;
+          uint4 vc[D / 32];
+          load_code_half<D>(vt + kKeys * D + kr * D + hh * (D / 2), kr, hh, vc);
+          group_bar(g);                                // every V code of the tile has been read
+          store_bf16_half<D>(vt, kr, hh, vc, vsc, (kr % pl.tk) < nv);
+          tc::fence_proxy_async_smem();
+        }
+      }
       // row max over the valid keys, lazy reference max
       float mx[TK / 2];
 #pragma unroll
@@ -998,8 +928,8 @@ bool map4(CUtensorMap *m, const void *base, int d, int heads, int rows, int batc
 // K or V [batch, rows, heads, d] viewed as (d, rows, heads, batch) -- rows and heads swapped -- with box
 // {64, box_rows, kvp, 1}: one load brings box_rows keys of kvp consecutive heads, head-major, which is
 // the tile layout the kernel uses (row p * box_rows + key of head kvh + p).  bf16 with the 128-byte
-// swizzle, or E4M3 codes (codes = true: whole d-byte rows, no swizzle: the converters read them row by
-// row).  batch_stride is in elements.
+// swizzle, or E4M3 codes (codes = true: whole d-byte rows, no swizzle: the softmax groups read them by
+// half rows).  batch_stride is in elements.
 bool map4_kv(CUtensorMap *m, const void *base, int d, int heads, int rows, int batch, int64_t batch_stride,
              int box_rows, int kvp, bool codes) {
   auto fn = encode_fn();
