@@ -187,25 +187,6 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w, float sc) {
   return make_uint2(o[0], o[1]);
 }
 
-// Row r of a bf16 K or V tile in the layout the 128-byte-swizzled TMA load writes: 64-column halves
-// of kKeys rows x 128 bytes, 16-byte chunk j of row r at chunk j ^ (r & 7).  `codes` holds the row's
-// D / 16 chunks of 16 codes; chunk slot c holds code chunk (c + r) mod (D / 16) (the rotation
-// spreads a warp's shared-memory accesses over the banks).
-template <int D>
-__device__ __forceinline__ void store_bf16_row(unsigned char *tile, int r, const uint4 (&codes)[D / 16], float sc) {
-  constexpr int NC = D / 16;
-#pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const int cc = (c + r) & (NC - 1);
-    const uint2 a = e4m3x4_to_bf16x4(codes[c].x, sc), b = e4m3x4_to_bf16x4(codes[c].y, sc);
-    const uint2 d = e4m3x4_to_bf16x4(codes[c].z, sc), e = e4m3x4_to_bf16x4(codes[c].w, sc);
-    unsigned char *half = tile + (cc >> 2) * (kKeys * 128) + r * 128;
-    const int j = (cc & 3) * 2;                      // first of the two 16-byte bf16 chunks
-    *(uint4 *)(half + ((j ^ (r & 7)) * 16)) = make_uint4(a.x, a.y, b.x, b.y);
-    *(uint4 *)(half + (((j + 1) ^ (r & 7)) * 16)) = make_uint4(d.x, d.y, e.x, e.y);
-  }
-}
-
 // Rotation of the code chunks of half h of row r: a quarter warp (four rows, both halves) then reads its
 // codes and writes its bf16 chunks in eight distinct 16-byte bank groups.
 template <int D>
@@ -254,13 +235,6 @@ __device__ __forceinline__ float cache_scale(const Args &a, const Plan &pl, cons
   const int hp = r / pl.tk;
   const int pos = (t.range == 2 && !pl.abs_suffix ? pl.f1 : 0) + t.row0 + (r - hp * pl.tk);
   return pos < a.n ? __ldg(scale + ((int64_t)b * a.n + pos) * a.hkv + kvh + hp) : 0.f;
-}
-
-template <int D>
-__device__ __forceinline__ void load_code_row(const unsigned char *row, int r, uint4 (&codes)[D / 16]) {
-  constexpr int NC = D / 16;
-#pragma unroll
-  for (int c = 0; c < NC; ++c) codes[c] = *(const uint4 *)(row + ((c + r) & (NC - 1)) * 16);
 }
 
 __device__ __forceinline__ void fail(Bars &br, int32_t *err, int site) {
