@@ -210,3 +210,61 @@ def test_per_sequence_window_splice_bit_exact():
             wk, wks, wv = want_kq[i:i + 1], want_ks[i:i + 1], want_kq[i:i + 1]
         assert np.array_equal(got_kq[i:i + 1], wk) and np.array_equal(got_ks[i:i + 1], wks)
         assert np.array_equal(got_vq[i:i + 1], wv)
+
+
+def _random_fp8_cache(rng, b, n, hkv, d):
+    """Seeded E4M3 codes drawn directly (random sign, exponent field 4..10, any mantissa: magnitudes
+    1/8..15) with power-of-two row scales 2^-3..2^0: a cache of a benchmark shape without running a
+    quantiser over it."""
+    raw = np.frombuffer(rng.bytes(b * n * hkv * d), dtype=np.uint8).reshape(b, n, hkv, d)
+    codes = (raw & 0x87) | ((((raw >> 3) & 0xF) % 7 + 4) << 3)   # sign and mantissa kept, exponent 4..10
+    scales = np.exp2(rng.integers(-3, 1, size=(b, n, hkv))).astype(np.float32)
+    return codes, scales
+
+
+def _bf16_normals(rng, shape):
+    return torch.from_numpy(rng.standard_normal(shape, dtype=np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("shape", [dict(batch=16, prompt_len=768, gen_length=256, hq=32, hkv=32),
+                                   dict(batch=8, prompt_len=512, gen_length=1024, hq=28, hkv=4)],
+                         ids=["llada-dual-batch16", "dream-gqa-batch8"])
+def test_benchmark_shapes_sampled_sequences(shape):
+    """The benchmark's FP8-cache launch configurations: LLaDA DualCache at batch 16 (four KV heads per
+    tile, 64 key tiles per CTA, so the ring wraps many times over tiles of both softmax groups) and Dream
+    GQA at batch 8.  Every query row of two sampled sequences against the oracle's attention over the
+    dequantised cache."""
+    b, prompt_len, gen_length, hq, hkv = (shape[k] for k in ("batch", "prompt_len", "gen_length", "hq", "hkv"))
+    d, block_size, block_idx = 128, 32, 0
+    n = prompt_len + gen_length
+    rng = np.random.default_rng(11 + b)
+    kq, ks = _random_fp8_cache(rng, b, n, hkv, d)
+    vq, vs = _random_fp8_cache(rng, b, n, hkv, d)
+    q = _bf16_normals(rng, (b, block_size, hq, d))
+    kf = _bf16_normals(rng, (b, block_size, hkv, d))
+    vf = _bf16_normals(rng, (b, block_size, hkv, d))
+    desc = F.attn_desc(batch=b, prompt_len=prompt_len, gen_length=gen_length, block_size=block_size,
+                       block_idx=block_idx, n_q_heads=hq, n_kv_heads=hkv, head_dim=d, use_cache=1, dual_cache=1,
+                       dtype=F.BF16, out_f32=1)
+    assert F.fdllm_attn_query_count(desc) == block_size
+    out = torch.zeros(b, block_size, hq, d, dtype=torch.float32, device="cuda")
+    lse = torch.zeros(b, block_size, hq, dtype=torch.float32, device="cuda")
+    wsb = F.fdllm_attn_workspace_size(desc)
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    t = lambda x: torch.from_numpy(x).cuda()
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    F.fdllm_block_attn_fp8kv(desc, None, q.cuda(), t(kq), t(ks), t(vq), t(vs), kf.cuda(), vf.cuda(), out, lse, ws,
+                             ws_bytes=wsb)
+    torch.cuda.synchronize()
+    assert F.fdllm_last_device_error() == (F.OK, 0)
+    o_gpu = out.cpu().numpy().astype(np.float64)
+    l_gpu = lse.cpu().numpy()
+    s, e = O.block_window(prompt_len, block_size, block_idx)
+    f = lambda x: x.float().numpy().astype(np.float64)
+    for bi in sorted(rng.choice(b, size=2, replace=False).tolist()):
+        sl = slice(bi, bi + 1)
+        o_ref, lse_ref = O.block_attention(f(q[sl]), O.dequantize_kv_rows(kq[sl], ks[sl]),
+                                           O.dequantize_kv_rows(vq[sl], vs[sl]), f(kf[sl]), f(vf[sl]), mode="dual",
+                                           s=s, e=e, n_q_heads=hq, n_kv_heads=hkv)
+        assert_attention_close(o_gpu[sl], o_ref)
+        assert np.abs(l_gpu[sl] - lse_ref).max() < 2e-3, bi
