@@ -3,8 +3,8 @@
 // logits = h W^T for the block rows (b * B <= 512), never stored.  The grid is
 // one CTA per SM, in clusters of CS = 1, 2 or 4 CTAs (CS 128-row tiles cover
 // the block rows): CTA c of a cluster owns block rows [128 c, 128 c + 128),
-// and each cluster owns a contiguous range of the vocabulary in units of 64
-// rows of W, streamed through shared memory once: every CTA of the cluster
+// and cluster k of K owns the units k, k + K, k + 2K, ... of the vocabulary (a
+// unit: 64 rows of W), streamed through shared memory once: every CTA of the cluster
 // loads 1/CS of each W tile and multicasts it to all of them, so W leaves HBM
 // once per cluster and each CTA reads only its own hidden rows.  Per CTA (256
 // threads):
@@ -19,7 +19,7 @@
 //           buffered so the epilogue of tile t overlaps the MMAs of tile t+1
 //   warps 4-7 epilogue: tcgen05.ld of the accumulator (one thread per block
 //           row), folded into the row's VocabStat in increasing vocabulary order
-// At the end every masked row writes its VocabStat for its cluster's range to
+// At the end every masked row writes its VocabStat for its cluster's units to
 // the partials [b * B, clusters] and arrives on a 64-bit ticket in the workspace
 // (high half: this call's epoch, low half: count; a ticket left by another call
 // or uninitialised memory is re-armed first, so the workspace needs no
@@ -170,7 +170,7 @@ __device__ __forceinline__ uint32_t share_bytes(int r, int nu) {
 // commits are settled the same way on the empty barriers: arrivals of CTAs that never committed a
 // stage are made by this CTA itself, and the phase then completes when the real ones have landed.
 template <int CS>
-__device__ void settle_after_abort(Shared &sh, int c, int u0, int u1, int kchunks, uint32_t a_bytes, int32_t *err) {
+__device__ void settle_after_abort(Shared &sh, int c, int nu_k, int kchunks, uint32_t a_bytes, int32_t *err) {
   using C = Cfg;
   int iss[CS], con[CS];
   int hi_iss = 0, hi_con = 0;
@@ -190,7 +190,7 @@ __device__ void settle_after_abort(Shared &sh, int c, int u0, int u1, int kchunk
   for (int it = con[c]; it < hi_iss; ++it) {
     const int st = it % C::STAGES;
     const int t = it / kchunks;
-    const int nu = min(C::UNITS, u1 - (u0 + t * C::UNITS));
+    const int nu = min(C::UNITS, nu_k - t * C::UNITS);
     uint32_t sent = iss[c] > it ? a_bytes : 0u;             // this CTA's own hidden tile
 #pragma unroll
     for (int r = 0; r < CS; ++r)
@@ -238,10 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t a_bytes = (uint32_t)(hidden_box_rows(rows, CS) * kRowBytes);   // hidden tile per stage
   constexpr uint16_t kAll = (uint16_t)((1u << CS) - 1u);   // every CTA of the cluster
 
-  // vocabulary units [u0, u1) of this cluster
+  // vocabulary units of this cluster: k, k + ncl, k + 2 ncl, ... (position p of its list is unit
+  // k + p ncl), so that at each step of their loops all clusters stream neighbouring rows of W: the
+  // grid sweeps W in order
   const int units = (V + kUnit - 1) / kUnit;
-  const int u0 = (int)((int64_t)units * k / ncl), u1 = (int)((int64_t)units * (k + 1) / ncl);
-  const int ntiles = (u1 - u0 + C::UNITS - 1) / C::UNITS;
+  const int nu_k = k < units ? (units - 1 - k) / ncl + 1 : 0;
+  auto unit_of = [&](int pos) { return k + pos * ncl; };
+  const int ntiles = (nu_k + C::UNITS - 1) / C::UNITS;
   const int kchunks = H / KC;
 
   if (threadIdx.x == 0) {
@@ -270,13 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     e = __shfl_sync(0xffffffffu, e, 0);
     if (e >= 1 && e <= kPrefetchers) {
       // one W box (64 rows x 128 bytes) per prefetch: the boxes of the first kPrefetchBytes of each
-      // row of the first tile of CTA ranges e - 1, e - 1 + kPrefetchers, ...
+      // row of the first tile of CTAs e - 1, e - 1 + kPrefetchers, ...
       const int nchunk = min(kPrefetchBytes / kRowBytes, kchunks);
       for (int j = e - 1; j < G; j += kPrefetchers) {
-        const int ju0 = (int)((int64_t)units * j / ncl), ju1 = (int)((int64_t)units * (j + 1) / ncl);
-        const int nu = min(C::UNITS, ju1 - ju0);
+        const int nu = j < units ? min(C::UNITS, (units - 1 - j) / ncl + 1) : 0;
         for (int q = lane; q < nu * nchunk; q += 32)
-          tc::prefetch_l2_tile_2d(&map_w, (q / nu) * kMapX, (ju0 + q % nu) * kUnit);
+          tc::prefetch_l2_tile_2d(&map_w, (q / nu) * kMapX, (j + (q % nu) * ncl) * kUnit);
       }
     }
   }
@@ -320,8 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         bool go = true;
         for (int t = 0; t < ntiles && go; ++t) {
-          const int tu0 = u0 + t * C::UNITS;
-          const int nu = min(C::UNITS, u1 - tu0);
+          const int nu = min(C::UNITS, nu_k - t * C::UNITS);
           const uint32_t bytes = a_bytes + (uint32_t)(nu * kUnit * kRowBytes);
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int st = it % C::STAGES;
@@ -337,11 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_load_2d(a, &map_h, &sh.full[st], kc * kMapX, c * kABox, pol_h);
             for (int u = c; u < nu; u += CS) {
               if (CS == 1)
-                tc::tma_load_2d(w + u * kUnit * kRowBytes, &map_w, &sh.full[st], kc * kMapX, (tu0 + u) * kUnit,
-                                pol_w);
+                tc::tma_load_2d(w + u * kUnit * kRowBytes, &map_w, &sh.full[st], kc * kMapX,
+                                unit_of(t * C::UNITS + u) * kUnit, pol_w);
               else
                 tc::tma_load_2d_multicast(w + u * kUnit * kRowBytes, &map_w, &sh.full[st], kc * kMapX,
-                                          (tu0 + u) * kUnit, kAll, pol_w);
+                                          unit_of(t * C::UNITS + u) * kUnit, kAll, pol_w);
             }
             atomicExch(&sh.issued, it + 1);
           }
@@ -362,8 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         int it = 0;
         for (int t = 0; t < ntiles && !*abort_flag; ++t) {
-          const int tu0 = u0 + t * C::UNITS;
-          const int nu = min(C::UNITS, u1 - tu0);
+          const int nu = min(C::UNITS, nu_k - t * C::UNITS);
           const uint32_t idesc =
               F8 ? tc::idesc_e4m3_f32(128, (uint32_t)(nu * kUnit)) : tc::idesc_bf16_f32(128, (uint32_t)(nu * kUnit));
           const int j = t & 1;
@@ -413,9 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float hs = F8 && row < rows ? h_scale[row] : 1.f;   // this row's scale
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
-        const int tu0 = u0 + t * C::UNITS;
-        const int ncol = min(C::UNITS, u1 - tu0) * kUnit;
-        const int v0 = tu0 * kUnit;
+        const int ncol = min(C::UNITS, nu_k - t * C::UNITS) * kUnit;
         const int j = t & 1;
         if (!tc::mbar_wait_or_abort(&sh.accf[j], (uint32_t)(t >> 1) & 1u, abort_flag)) {
           if (lane == 0 && !*abort_flag) set_abort<CS>(sh, err, 105, shape_ok);
@@ -428,19 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // lane computes; rows without a masked position are simply not stored)
           const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * C::NV);
           for (int c0 = 0; c0 < ncol; c0 += 32) {
+            const int vb = unit_of(t * C::UNITS + c0 / kUnit) * kUnit + c0 % kUnit;   // vocabulary id of column c0
             uint32_t r[32];
             tc::tmem_ld_32x32b_x32(base + (uint32_t)c0, r);
             // F8: lane e holds the scale of column v0 + c0 + e (both scales are powers of two, so the
             // scaled logit is exact)
-            const float wsl = F8 && v0 + c0 + lane < V ? __ldg(w_scale + v0 + c0 + lane) : 0.f;
+            const float wsl = F8 && vb + lane < V ? __ldg(w_scale + vb + lane) : 0.f;
             tc::tmem_ld_wait();
             float x[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const float a = F8 ? __uint_as_float(r[e]) * hs * __shfl_sync(0xffffffffu, wsl, e) : __uint_as_float(r[e]);
-              x[e] = v0 + c0 + e < V ? a : kNegInf;
+              x[e] = vb + e < V ? a : kNegInf;
             }
-            st = vs_merge(st, vs_chunk32(x, v0 + c0));
+            st = vs_merge(st, vs_chunk32(x, vb));
           }
         }
         tc::fence_before_sync();
@@ -457,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barrier every CTA of the cluster has stopped too, and an abort anywhere is visible everywhere, so
   // either no CTA or every CTA settles.
   if (CS > 1 && shape_ok) tc::cluster_sync();
-  if (*abort_flag && run && threadIdx.x == 0) settle_after_abort<CS>(sh, c, u0, u1, kchunks, a_bytes, err);
+  if (*abort_flag && run && threadIdx.x == 0) settle_after_abort<CS>(sh, c, nu_k, kchunks, a_bytes, err);
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
   if (CS > 1 && shape_ok) tc::cluster_sync();          // no CTA leaves while a peer may still address it
