@@ -73,7 +73,7 @@ __host__ __device__ __forceinline__ int hidden_box_rows(int rows, int cs) {
 }
 constexpr int kMaxSelectors = 8; // CTAs that run the merge + select at the end
 constexpr int kPrefetchers = 24; // first CTAs to start that warm L2 with the head of every CTA's W range
-constexpr int kPrefetchBytes = 1536;  // bytes of each W row of a first tile warmed in L2
+constexpr int kPrefetchBytes = 768;   // bytes of each W row of a first tile warmed in L2
 
 struct Cfg {
   static constexpr int NV = 256;                            // vocabulary rows per tile
