@@ -255,6 +255,7 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   p.kappa_tau = tau >= 1.0 ? -INFINITY : (tau <= 0.0 ? INFINITY : (float)log((1.0 - tau) / tau));
   p.in_bf16 = d->dtype == FDLLM_BF16;
   p.fp8w = 0;
+  p.quant_hidden = 0;
   p.w_scale = nullptr;
   p.h_scale = nullptr;
   p.hq = nullptr;
@@ -297,9 +298,12 @@ cudaError_t run_select(const SelectProblem &p, const SelectLayout &L, void *ws, 
     SelectProblem q = p;
     q.hq = (char *)ws + L.hq_off;
     q.h_scale = (const float *)((char *)ws + L.hs_off);
-    cudaError_t e = launch_quantize_fp8(p.hidden, true, (int64_t)p.batch * p.B, p.H, (uint8_t *)q.hq,
-                                        (float *)q.h_scale, st);
-    if (e != cudaSuccess) return e;
+    q.quant_hidden = lmhead_tc_quantises_hidden(p) ? 1 : 0;   // else the row quantiser runs first
+    if (!q.quant_hidden) {
+      cudaError_t e = launch_quantize_fp8(p.hidden, true, (int64_t)p.batch * p.B, p.H, (uint8_t *)q.hq,
+                                          (float *)q.h_scale, st);
+      if (e != cudaSuccess) return e;
+    }
     return launch_lmhead_tc(q, part, (unsigned long long *)ws, L.splits, st);
   }
   if (L.tc) return launch_lmhead_tc(p, part, (unsigned long long *)ws, L.splits, st);

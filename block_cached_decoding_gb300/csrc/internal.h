@@ -46,8 +46,9 @@ struct SelectProblem {
   int in_bf16;
   const void *hidden, *w;
   // FP8 weight cache (fp8w = 1): w holds E4M3 codes [V, H] with w_scale [V]; the hidden rows are
-  // quantised per row into hq [b * B, H] (E4M3) with h_scale [b * B] before the LM head
-  int fp8w;
+  // quantised per row into hq [b * B, H] (E4M3) with h_scale [b * B] before the LM head, or, with
+  // quant_hidden, by the LM-head kernel itself (both in the workspace)
+  int fp8w, quant_hidden;
   const float *w_scale, *h_scale;
   const void *hq;
   int32_t *tokens;
@@ -97,6 +98,7 @@ bool lmhead_tc_supported(const SelectProblem &p);
 // current device
 bool lmhead_tc_clustered(const SelectProblem &p);
 int lmhead_tc_grid(const SelectProblem &p);
+bool lmhead_tc_quantises_hidden(const SelectProblem &p);
 cudaError_t launch_lmhead_tc(const SelectProblem &p, VocabStat *part, unsigned long long *ticket, int splits,
                              cudaStream_t st);
 

@@ -46,6 +46,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "fp8_rule.cuh"
 #include "select_impl.cuh"
 #include "tc.cuh"
 
@@ -221,7 +222,7 @@ template <int CS, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                      const SelectProblem sp, VocabStat *__restrict__ part, unsigned long long *ticket,
-                     uint32_t epoch, const float *__restrict__ h_scale, const float *__restrict__ w_scale) {
+                     uint32_t epoch, const float *h_scale, const float *__restrict__ w_scale) {
   constexpr int KC = kChunk<F8>;                           // K elements per stage
   const int32_t *__restrict__ tokens = sp.tokens;
   const int batch = sp.batch, seq_len = sp.seq_len, B = sp.B, mask_id = sp.mask_id, H = sp.H, V = sp.V;
@@ -286,6 +287,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // stream, which may produce the tokens, hidden rows or W (or still read the workspace).
   tc::pdl_wait_primary();
   tc::pdl_launch_dependents();
+  if constexpr (F8) {
+    // quant_hidden: the block's hidden rows into E4M3 by the row quantiser's rule, row g by CTA g (the
+    // lowest CTA indices, which wait for no one), each then arriving on the quantisation ticket; every
+    // CTA waits for all of them before it reads a quantised row or scale (producer, epilogue)
+    if (sp.quant_hidden && g < rows) {
+      const __nv_bfloat16 *hrow = (const __nv_bfloat16 *)sp.hidden + (int64_t)g * H;
+      uint8_t *qrow = (uint8_t *)sp.hq + (int64_t)g * H;
+      const bool vec = H % 16 == 0 && ((uintptr_t)sp.hidden & 15) == 0 && ((uintptr_t)sp.hq & 15) == 0;
+      fp8rule::quantize_row<kThreads>(hrow, H, qrow, const_cast<float *>(h_scale) + g, vec, (float *)tiles);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        if (arrive_ticket(ticket + 3, epoch) == 0) record_device_error(err, 114);
+      }
+    }
+  }
   __syncthreads();
   // masked block rows (same on every CTA)
   for (int r = threadIdx.x; r < CS * kABox; r += kThreads) {
@@ -321,6 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_h = tc::policy_evict_last();
         int it = 0;
         bool go = true;
+        if (F8 && sp.quant_hidden) {
+          // every hidden row quantised (its generic writes then made visible to this thread's TMA)
+          if (!wait_ticket(ticket + 3, epoch, rows)) {
+            set_abort<CS>(sh, err, 115, shape_ok);
+            go = false;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         for (int t = 0; t < ntiles && go; ++t) {
           const int nu = min(C::UNITS, nu_k - t * C::UNITS);
           const uint32_t bytes = a_bytes + (uint32_t)(nu * kUnit * kRowBytes);
@@ -410,7 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = ((active >> c) & 1) && sh.masked[row] != 0;
       const bool any = __ballot_sync(0xffffffffu, valid) != 0u;
       VocabStat st = vs_identity();
-      const float hs = F8 && row < rows ? h_scale[row] : 1.f;   // this row's scale
+      if (F8 && sp.quant_hidden) {                     // the scales are written by other CTAs
+        if (lane == 0 && !wait_ticket(ticket + 3, epoch, rows)) set_abort<CS>(sh, err, 115, shape_ok);
+        __syncwarp();
+      }
+      const float hs = F8 && row < rows ? __ldcg(h_scale + row) : 1.f;   // this row's scale
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
         const int ncol = min(C::UNITS, nu_k - t * C::UNITS) * kUnit;
@@ -491,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned long long armed = (unsigned long long)epoch << 32;
       atomicExch(ticket, armed);
       atomicExch(ticket + 1, armed);
+      atomicExch(ticket + 3, armed);
       atomicExch(ticket + 2, 0ull);
     }
   }
@@ -607,6 +636,12 @@ bool lmhead_tc_supported(const SelectProblem &p) {
 }
 
 bool lmhead_tc_clustered(const SelectProblem &p) { return cluster_size(p) > 1; }
+
+// The FP8-weight LM head quantises the block's hidden rows itself when one CTA row tile holds them
+// and the grid has a CTA for each (the row quantiser kernel is then not launched).
+bool lmhead_tc_quantises_hidden(const SelectProblem &p) {
+  return p.fp8w && cluster_size(p) == 1 && p.batch * p.B <= lmhead_tc_grid(p);
+}
 
 int lmhead_tc_grid(const SelectProblem &p) {
   // vocabulary splits = clusters: as many as can be resident at once (one CTA per SM), at least one

@@ -130,7 +130,8 @@ def fp8_step(*, batch, prompt_len, gen_length, block_size, block_idx, H, V, tau=
 @pytest.mark.parametrize("batch,B,H,V", [
     (1, 32, 256, 5000),      # one 128-row tile, clusters of one
     (1, 7, 128, 3001),       # ragged block, vocabulary not a multiple of the 64-row unit
-    (4, 32, 512, 20000),     # 128 block rows
+    (4, 32, 512, 20000),     # 128 block rows, quantised by the LM-head kernel itself (a CTA per row)
+    (4, 32, 128, 2000),      # 128 rows but only 32 vocabulary splits: the row quantiser kernel first
     (8, 32, 256, 3000),      # 256 rows: clusters of two sharing each W tile
     (16, 32, 128, 2000),     # 512 rows: clusters of four
 ])
