@@ -262,8 +262,8 @@ fdllm_status resolve_select(const fdllm_select_desc *d, SelectProblem &p) {
   return FDLLM_OK;
 }
 
-// workspace: [8-byte arrival ticket, 8-byte start ticket, 8-byte selectors-done count] [partials VocabStat
-// [b * B, splits], 16 bytes each, from byte 256]; the tensor-core kernel serves bf16
+// workspace: [8-byte tickets: arrivals, starts, selectors done, quantised rows] [partials
+// VocabStat [b * B, splits], 16 bytes each, from byte 256]; the tensor-core kernel serves bf16
 // blocks of up to 512 rows (and runs the select itself), the CUDA-core kernel the
 // rest (followed by select_kernel)
 struct SelectLayout {

@@ -505,11 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int sel = sh.arrival - (G - W) - 1;            // selector index, < 0 for the first G - W arrivals
   if (sh.arrival == 0 || sel < 0) return;
   SelectScratch &sc = *(SelectScratch *)tiles;         // the tile ring is free now
-  select_prepare<kThreads>(sp, sel, sc);               // inputs only: overlaps the wait below
+  // the masked positions from the flags this CTA computed at its start: the tokens are not read again
+  select_prepare<kThreads>(sp, sel, sc, sh.masked);    // overlaps the wait below
   if (threadIdx.x == 0 && !wait_ticket(ticket, epoch, G)) record_device_error(err, 107);
   __syncthreads();
   select_finish<kThreads>(sp, part, ncl, sel, sc);
-  for (int seq = sel + W; seq < batch; seq += W) select_sequence<kThreads>(sp, part, ncl, seq, sc);
+  for (int seq = sel + W; seq < batch; seq += W) select_sequence<kThreads>(sp, part, ncl, seq, sc, sh.masked);
   // The last selector to finish re-arms both tickets to (this epoch, 0): every CTA has arrived and
   // every selector has seen the full count, so no one reads them again in this launch.  A launch that
   // repeats this one's parameters (a CUDA graph replay: same epoch) then counts from zero.

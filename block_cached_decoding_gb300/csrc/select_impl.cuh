@@ -62,9 +62,13 @@ __device__ __forceinline__ void store_row(SelectScratch &sc, int j, const VocabS
 
 // The two phases below are called by all NT threads of the CTA (NT >= block
 // size, a multiple of 32).  select_prepare reads only the tokens (an input):
-// this sequence's masked positions, in order, and a cleared scratch.
+// this sequence's masked positions, in order, and a cleared scratch.  A caller
+// that has already compared every block row's token with the mask id passes
+// those flags (`masked`, shared memory, indexed by b * B + i), and the tokens
+// are not read again.
 template <int NT>
-__device__ __forceinline__ void select_prepare(const SelectProblem &p, int b, SelectScratch &sc) {
+__device__ __forceinline__ void select_prepare(const SelectProblem &p, int b, SelectScratch &sc,
+                                               const uint8_t *masked = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = p.B;
   const int sb = seq_block_start(p, b);
@@ -77,7 +81,7 @@ __device__ __forceinline__ void select_prepare(const SelectProblem &p, int b, Se
     int base = 0;
     for (int c = 0; c < B; c += 32) {
       const int i = c + lane;
-      const bool m = sb >= 0 && i < B && trow[i] == p.mask_id;
+      const bool m = sb >= 0 && i < B && (masked ? masked[b * B + i] != 0 : trow[i] == p.mask_id);
       const unsigned bal = __ballot_sync(0xffffffffu, m);
       if (m) sc.mpos[base + __popc(bal & ((1u << lane) - 1u))] = i;
       base += __popc(bal);
@@ -249,8 +253,9 @@ __device__ __forceinline__ void select_finish(const SelectProblem &p, const Voca
 // Both phases for sequence b.
 template <int NT>
 __device__ __forceinline__ void select_sequence(const SelectProblem &p, const VocabStat *__restrict__ part,
-                                                int splits, int b, SelectScratch &sc) {
-  select_prepare<NT>(p, b, sc);
+                                                int splits, int b, SelectScratch &sc,
+                                                const uint8_t *masked = nullptr) {
+  select_prepare<NT>(p, b, sc, masked);
   select_finish<NT>(p, part, splits, b, sc);
 }
 

@@ -144,8 +144,8 @@ typedef struct {
   int32_t dtype;        /* fdllm_dtype of hidden and lm_head_w */
 } fdllm_select_desc;
 
-/* Scratch bytes fdllm_confidence_select needs (three 8-byte ticket words plus the
- * per-split softmax partials of up to batch * block_size rows); 0 on an invalid
+/* Scratch bytes fdllm_confidence_select needs (a 256-byte header of 8-byte ticket
+ * words plus the per-split softmax partials of up to batch * block_size rows); 0 on an invalid
  * descriptor.  The workspace needs no initialisation and may be reused by
  * consecutive calls, but two calls that may run at the same time (different
  * streams) must not share one. */

@@ -126,6 +126,21 @@ def test_many_sequences_per_selector(batch, B, H, V):
              seed=8, premask=pm)
 
 
+@pytest.mark.parametrize("n_masked,strategy,kw", [(0, "threshold", {}), (1, "threshold", {}), (3, "threshold", {}),
+                                                  (9, "factor", dict(factor=0.5)), (32, "topk", dict(topk=5)),
+                                                  (32, "threshold", {})])
+def test_one_sequence_partly_decoded_blocks(n_masked, strategy, kw):
+    """One sequence at every stage of a block (one to 32 masked rows, or none) under each rule: the
+    selector takes the masked positions from the flags the LM-head CTA computed at its start."""
+    rng = np.random.default_rng(40 + n_masked)
+    pm = np.zeros((1, 32), bool)
+    pm[0, rng.choice(32, n_masked, replace=False)] = True
+    info, got = one_step(batch=1, prompt_len=40, gen_length=64, block_size=32, block_idx=1, H=512, V=20000,
+                         dtype="bf16", seed=13, premask=pm, strategy=strategy, **kw)
+    assert got["n_left"][0] == n_masked - got["unmask"][0].sum()
+    assert (got["token"][0] >= 0).sum() == n_masked
+
+
 def test_nothing_masked_anywhere():
     info, got = one_step(batch=2, prompt_len=8, gen_length=32, block_size=32, block_idx=0, H=256, V=1000,
                          dtype="bf16", seed=7, premask=np.zeros((2, 32), bool))
@@ -143,7 +158,7 @@ def _select_outputs(desc, hid, w, tokens0, ws):
 
 
 def test_workspace_needs_no_initialisation_and_can_be_shared():
-    """The workspace holds three ticket words and the softmax partials; whatever it contains on
+    """The workspace holds the ticket words and the softmax partials; whatever it contains on
     entry (all ones, random bytes, another shape's leftovers), the results are the
     same as with a fresh workspace."""
     rng = np.random.default_rng(11)
