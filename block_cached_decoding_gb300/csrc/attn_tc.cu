@@ -89,6 +89,10 @@ struct Plan {
   int nvr;              // tile rows that can hold a query (the rest are padding in every unit)
   int rpc;              // split merge: rows owned per CTA of a cluster (multiple of 8; 128 without a split)
   int nsp;              // ring stages of the K/V pipeline (the ring's last stages receive merged rows)
+  // rows of the suffix's last, partial tile that share the one fresh tile (0: none).  With fewer fresh
+  // rows than a tile, their tile is completed by the suffix's tail (rows [0, nq) fresh, [nq, nq + join)
+  // the last cached rows), so the unit has one key tile less to split over its cluster.
+  int join;
 };
 
 template <int D>
@@ -147,7 +151,7 @@ __device__ __forceinline__ KeyTile key_tile(const Plan &pl, int nq, int n, int k
   if (k < pl.ka) {
     t.range = 0; t.row0 = k * pl.tk; t.nvalid = min(pl.tk, pl.f0 - t.row0);
   } else if (k < pl.ka + pl.kf) {
-    t.range = 1; t.row0 = (k - pl.ka) * pl.tk; t.nvalid = min(pl.tk, nq - t.row0);
+    t.range = 1; t.row0 = (k - pl.ka) * pl.tk; t.nvalid = min(pl.tk, nq - t.row0) + pl.join;
   } else {
     const int r2 = (k - pl.ka - pl.kf) * pl.tk;    // row within the suffix
     t.range = 2; t.row0 = (pl.abs_suffix ? pl.f1 : 0) + r2; t.nvalid = min(pl.tk, n - pl.f1 - r2);
@@ -285,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap mkf, const __grid_constant__ CUtensorMap mkc,
                    const __grid_constant__ CUtensorMap mva, const __grid_constant__ CUtensorMap mvf,
                    const __grid_constant__ CUtensorMap mvc,
-                   const __grid_constant__ CUtensorMap mwk, const __grid_constant__ CUtensorMap mwv, const Args a) {
+                   const __grid_constant__ CUtensorMap mwk, const __grid_constant__ CUtensorMap mwv,
+                   const __grid_constant__ CUtensorMap mkt, const __grid_constant__ CUtensorMap mvt, const Args a) {
   using CF = Cfg<D>;
   constexpr int NS = CF::NS;
   constexpr int TK = kKeys / KVP;                      // keys of one KV head in a key tile
@@ -341,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C > 1) tc::mbar_arrive_expect_tx(&br.mrg, (uint32_t)((C - 1) * seg_rows(crank) * (CF::RB + 8)));
     for (const CUtensorMap *m : {&mq, &mka, &mkf, &mkc, &mva, &mvf, &mvc}) tc::prefetch_tensormap(m);
     if (a.win_box > 0) { tc::prefetch_tensormap(&mwk); tc::prefetch_tensormap(&mwv); }
+    if (pl.join > 0) { tc::prefetch_tensormap(&mkt); tc::prefetch_tensormap(&mvt); }
   }
   if (warp == 1) tc::tmem_alloc(&br.tmem_base, CF::TMEM_COLS);
   // Launched as a programmatic dependent: everything above overlaps the previous kernel in the
@@ -417,6 +423,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int off = dh * CF::KVHALF;        // (64 / KVP) keys, head-major, in one box
             tc::tma_load_4d(ks + off, mk, &br.kvfull[st], dh * 64, kt.row0, kvh, b, pol_kv);
             tc::tma_load_4d(ks + CF::KV_BYTES + off, mv, &br.kvfull[st], dh * 64, kt.row0, kvh, b, pol_kv);
+            if (kt.range == 1 && pl.join > 0) {
+              // the joined tile: the nq fresh rows (a box of nq rows) then the suffix's tail (a box of the
+              // remaining tk - nq rows from its last, partial tile; rows past the cache read as zeros)
+              const int ro = a.nq * 128;           // a multiple of 1024 bytes: the swizzle atoms line up
+              tc::tma_load_4d(ks + off + ro, &mkt, &br.kvfull[st], dh * 64, pl.kcn * pl.tk, kvh, b, pol_kv);
+              tc::tma_load_4d(ks + CF::KV_BYTES + off + ro, &mvt, &br.kvfull[st], dh * 64, pl.kcn * pl.tk, kvh, b,
+                              pol_kv);
+            }
           }
         }
         atomicExch(&br.issued, i + 1);
@@ -943,6 +957,16 @@ Plan make_plan(const AttnProblem &p) {
   pl.kf = (p.nq + pl.tk - 1) / pl.tk;
   pl.kcn = (p.seq_len - pl.f1 + pl.tk - 1) / pl.tk;
   pl.kt = pl.ka + pl.kf + pl.kcn;
+  // fewer fresh rows than a tile, and the suffix's last tile short enough to complete theirs: one joined
+  // tile (single-head tiles of a bf16 cache, blocks at the same position in every sequence)
+  pl.join = 0;
+  const int suffix = p.seq_len - pl.f1;
+  if (pl.kvp == 1 && !p.f8kv && p.blocks == nullptr && p.nq < pl.tk && p.nq % 8 == 0 && suffix > 0 &&
+      suffix % pl.tk > 0 && p.nq + suffix % pl.tk <= pl.tk) {
+    pl.join = suffix % pl.tk;
+    pl.kcn = suffix / pl.tk;
+    pl.kt = pl.ka + pl.kf + pl.kcn;
+  }
   if (pl.kvp > 1) {
     pl.qr = kTile / pl.kvp;
     pl.ht = pl.kvp;
@@ -1013,7 +1037,7 @@ cudaError_t launch_d(const Plan &pl, const CUtensorMap *maps, const Args &a, cud
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], maps[8],
-                         a);
+                         maps[9], maps[10], a);
   count_launches(1);
   return e;
 }
@@ -1046,7 +1070,7 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t cstride = (int64_t)p.seq_len * p.hkv * p.d;  // cache batch stride
   const int64_t fstride = (int64_t)p.nq * p.hkv * p.d;       // fresh batch stride
   const int64_t qstride = (int64_t)p.nq * p.hq * p.d;
-  CUtensorMap maps[9];
+  CUtensorMap maps[11];
   const __nv_bfloat16 *kc = (const __nv_bfloat16 *)p.kc, *vc = (const __nv_bfloat16 *)p.vc;
   // per-sequence blocks: prefix and suffix tiles are read through maps of the whole cache; rows of a
   // sequence's own window that fall in a boundary tile are read and weighted by exactly zero
@@ -1054,9 +1078,11 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
   const int64_t off_c = per_seq ? 0 : (int64_t)pl.f1 * p.hkv * p.d;
   const int rows_a = per_seq ? p.seq_len : pl.f0, rows_c = per_seq ? p.seq_len : p.seq_len - pl.f1;
   const int kvp = pl.kvp;
+  // a joined tile reads the fresh rows as one box of nq rows
+  const int fbox = pl.join > 0 ? p.nq : pl.tk;
   bool ok = map4(&maps[0], p.q, p.d, p.hq, p.nq, p.batch, qstride, pl.qr) &&
-            map4_kv(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false) &&
-            map4_kv(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, pl.tk, kvp, false);
+            map4_kv(&maps[2], p.kf, p.d, p.hkv, p.nq, p.batch, fstride, fbox, kvp, false) &&
+            map4_kv(&maps[5], p.vf, p.d, p.hkv, p.nq, p.batch, fstride, fbox, kvp, false);
   if (p.f8kv) {   // the cache as E4M3 codes (one byte per element)
     const uint8_t *kq = (const uint8_t *)p.kc, *vq = (const uint8_t *)p.vc;
     ok = ok && map4_kv(&maps[1], kq, p.d, p.hkv, rows_a, p.batch, cstride, pl.tk, kvp, true) &&
@@ -1078,6 +1104,12 @@ cudaError_t launch_attn_tc(const AttnProblem &p, cudaStream_t st) {
            map4_kv(&maps[8], p.vc_w, p.d, p.hkv, p.seq_len, p.batch, cstride, win_box, kvp, false);
   }
   if (win_box == 0) maps[7] = maps[8] = maps[1];
+  // the joined tile's suffix rows: the suffix maps with boxes of tk - nq rows (unused copies otherwise)
+  if (pl.join > 0)
+    ok = ok && map4_kv(&maps[9], kc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk - p.nq, kvp, false) &&
+         map4_kv(&maps[10], vc + off_c, p.d, p.hkv, rows_c, p.batch, cstride, pl.tk - p.nq, kvp, false);
+  else
+    maps[9] = maps[10] = maps[3];
   if (!ok) return cudaErrorInvalidValue;
   Args a;
   a.win = p.update ? p.win : 0;

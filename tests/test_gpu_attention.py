@@ -74,6 +74,20 @@ def test_mha_heads_packed_per_tile(batch, hq, d, block, prompt, gen, out_f32):
              mode="dual", dtype="bf16", seed=9, out_f32=out_f32)
 
 
+@pytest.mark.parametrize("prompt,gen,block,k,hq,hkv,d", [
+    (100, 64, 16, 0, 4, 4, 128),     # 16 fresh rows + the suffix's last 48: one full joined tile
+    (100, 32, 16, 0, 4, 4, 64),      # 16 fresh + 16 suffix rows; the rest of the joined tile past the cache
+    (64, 128, 8, 1, 8, 2, 128),      # 8 fresh + 48 suffix rows, grouped-query heads
+    (40, 192, 48, 1, 4, 4, 128),     # 48 fresh + 32 suffix rows do not fit one tile: no joined tile
+    (200, 96, 32, 1, 28, 4, 128)])   # the Dream head layout, 32 + 32 rows
+def test_dual_fresh_tile_joined_with_suffix_tail(prompt, gen, block, k, hq, hkv, d):
+    """DualCache with fewer fresh rows than a key tile: when the suffix's last, partial tile fits
+    beside them, both share one tile (the fresh rows, then the cached tail), so the unit has one key
+    tile less; the attention over every position must not change."""
+    run_case(batch=3, prompt_len=prompt, gen_length=gen, block_size=block, block_idx=k, hq=hq, hkv=hkv, d=d,
+             mode="dual", dtype="bf16", seed=12, out_f32=0)
+
+
 @pytest.mark.parametrize("hq,hkv", [(28, 4), (8, 1), (6, 2)])
 def test_bf16_gqa(hq, hkv):
     run_case(batch=2, prompt_len=130, gen_length=64, block_size=32, block_idx=0, hq=hq, hkv=hkv, d=128,
