@@ -140,6 +140,26 @@ __device__ __forceinline__ void group_bar(int g) { asm volatile("bar.sync %0, 12
 // The softmax warps and warp 3, which sends the split merge's rows once the softmax warps have staged them.
 __device__ __forceinline__ void send_bar() { asm volatile("bar.sync 9, 288;" ::: "memory"); }
 
+// The maximum of m[0, LEN) by three-input maxima, level by level in place (LEN / 2 instructions for LEN
+// a power of two): every index is known at compile time, so the array stays in registers.
+template <int LEN, int CAP>
+struct Max3Tree {
+  static __device__ __forceinline__ float run(float (&m)[CAP]) {
+    constexpr int OUT = (LEN + 2) / 3;
+#pragma unroll
+    for (int e = 0; e < OUT; ++e) {
+      if (3 * e + 2 < LEN) m[e] = tc::max3(m[3 * e], m[3 * e + 1], m[3 * e + 2]);
+      else if (3 * e + 1 < LEN) m[e] = fmaxf(m[3 * e], m[3 * e + 1]);
+      else m[e] = m[3 * e];
+    }
+    return Max3Tree<OUT, CAP>::run(m);
+  }
+};
+template <int CAP>
+struct Max3Tree<1, CAP> {
+  static __device__ __forceinline__ float run(float (&m)[CAP]) { return m[0]; }
+};
+
 struct KeyTile {
   int range;   // 0 prefix cache, 1 fresh, 2 suffix cache
   int row0;    // first row within the range's map
@@ -185,7 +205,8 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w, float sc) {
   for (int h = 0; h < 2; ++h) {
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> (16 * h)), __NV_E4M3);
     const float2 f = __half22float2(*(const __half2 *)&hr);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+    const float2 g = tc::f2_unpack(tc::f2_mul(tc::f2_pack(f.x, f.y), tc::f2_pack(sc, sc)));   // both lanes at once
+    const __nv_bfloat162 b = __floats2bfloat162_rn(g.x, g.y);
     o[h] = *(const uint32_t *)&b;
   }
   return make_uint2(o[0], o[1]);
@@ -637,8 +658,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_ld_32x32b_x16(s_col, xr);
         }
         tc::tmem_ld_wait();
+        if (nv >= TK) {                                // a full tile: no per-key validity test
 #pragma unroll
-        for (int e = 0; e < TK; ++e) x[e] = e < nv ? __uint_as_float(xr[e]) : kNegInf;
+          for (int e = 0; e < TK; ++e) x[e] = __uint_as_float(xr[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < TK; ++e) x[e] = e < nv ? __uint_as_float(xr[e]) : kNegInf;
+        }
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -658,15 +684,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_proxy_async_smem();
         }
       }
-      // row max over the valid keys, lazy reference max
-      float mx[TK / 2];
+      // row max over the valid keys (three-input maxima: a tree of TK / 2 instructions), lazy reference max
+      float mx[TK];
 #pragma unroll
-      for (int e = 0; e < TK / 2; ++e) mx[e] = fmaxf(x[e], x[e + TK / 2]);
-#pragma unroll
-      for (int w2 = TK / 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-        for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
-      const float tm = mx[0];
+      for (int e = 0; e < TK; ++e) mx[e] = x[e];
+      const float tm = Max3Tree<TK, TK>::run(mx);
       // the group's previous PV product has read P_g and finished updating O_g
       if (u > 0 && !tc::mbar_wait_or_abort(&br.pvdone[g], (uint32_t)(u - 1) & 1u, abort_flag)) {
         if (!*abort_flag) fail(br, a.err, 219);
@@ -694,13 +716,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ms = m_run * sl2;
       uint32_t pw[TK / 2];
       float lt[4] = {0.f, 0.f, 0.f, 0.f};             // four independent partial sums
+      if (nv >= TK) {
+        // key pairs: one paired fma for both exponents' arguments, one paired add into two running sums
+        const uint64_t sc2 = tc::f2_pack(sl2, sl2), ms2 = tc::f2_pack(-ms, -ms);
+        uint64_t acc[2] = {tc::f2_pack(0.f, 0.f), tc::f2_pack(0.f, 0.f)};
 #pragma unroll
-      for (int e = 0; e < TK / 2; ++e) {
-        const float p0 = 2 * e < nv ? tc::ex2_approx(fmaf(x[2 * e], sl2, -ms)) : 0.f;
-        const float p1 = 2 * e + 1 < nv ? tc::ex2_approx(fmaf(x[2 * e + 1], sl2, -ms)) : 0.f;
-        lt[e & 3] += p0 + p1;
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        pw[e] = *(uint32_t *)&h2;
+        for (int e = 0; e < TK / 2; ++e) {
+          const float2 ar = tc::f2_unpack(tc::f2_fma(tc::f2_pack(x[2 * e], x[2 * e + 1]), sc2, ms2));
+          const float p0 = tc::ex2_approx(ar.x), p1 = tc::ex2_approx(ar.y);
+          acc[e & 1] = tc::f2_add(acc[e & 1], tc::f2_pack(p0, p1));
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pw[e] = *(uint32_t *)&h2;
+        }
+        const float2 s0 = tc::f2_unpack(acc[0]), s1 = tc::f2_unpack(acc[1]);
+        lt[0] = s0.x; lt[1] = s0.y; lt[2] = s1.x; lt[3] = s1.y;
+      } else {
+#pragma unroll
+        for (int e = 0; e < TK / 2; ++e) {
+          const float p0 = 2 * e < nv ? tc::ex2_approx(fmaf(x[2 * e], sl2, -ms)) : 0.f;
+          const float p1 = 2 * e + 1 < nv ? tc::ex2_approx(fmaf(x[2 * e + 1], sl2, -ms)) : 0.f;
+          lt[e & 3] += p0 + p1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pw[e] = *(uint32_t *)&h2;
+        }
       }
       l_run += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       if constexpr (TK == 64) tc::tmem_st_32x32b_x32(p_col, *(const uint32_t(*)[32])&pw[0]);
