@@ -684,7 +684,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_proxy_async_smem();
         }
       }
-      // row max over the valid keys (three-input maxima: a tree of TK / 2 instructions), lazy reference max
+      // P = 2^(S scale log2(e) - ms) into pw (bf16 pairs) and its four partial row sums into lt
+      uint32_t pw[TK / 2];
+      float lt[4];
+      auto exps = [&](float ms) {
+        if (nv >= TK) {
+          // key pairs: one paired fma for both exponents' arguments, one paired add into two running sums
+          const uint64_t sc2 = tc::f2_pack(sl2, sl2), ms2 = tc::f2_pack(-ms, -ms);
+          uint64_t acc[2] = {tc::f2_pack(0.f, 0.f), tc::f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int e = 0; e < TK / 2; ++e) {
+            const float2 ar = tc::f2_unpack(tc::f2_fma(tc::f2_pack(x[2 * e], x[2 * e + 1]), sc2, ms2));
+            const float p0 = tc::ex2_approx(ar.x), p1 = tc::ex2_approx(ar.y);
+            acc[e & 1] = tc::f2_add(acc[e & 1], tc::f2_pack(p0, p1));
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            pw[e] = *(uint32_t *)&h2;
+          }
+          const float2 s0 = tc::f2_unpack(acc[0]), s1 = tc::f2_unpack(acc[1]);
+          lt[0] = s0.x; lt[1] = s0.y; lt[2] = s1.x; lt[3] = s1.y;
+        } else {
+          lt[0] = lt[1] = lt[2] = lt[3] = 0.f;
+#pragma unroll
+          for (int e = 0; e < TK / 2; ++e) {
+            const float p0 = 2 * e < nv ? tc::ex2_approx(fmaf(x[2 * e], sl2, -ms)) : 0.f;
+            const float p1 = 2 * e + 1 < nv ? tc::ex2_approx(fmaf(x[2 * e + 1], sl2, -ms)) : 0.f;
+            lt[e & 3] += p0 + p1;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            pw[e] = *(uint32_t *)&h2;
+          }
+        }
+      };
+      // After the first tile the reference max rarely moves, so P is computed against it at once, beside
+      // the row max (three-input maxima: a tree of TK / 2 instructions), and before the wait for the
+      // previous PV product, which only the store of P and a rescale need; a tile whose max does move
+      // the reference is computed again below.
+      if (u > 0) exps(m_run * sl2);
       float mx[TK];
 #pragma unroll
       for (int e = 0; e < TK; ++e) mx[e] = x[e];
@@ -696,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       const bool need = m_run == kNegInf || (tm - m_run) * sl2 > 8.f;
-      if (__any_sync(0xffffffffu, need)) {
+      if (u == 0 || __any_sync(0xffffffffu, need)) {
         const float m_new = need ? fmaxf(m_run, tm) : m_run;
         const float al = tc::ex2_approx((m_run - m_new) * sl2);   // 0 on a row's first tile
         if (u > 0) {
@@ -712,33 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         l_run *= al;
         m_run = m_new;
-      }
-      const float ms = m_run * sl2;
-      uint32_t pw[TK / 2];
-      float lt[4] = {0.f, 0.f, 0.f, 0.f};             // four independent partial sums
-      if (nv >= TK) {
-        // key pairs: one paired fma for both exponents' arguments, one paired add into two running sums
-        const uint64_t sc2 = tc::f2_pack(sl2, sl2), ms2 = tc::f2_pack(-ms, -ms);
-        uint64_t acc[2] = {tc::f2_pack(0.f, 0.f), tc::f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int e = 0; e < TK / 2; ++e) {
-          const float2 ar = tc::f2_unpack(tc::f2_fma(tc::f2_pack(x[2 * e], x[2 * e + 1]), sc2, ms2));
-          const float p0 = tc::ex2_approx(ar.x), p1 = tc::ex2_approx(ar.y);
-          acc[e & 1] = tc::f2_add(acc[e & 1], tc::f2_pack(p0, p1));
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pw[e] = *(uint32_t *)&h2;
-        }
-        const float2 s0 = tc::f2_unpack(acc[0]), s1 = tc::f2_unpack(acc[1]);
-        lt[0] = s0.x; lt[1] = s0.y; lt[2] = s1.x; lt[3] = s1.y;
-      } else {
-#pragma unroll
-        for (int e = 0; e < TK / 2; ++e) {
-          const float p0 = 2 * e < nv ? tc::ex2_approx(fmaf(x[2 * e], sl2, -ms)) : 0.f;
-          const float p1 = 2 * e + 1 < nv ? tc::ex2_approx(fmaf(x[2 * e + 1], sl2, -ms)) : 0.f;
-          lt[e & 3] += p0 + p1;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          pw[e] = *(uint32_t *)&h2;
-        }
+        exps(m_run * sl2);
       }
       l_run += (lt[0] + lt[1]) + (lt[2] + lt[3]);
       if constexpr (TK == 64) tc::tmem_st_32x32b_x32(p_col, *(const uint32_t(*)[32])&pw[0]);
