@@ -4,7 +4,8 @@
 // that no row outside a range is ever read: the cached prefix [0, f0), the fresh
 // keys of this step (nq rows, the query positions) and the cached suffix
 // [f1, N).  Softmax is invariant to the order of the keys, so the key tiles of
-// 64 rows are enumerated range by range.
+// 64 rows are enumerated range by range; with fewer fresh rows than a tile, the
+// suffix's last, partial tile may complete the fresh one (a joined tile).
 //
 // One CTA = (sequence, KV head, 128-row query tile, split of the key tiles);
 // all query heads sharing the KV head are packed into the 128 rows when
@@ -27,7 +28,9 @@
 //              exceeds it by more than 2^8, and then O_g's row and l are
 //              rescaled in TMEM after the group's previous PV product has
 //              landed), P = 2^((S - m_ref) * scale * log2 e) stored as bf16 to
-//              TMEM.  Each group keeps its own (m, l, O_g); while one group
+//              TMEM (after a group's first tile computed against the current
+//              reference before the row max is known, and again if it moves).
+//              Each group keeps its own (m, l, O_g); while one group
 //              computes its softmax the tensor core works on the other's tile.
 // At the end the two groups' rows are combined in the CTA.  Splits of one unit
 // form a thread block cluster (<= 8) and merge through distributed shared
