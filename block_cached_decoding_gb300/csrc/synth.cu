@@ -64,7 +64,9 @@ __device__ __forceinline__ uint64_t row_key(uint64_t seed, int kind, int b, int6
                   (uint64_t)pos);
 }
 
-// rows [b, npos, width]: grid (npos, b); the step is step + *step_add when step_add is given (a device
+constexpr int kRowChunk = 512;   // row elements per CTA (grid z): short row batches still fill the GPU
+
+// rows [b, npos, width]: grid (npos, b, row chunks); the step is step + *step_add when step_add is given (a device
 // counter, e.g. a graph loop's); per-sequence steps and first positions when step_seq / pos_seq are given
 template <typename T>
 __global__ void rows_kernel(uint64_t seed, int kind, int64_t step, const int64_t *step_add, int pos0, int npos,
@@ -76,7 +78,8 @@ __global__ void rows_kernel(uint64_t seed, int kind, int64_t step, const int64_t
   if (pos_seq != nullptr) pos0 = pos_seq[b];
   const uint64_t key = row_key(seed, kind, b, step, pos0 + p);
   T *row = out + ((int64_t)b * npos + p) * width;
-  for (int i = threadIdx.x; i < width; i += blockDim.x)
+  const int i1 = min(width, ((int)blockIdx.z + 1) * kRowChunk);
+  for (int i = (int)blockIdx.z * kRowChunk + threadIdx.x; i < i1; i += blockDim.x)
     store(row + i, __fmul_rn(normal12(key, (uint64_t)i), sigma));
 }
 
@@ -93,7 +96,8 @@ __global__ void hidden_kernel(uint64_t seed, int64_t step, const int64_t *step_a
   const int64_t target = (int64_t)(((splitmix(pk, 1) >> 32) * (uint64_t)vocab) >> 32);
   const uint64_t key = row_key(seed, FDLLM_SYNTH_HID, b, step, pos0 + p);
   T *row = out + ((int64_t)b * npos + p) * hidden;
-  for (int i = threadIdx.x; i < hidden; i += blockDim.x) {
+  const int i1 = min(hidden, ((int)blockIdx.z + 1) * kRowChunk);
+  for (int i = (int)blockIdx.z * kRowChunk + threadIdx.x; i < i1; i += blockDim.x) {
     float z = normal12(key, (uint64_t)i);
     if (planted) z = __fadd_rn(z, __fmul_rn(6.0f, to_f32(w[target * hidden + i])));
     store(row + i, z);
@@ -171,11 +175,11 @@ extern "C" int32_t fdllm_synth_rows(uint64_t seed, int32_t kind, int32_t batch, 
 extern "C" int32_t fdllm_synth_rows_at(uint64_t seed, int32_t kind, int32_t batch, int64_t step,
                                        const int64_t *step_add, int32_t pos0, int32_t npos, int32_t width,
                                        float sigma, int32_t dtype, void *out, fdllm_stream_t stream) {
-  if (batch < 1 || batch > 65535 || npos < 0 || width < 1 || (npos > 0 && !out) ||
+  if (batch < 1 || batch > 65535 || npos < 0 || width < 1 || width > 65535 * kRowChunk || (npos > 0 && !out) ||
       (dtype != FDLLM_BF16 && dtype != FDLLM_F32))
     return FDLLM_EINVAL;
   if (npos == 0) return FDLLM_OK;
-  dim3 grid(npos, batch);
+  dim3 grid(npos, batch, (width + kRowChunk - 1) / kRowChunk);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
     rows_kernel<<<grid, 128, 0, st>>>(seed, kind, step, step_add, pos0, npos, width, sigma, (__nv_bfloat16 *)out);
@@ -194,13 +198,13 @@ extern "C" int32_t fdllm_synth_hidden(uint64_t seed, int32_t batch, int64_t step
 extern "C" int32_t fdllm_synth_hidden_at(uint64_t seed, int32_t batch, int64_t step, const int64_t *step_add,
                                          int32_t pos0, int32_t npos, int32_t hidden, int32_t vocab, double p_plant,
                                          const void *w, int32_t dtype, void *out, fdllm_stream_t stream) {
-  if (batch < 1 || batch > 65535 || npos < 0 || hidden < 1 || vocab < 1 || !w ||
+  if (batch < 1 || batch > 65535 || npos < 0 || hidden < 1 || hidden > 65535 * kRowChunk || vocab < 1 || !w ||
       (npos > 0 && !out) || (dtype != FDLLM_BF16 && dtype != FDLLM_F32) || !(p_plant >= 0.0))
     return FDLLM_EINVAL;
   if (npos == 0) return FDLLM_OK;
   // plant iff (draw >> 40) < floor(p * 2^24), as on the host
   const uint64_t thr = (uint64_t)floor(p_plant * (double)(1 << 24));
-  dim3 grid(npos, batch);
+  dim3 grid(npos, batch, (hidden + kRowChunk - 1) / kRowChunk);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
     hidden_kernel<<<grid, 128, 0, st>>>(seed, step, step_add, pos0, npos, hidden, vocab, thr,
@@ -214,11 +218,12 @@ extern "C" int32_t fdllm_synth_hidden_at(uint64_t seed, int32_t batch, int64_t s
 extern "C" int32_t fdllm_synth_rows_seq(uint64_t seed, int32_t kind, int32_t batch, const int32_t *step,
                                         const int32_t *pos0, int32_t npos, int32_t width, float sigma, int32_t dtype,
                                         void *out, fdllm_stream_t stream) {
-  if (batch < 1 || batch > 65535 || npos < 0 || width < 1 || !step || !pos0 || (npos > 0 && !out) ||
+  if (batch < 1 || batch > 65535 || npos < 0 || width < 1 || width > 65535 * kRowChunk || !step || !pos0 ||
+      (npos > 0 && !out) ||
       (dtype != FDLLM_BF16 && dtype != FDLLM_F32))
     return FDLLM_EINVAL;
   if (npos == 0) return FDLLM_OK;
-  dim3 grid(npos, batch);
+  dim3 grid(npos, batch, (width + kRowChunk - 1) / kRowChunk);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
     rows_kernel<<<grid, 128, 0, st>>>(seed, kind, 0, nullptr, 0, npos, width, sigma, (__nv_bfloat16 *)out, step,
@@ -231,12 +236,13 @@ extern "C" int32_t fdllm_synth_rows_seq(uint64_t seed, int32_t kind, int32_t bat
 extern "C" int32_t fdllm_synth_hidden_seq(uint64_t seed, int32_t batch, const int32_t *step, const int32_t *pos0,
                                           int32_t npos, int32_t hidden, int32_t vocab, double p_plant, const void *w,
                                           int32_t dtype, void *out, fdllm_stream_t stream) {
-  if (batch < 1 || batch > 65535 || npos < 0 || hidden < 1 || vocab < 1 || !w || !step || !pos0 ||
+  if (batch < 1 || batch > 65535 || npos < 0 || hidden < 1 || hidden > 65535 * kRowChunk || vocab < 1 || !w ||
+      !step || !pos0 ||
       (npos > 0 && !out) || (dtype != FDLLM_BF16 && dtype != FDLLM_F32) || !(p_plant >= 0.0))
     return FDLLM_EINVAL;
   if (npos == 0) return FDLLM_OK;
   const uint64_t thr = (uint64_t)floor(p_plant * (double)(1 << 24));
-  dim3 grid(npos, batch);
+  dim3 grid(npos, batch, (hidden + kRowChunk - 1) / kRowChunk);
   cudaStream_t st = (cudaStream_t)stream;
   if (dtype == FDLLM_BF16)
     hidden_kernel<<<grid, 128, 0, st>>>(seed, 0, nullptr, 0, npos, hidden, vocab, thr, (const __nv_bfloat16 *)w,

@@ -56,7 +56,8 @@ int32_t fdllm_synth_kv_cache_at(uint64_t seed, int32_t kind, int32_t batch, int3
                                 int32_t head_dim, int64_t epoch, const int64_t *epoch_add, int64_t epoch_div,
                                 float sigma, int32_t dtype, void *out, fdllm_stream_t stream);
 
-/* Per-position rows: out [b, npos, width]; row (b, p) uses key (seed, kind, b, step, pos0 + p). */
+/* Per-position rows: out [b, npos, width]; row (b, p) uses key (seed, kind, b, step, pos0 + p).
+ * width (and hidden below) at most 65535 * 512; FDLLM_EINVAL otherwise. */
 int32_t fdllm_synth_rows(uint64_t seed, int32_t kind, int32_t batch, int64_t step, int32_t pos0,
                          int32_t npos, int32_t width, float sigma, int32_t dtype, void *out,
                          fdllm_stream_t stream);
