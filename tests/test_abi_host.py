@@ -184,3 +184,17 @@ def test_block_loop_validates_on_the_host(lib):
     assert lib.fdllm_block_loop_create(C.byref(h), cb, None, v, 1, 0, v, None) == F.EINVAL
     assert lib.fdllm_block_loop_create(C.byref(h), cb, None, v, 1, 4, None, None) == F.EINVAL
     assert lib.fdllm_block_loop_launch(None, None) == F.EINVAL
+
+
+def test_synth_generators_validate_on_the_host(lib):
+    """The seeded input generators reject shapes their launch cannot cover (a row of more than
+    65535 chunks of 512 elements, more than 65535 sequences) and missing pointers before any launch."""
+    v = C.c_void_p(16)
+    assert lib.fdllm_synth_rows(1, 2, 1, 0, 0, 4, 65535 * 512 + 1, 1.0, F.BF16, v, None) == F.EINVAL
+    assert lib.fdllm_synth_rows(1, 2, 65536, 0, 0, 4, 64, 1.0, F.BF16, v, None) == F.EINVAL
+    assert lib.fdllm_synth_rows(1, 2, 1, 0, 0, 4, 64, 1.0, 7, v, None) == F.EINVAL
+    assert lib.fdllm_synth_rows(1, 2, 1, 0, 0, 4, 64, 1.0, F.BF16, None, None) == F.EINVAL
+    assert lib.fdllm_synth_rows(1, 2, 1, 0, 0, 0, 64, 1.0, F.BF16, None, None) == F.OK   # nothing to draw
+    assert lib.fdllm_synth_hidden(1, 1, 0, 0, 4, 65535 * 512 + 1, 100, 0.5, v, F.BF16, v, None) == F.EINVAL
+    assert lib.fdllm_synth_hidden(1, 1, 0, 0, 4, 64, 100, -0.5, v, F.BF16, v, None) == F.EINVAL
+    assert lib.fdllm_synth_hidden(1, 1, 0, 0, 4, 64, 100, 0.5, None, F.BF16, v, None) == F.EINVAL
